@@ -1,0 +1,53 @@
+"""Acceptance criteria for an emulated-FP32 GEMM result (test infrastructure).
+
+The pages say that BF16x9 matches or beats native FP32 accuracy against an
+FP64 reference ("Unlocking Tensor Core Performance for Machine Learning
+Interatomic Potentials", section "Limitations and decision criteria"); the
+criteria below make that concrete:
+
+* element-wise, with u = 2^-24 (unit roundoff of FP32):
+      |C - C_ref| <= (2K + 2) u |alpha| S_abs + 2 u |beta C0| + (9K + 4) 2^-149
+  where S_abs = sum_k |a_mk||b_kn|.  2K u |alpha| S_abs is the worst case of a
+  K-term FP32 accumulation (one rounding per step, each at most u times the
+  running magnitude); the 2u terms cover the two roundings of the epilogue
+  alpha*acc + beta*C0; the last term covers products and partial sums that
+  land among FP32 subnormals (absolute spacing 2^-149).
+* TF32x3 drops the residual*residual product and its residual is itself
+  rounded to TF32, which costs at most 3 * 2^-22 |a||b| < 2^-20 |a||b| per
+  product, so its bound adds 2^-20 |alpha| S_abs.
+* relative Frobenius error ||C - C_ref||_F / ||C_ref||_F <= 2e-6 on
+  normally distributed inputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+U = 2.0 ** -24
+SUB = 2.0 ** -149
+FROBENIUS_TOL = 2e-6
+
+
+def elementwise_bound(K, alpha, beta, Sabs, C0=None, mode="bf16x9"):
+    base = (2 * K + 2) * U
+    if mode == "tf32x3":
+        base += 2.0 ** -20
+    b = base * abs(float(alpha)) * np.asarray(Sabs, np.float64)
+    if beta != 0.0:
+        b = b + 2 * U * abs(float(beta)) * np.abs(np.asarray(C0, np.float64))
+    return b + (9 * K + 4) * SUB
+
+
+def error_ratio(C, Cref, Sabs, K, alpha, beta, C0=None, mode="bf16x9"):
+    """max |C - C_ref| / bound; the result passes when this is <= 1."""
+    err = np.abs(np.asarray(C, np.float64) - np.asarray(Cref, np.float64))
+    bound = elementwise_bound(K, alpha, beta, Sabs, C0, mode)
+    if err.size == 0:
+        return 0.0
+    return float(np.max(err / bound))
+
+
+def rel_frobenius(C, Cref):
+    Cref = np.asarray(Cref, np.float64)
+    d = np.asarray(C, np.float64) - Cref
+    den = np.linalg.norm(Cref)
+    return float(np.linalg.norm(d) / den) if den > 0 else float(np.linalg.norm(d))
