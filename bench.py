@@ -1,0 +1,401 @@
+"""Benchmark of the emulated-FP32 GEMM on GB300: prints one JSON line.
+
+Metric: effective FP32 TFLOP/s = 2MNK / t, also as a fraction of the dense
+BF16 tensor peak / 9 (nine BF16 products per emulated FP32 product).  A step
+is one emu_sgemm call -- the whole hot path: split of A, split of B, the
+tensor-core GEMM with its epilogue -- on inputs already resident in HBM.
+
+Default workload: C = A B with A, B 8192 x 8192 drawn from N(0, 1), BF16x9,
+beta = 0 (the size at which the method's square-GEMM speedups are quoted).
+Each operand is 256 MiB, larger than the 129 MB L2, so no flush is needed
+between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--mode bf16x9|tf32x3|fp32_simt] [--impl reference]
+
+--impl reference times the CPU oracle (the plain reference implementation of
+the method) on the host cores, on a bounded block of rows of the same
+workload, and prints the same metric.  Under torchrun (N > 1) every rank runs
+an independent replica on its own GPU (the GEMM does not exchange data);
+value is the total over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "emulated-FP32 GEMM TFLOP/s (2MNK/t) and % of BF16 dense peak/9 on 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows),
+                "samples": len(loaded),
+                "reasons": reasons}
+
+
+# ------------------------------------------------------------- GPU arm --
+
+def bench_gpu(args):
+    import numpy as np
+    import torch
+
+    from fp32_emulated_gemm_split_gb300 import _build
+    from fp32_emulated_gemm_split_gb300 import workloads as W
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    _build.build()
+    import fp32_emulated_gemm_split_gb300 as emu
+
+    g = W.with_mode(W.WORKLOADS[args.workload], args.mode or W.WORKLOADS[args.workload].mode)
+    A, B, C0 = W.generate(g)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.from_numpy(C0).cuda() if C0 is not None else torch.empty((g.M, g.N), device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        emu.emu_sgemm(dA, dB, dC, transA=g.transA, transB=g.transB, alpha=g.alpha, beta=g.beta,
+                      mode=g.mode, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    emu.emu_profile_enable(True)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    ms_total = start.elapsed_time(stop)
+    prof = {k: emu.emu_profile_read(k) for k in ("split", "gemm_tc", "gemm_fused", "gemm_simt", "scale")}
+    emu.emu_profile_enable(False)
+    assert emu.emu_get_last_device_error() == 0, "device-side wait gave up during the bench"
+
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    ms_step = ms_total / args.steps
+    flops = g.flops
+    value = flops * world * args.steps / (ms_total * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    p_bf16 = float(peaks["bf16_tflops"])
+    frac9 = value / world / (p_bf16 / 9.0)
+
+    # dominant kernel: the tensor-core GEMM (or the SIMT kernel in that mode)
+    launches = sum(n for n, _ in prof.values())
+    if g.mode == "fp32_simt":
+        dom_name, (n_dom, ms_dom) = "gemm_simt", prof["gemm_simt"]
+    elif prof["gemm_fused"][0] > 0:
+        dom_name, (n_dom, ms_dom) = "gemm_fused", prof["gemm_fused"]
+    else:
+        dom_name, (n_dom, ms_dom) = "gemm_tc", prof["gemm_tc"]
+    per_launch_ms = ms_dom / max(n_dom, 1)
+    products = {"bf16x9": 9, "tf32x3": 3, "fp32_simt": 1}[g.mode]
+    if g.mode == "fp32_simt":
+        roofline = {"bound": "alu", "achieved": flops / (per_launch_ms * 1e-3) / 1e12,
+                    "peak": None, "unit": "TFLOP/s", "frac": None, "traffic": None}
+    else:
+        # tensor FLOPs per launch: products * 2MNK; TF32 runs at half the BF16 rate
+        tensor_flops = products * flops
+        achieved = tensor_flops / (per_launch_ms * 1e-3) / 1e12
+        peak = p_bf16 if g.mode == "bf16x9" else p_bf16 / 2.0
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "kernel": dom_name,
+                    "peak_source": f"{peak_src} bf16 burst" + (" / 2 (tf32 nominal ratio)" if g.mode == "tf32x3" else ""),
+                    "kernel_ms": round(per_launch_ms, 4)}
+        traffic = load_traffic(dom_name, args.workload, g.mode)
+        if traffic is not None:
+            roofline["traffic"] = traffic
+
+    split_n, split_ms = prof["split"]
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": g.name, "M": g.M, "N": g.N, "K": g.K, "mode": g.mode,
+                   "transA": g.transA, "transB": g.transB, "alpha": g.alpha, "beta": g.beta,
+                   "path": emu.emu_get_path(), "emulates": "fp32",
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{world}"},
+        "pct_of_bf16_peak_over_9": round(100.0 * frac9, 2),
+        "bf16_peak_tflops": p_bf16,
+        "roofline": roofline,
+        "kernels": {"split_ms_per_step": round(split_ms / args.steps, 4),
+                    f"{dom_name}_ms_per_launch": round(per_launch_ms, 4)},
+        "gpu_launches": launches,
+    }
+    out["clocks"] = clocks.summary()
+
+    if rank == 0:
+        out["e2e"] = bench_e2e(emu, g, A, B, C0, stream, args)
+        if not args.no_simt and g.mode != "fp32_simt":
+            out["simt_fp32"] = bench_simt(emu, g, dA, dB, dC, stream)
+        if not args.no_cpu:
+            out["cpu_baseline"] = cpu_baseline(g, A, B, C0, args.cpu_seconds)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def load_traffic(kernel, workload, mode):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, if one
+    matches this kernel, workload and mode (profiles/traffic.json)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    return d.get(f"{kernel}:{workload}:{mode}")
+
+
+def bench_e2e(emu, g, A, B, C0, stream, args):
+    """Same metric through emu_sgemm_host: host->device copies of A and B (and
+    C0), the GEMM and the device->host copy of C inside the timed region."""
+    import numpy as np
+    import torch
+    pa = torch.empty(A.shape, dtype=torch.float32, pin_memory=True).numpy()
+    pb = torch.empty(B.shape, dtype=torch.float32, pin_memory=True).numpy()
+    pc = torch.empty((g.M, g.N), dtype=torch.float32, pin_memory=True).numpy()
+    pa[...] = A
+    pb[...] = B
+    if C0 is not None:
+        pc[...] = C0
+
+    def once():
+        emu.emu_sgemm_host(pa, pb, pc, transA=g.transA, transB=g.transB, alpha=g.alpha,
+                           beta=g.beta, mode=g.mode, stream=stream)
+
+    once()
+    steps = max(2, min(args.steps, 5))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        once()
+    dt = (time.perf_counter() - t0) / steps
+    h2d = (A.size + B.size + (C0.size if C0 is not None else 0)) * 4
+    return {"value": round(g.flops / dt / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(g.M * g.N * 4),
+            "ms_per_step": round(dt * 1e3, 3), "api": "emu_sgemm_host", "memory": "pinned"}
+
+
+def bench_simt(emu, g, dA, dB, dC, stream):
+    """The library's own FP32 SIMT kernel on the same operands (context)."""
+    import torch
+    run = lambda: emu.emu_sgemm(dA, dB, dC, transA=g.transA, transB=g.transB, alpha=g.alpha,
+                                beta=g.beta, mode="fp32_simt", stream=stream)
+    run()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 3
+    s.record(stream)
+    for _ in range(n):
+        run()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"value": round(g.flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_call": round(ms, 3)}
+
+
+def cpu_baseline(g, A, B, C0, seconds):
+    """The CPU oracle (plain C, OpenMP over the host cores) on a block of rows
+    of the same GEMM, scaled to the metric's unit."""
+    import numpy as np
+    import oracle
+    fn = {"bf16x9": oracle.gemm_bf16x9, "tf32x3": oracle.gemm_tf32x3,
+          "fp32_simt": oracle.gemm_fp32}[g.mode]
+    threads = oracle.max_threads()
+
+    def rows_pairs(r):
+        mi = np.repeat(np.arange(r, dtype=np.int64), g.N)
+        ni = np.tile(np.arange(g.N, dtype=np.int64), r)
+        return mi, ni
+
+    r = 1
+    t0 = time.perf_counter()
+    fn(A, B, g.transA, g.transB, g.alpha, g.beta, C0, pairs=rows_pairs(r))
+    t1 = time.perf_counter() - t0
+    # size the sample to about `seconds` of CPU time
+    r = int(max(1, min(g.M, seconds / max(t1, 1e-6))))
+    t0 = time.perf_counter()
+    fn(A, B, g.transA, g.transB, g.alpha, g.beta, C0, pairs=rows_pairs(r))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * r * g.N * g.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{r} of {g.M} rows x all {g.N} columns of {g.name} ({g.mode}), "
+                      f"{dt:.1f} s, scaled linearly"}
+
+
+# ------------------------------------------------------- reference arm --
+
+def bench_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    from fp32_emulated_gemm_split_gb300 import workloads as W
+    import oracle
+    g = W.with_mode(W.WORKLOADS[args.workload], args.mode or W.WORKLOADS[args.workload].mode)
+    A, B, C0 = W.generate(g)
+    oracle.build()
+    fn = {"bf16x9": oracle.gemm_bf16x9, "tf32x3": oracle.gemm_tf32x3,
+          "fp32_simt": oracle.gemm_fp32}[g.mode]
+    # each step is a block of rows sized so the whole run takes a few minutes
+    budget = max(20.0, min(150.0, args.cpu_seconds * 6))
+    per_step = budget / (args.steps + args.warmup)
+    mi = np.zeros(g.N, np.int64)
+    ni = np.arange(g.N, dtype=np.int64)
+    t0 = time.perf_counter()
+    fn(A, B, g.transA, g.transB, g.alpha, g.beta, C0, pairs=(mi, ni))
+    t_row = time.perf_counter() - t0
+    rows = int(max(1, min(g.M, per_step / max(t_row, 1e-6))))
+    pairs = (np.repeat(np.arange(rows, dtype=np.int64), g.N),
+             np.tile(np.arange(g.N, dtype=np.int64), rows))
+    for _ in range(args.warmup):
+        fn(A, B, g.transA, g.transB, g.alpha, g.beta, C0, pairs=pairs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn(A, B, g.transA, g.transB, g.alpha, g.beta, C0, pairs=pairs)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 2.0 * rows * g.N * g.K / dt / 1e12
+    sample = f"{rows} of {g.M} rows x all {g.N} columns of {g.name} per step, scaled linearly"
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": g.name, "M": g.M, "N": g.N, "K": g.K, "mode": g.mode,
+                   "transA": g.transA, "transB": g.transB, "alpha": g.alpha, "beta": g.beta,
+                   "emulates": "fp32"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="square8192_normal")
+    ap.add_argument("--mode", default=None, choices=[None, "bf16x9", "tf32x3", "fp32_simt"])
+    ap.add_argument("--impl", default="emu", choices=["emu", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-simt", action="store_true", help="skip the SIMT FP32 context number")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

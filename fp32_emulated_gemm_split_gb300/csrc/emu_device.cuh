@@ -1,0 +1,268 @@
+// emu_device.cuh -- device-side building blocks shared by the library's
+// kernels: inline-PTX wrappers for mbarriers, TMA, tcgen05 (TMEM allocation,
+// MMA, commit, loads), bounded waits and the sticky device error word.
+//
+// Every wait in this library is bounded: a wait that has not completed after
+// EMU_WAIT_LIMIT_NS of %globaltimer records an error code in the device's
+// sticky error word (its address is a kernel argument) and returns false, and
+// the calling kernel winds down instead of spinning forever.  No kernel traps.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "emu_internal.h"
+
+namespace emu {
+
+#ifndef EMU_WAIT_LIMIT_NS
+#define EMU_WAIT_LIMIT_NS 2000000000ull   // 2 s: far above any legitimate wait
+#endif
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void record_error(int* err, int code) {
+    atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier --
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Returns false (and
+// records `code` in *err) if it has not completed within the limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err, int code,
+                                          uint64_t limit_ns = EMU_WAIT_LIMIT_NS) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
+            record_error(err, code);
+            return false;
+        }
+    }
+}
+
+// --------------------------------------------------------------------- TMA --
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
+}
+
+// 3-D tiled load into this CTA's shared memory, completion signalled on `bar`
+// as transaction bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05 --
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 "matrix descriptor") for a K-major
+// operand tile stored with the 128-byte swizzle: rows of 128 bytes, groups of
+// 8 rows 1024 bytes apart.  Fields: start address >> 4 in bits 0-13, leading
+// byte offset >> 4 in bits 16-29 (unused by this swizzled K-major layout),
+// stride byte offset >> 4 in bits 32-45, the fixed value 1 in bits 46-47,
+// base offset 0 (tiles are 1024-byte aligned), swizzle mode 2 (128-byte) in
+// bits 61-63.
+__device__ __forceinline__ uint64_t make_sw128_kmajor_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1u) << 16;                 // LBO: 16 bytes (ignored)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;         // SBO: 1024 bytes
+    d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version
+    d |= static_cast<uint64_t>(2u) << 61;                 // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor for a dense tcgen05.mma with FP32 accumulation and
+// both operands K-major: D format F32 (bits 4-5 = 1), A and B formats in bits
+// 7-9 and 10-12 (kind::f16: 1 = BF16; kind::tf32: 2 = TF32), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t M, uint32_t N) {
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+template <int KIND_TF32>
+__device__ __forceinline__ void mma_cta1(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    if constexpr (KIND_TF32) {
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
+            :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+    } else {
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+            :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+    }
+}
+
+// D = A*B + 2^-8 * D: the accumulator is rescaled by the tensor core itself
+// (the scale-input-d operand), which is how a finished band is shifted down
+// by one band (2^-8) before the next, larger band is added on top of it.
+template <int KIND_TF32>
+__device__ __forceinline__ void mma_cta1_scaled8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc) {
+    if constexpr (KIND_TF32) {
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, 1, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p, 8;\n}\n"
+            :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc) : "memory");
+    } else {
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, 1, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p, 8;\n}\n"
+            :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc) : "memory");
+    }
+}
+
+// Arrive (once) on `bar` when all tcgen05 operations issued so far by this
+// thread have completed.
+__device__ __forceinline__ void tc_commit_cta1(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_cta1(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(dst_smem), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_cta1(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                 :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives the
+// 32 columns of TMEM lane (lane base + t).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------- the split --
+
+// Nearest BF16 (ties to even) of a finite FP32 value; a value whose nearest
+// BF16 would be infinite takes the largest finite BF16 of its sign, which is
+// the truncated value (the `satfinite` form of the conversion).
+__device__ __forceinline__ uint16_t bf16_rn_sat(float x) {
+    uint16_t h;
+    asm("cvt.rn.satfinite.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
+    return h;
+}
+
+__device__ __forceinline__ float bf16_as_f32(uint16_t h) {
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// x = x0 + 2^-8 x1 + 2^-16 x2 with three BF16 pieces, x1 and x2 scaled up by
+// 2^8 and 2^16 so that each piece keeps a full BF16 significand.  Rounding is
+// to nearest, ties to even, with signed residuals; +-inf -> (x, +0, +0); NaN ->
+// three canonical quiet NaNs.  The subtraction and the scaling are exact.
+__device__ __forceinline__ void split_bf16x3(float x, uint16_t& h0, uint16_t& h1, uint16_t& h2) {
+    const uint32_t u = __float_as_uint(x);
+    if ((u & 0x7F800000u) == 0x7F800000u) {
+        const bool nan = (u & 0x007FFFFFu) != 0;
+        h0 = nan ? uint16_t(0x7FC0) : uint16_t(u >> 16);
+        h1 = nan ? uint16_t(0x7FC0) : uint16_t(0);
+        h2 = h1;
+        return;
+    }
+    h0 = bf16_rn_sat(x);
+    const float s1 = __fmul_rn(__fsub_rn(x, bf16_as_f32(h0)), 256.0f);
+    h1 = bf16_rn_sat(s1);
+    const float s2 = __fmul_rn(__fsub_rn(s1, bf16_as_f32(h1)), 256.0f);
+    h2 = bf16_rn_sat(s2);
+}
+
+// Nearest TF32 (10 explicit mantissa bits, ties to even) kept in an FP32
+// container with the low 13 bits zero; overflow to inf is replaced by the
+// truncated value.  Integer rounding on the bit pattern.
+__device__ __forceinline__ uint32_t tf32_rn_bits(float x) {
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t r = (u + 0x0FFFu + ((u >> 13) & 1u)) & 0xFFFFE000u;
+    return ((r & 0x7F800000u) == 0x7F800000u) ? (u & 0xFFFFE000u) : r;
+}
+
+// x = hi + lo, both TF32, no scaling.
+__device__ __forceinline__ void split_tf32x2(float x, float& hi, float& lo) {
+    const uint32_t u = __float_as_uint(x);
+    if ((u & 0x7F800000u) == 0x7F800000u) {
+        const bool nan = (u & 0x007FFFFFu) != 0;
+        hi = nan ? __uint_as_float(0x7FC00000u) : x;
+        lo = nan ? __uint_as_float(0x7FC00000u) : 0.0f;
+        return;
+    }
+    hi = __uint_as_float(tf32_rn_bits(x));
+    lo = __uint_as_float(tf32_rn_bits(__fsub_rn(x, hi)));
+}
+
+}  // namespace emu

@@ -1,0 +1,53 @@
+// emu_internal.h -- declarations shared by the translation units of
+// libemusgemm (host launchers and kernel parameters).  Not installed.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace emu {
+
+// Device error codes recorded in the sticky error word (same values as the
+// public emu_status_t).
+enum : int {
+    kDevErrTimeout = -5,
+};
+
+// Tile shape of the tensor-core GEMM (cta_group::1, one CTA per SM).
+constexpr int kTcBM = 128;          // rows of C per CTA (MMA M)
+constexpr int kTcBN = 256;          // columns of C per CTA (MMA N)
+constexpr int kTcBKBytes = 128;     // K extent of one stage in bytes (one 128-byte swizzle row)
+constexpr int kTcStages = 4;        // shared-memory pipeline depth
+constexpr int kTcThreads = 192;     // 4 epilogue warps, 1 TMA warp, 1 MMA warp
+
+// Row stride, in elements, of the split pieces in the workspace: a multiple
+// of 8 so that every row starts on a 16-byte boundary (a TMA requirement).
+inline int64_t plane_ld(int64_t K) { return (K + 7) / 8 * 8; }
+
+struct TcGemmParams {
+    int* err;            // the device's sticky error word
+    int M, N, K;
+    int num_kb;          // number of K stages: ceil(K / elements per stage)
+    int tiles_m, tiles_n;
+    float alpha, beta;
+    float* C;
+    int64_t ldc;
+};
+
+// Launchers (return the launch status; nothing is synchronised).
+cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
+                                uint16_t* P0, uint16_t* P1, uint16_t* P2, int64_t ldp,
+                                cudaStream_t stream);
+cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
+                                float* HI, float* LO, int64_t ldp, cudaStream_t stream);
+cudaError_t launch_gemm_tc(int tf32, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                           const TcGemmParams& p, cudaStream_t stream);
+cudaError_t launch_gemm_simt(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                             const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                             float* C, int64_t ldc, cudaStream_t stream);
+cudaError_t launch_scale(int64_t M, int64_t N, float beta, float* C, int64_t ldc,
+                         cudaStream_t stream);
+cudaError_t launch_timeout_probe(int* err, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace emu

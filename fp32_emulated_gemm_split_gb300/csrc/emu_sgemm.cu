@@ -1,0 +1,474 @@
+// emu_sgemm.cu -- host side of libemusgemm: the C ABI declared in
+// include/emu_sgemm.h.  Argument checks, the per-device workspace, TMA tensor
+// maps, dispatch between the two-pass, fused and SIMT paths, kernel timing
+// and the host-buffer entry point.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "emu_device.cuh"
+#include "emu_sgemm.h"
+
+namespace emu {
+
+__device__ int g_emu_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    int checked = 0;           // 0 unknown, 1 supported, -1 unsupported
+    int sms = 0;
+    int* err = nullptr;        // device address of g_emu_error
+    void* ws = nullptr;        // workspace for the split pieces
+    size_t ws_bytes = 0;
+    void* stage = nullptr;     // device staging for emu_sgemm_host
+    size_t stage_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+int g_path = -1;               // -1: not yet read from the environment
+
+// ------------------------------------------------------------ profiling --
+struct ProfRecord { int kind; cudaEvent_t start, stop; };
+bool g_prof_on = false;
+std::vector<ProfRecord> g_prof_pending;
+std::vector<cudaEvent_t> g_event_pool;
+int64_t g_prof_launches[5] = {0, 0, 0, 0, 0};
+double g_prof_ms[5] = {0, 0, 0, 0, 0};
+
+cudaEvent_t pool_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+struct ProfScope {
+    int kind;
+    cudaStream_t stream;
+    cudaEvent_t start = nullptr;
+    ProfScope(int k, cudaStream_t s) : kind(k), stream(s) {
+        if (g_prof_on) {
+            start = pool_event();
+            cudaEventRecord(start, stream);
+        }
+    }
+    ~ProfScope() {
+        if (start) {
+            cudaEvent_t stop = pool_event();
+            cudaEventRecord(stop, stream);
+            g_prof_pending.push_back({kind, start, stop});
+        }
+    }
+};
+
+// ----------------------------------------------------------- helpers --
+
+emu_status_t from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return EMU_OK;
+    if (e == cudaErrorMemoryAllocation) return EMU_ERR_ALLOC;
+    if (e == cudaErrorLaunchFailure || e == cudaErrorInvalidConfiguration ||
+        e == cudaErrorLaunchOutOfResources || e == cudaErrorInvalidDeviceFunction ||
+        e == cudaErrorNoKernelImageForDevice)
+        return EMU_ERR_LAUNCH;
+    return EMU_ERR_CUDA;
+}
+
+int read_path_env() {
+    const char* s = std::getenv("EMU_SGEMM_PATH");
+    if (!s) return EMU_PATH_AUTO;
+    if (!std::strcmp(s, "twopass")) return EMU_PATH_TWOPASS;
+    if (!std::strcmp(s, "fused")) return EMU_PATH_FUSED;
+    return EMU_PATH_AUTO;
+}
+
+// Current device state, checking the architecture once.
+emu_status_t current_device(DeviceState** out, int* dev_out = nullptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return EMU_ERR_CUDA;
+    DeviceState& d = g_dev[dev];
+    if (d.checked == 0) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        d.checked = (major == 10 && minor == 3) ? 1 : -1;
+        if (d.checked > 0 &&
+            cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_emu_error) != cudaSuccess) {
+            cudaGetLastError();
+            d.checked = 0;
+            return EMU_ERR_CUDA;
+        }
+    }
+    if (d.checked < 0) return EMU_ERR_ARCH;
+    *out = &d;
+    if (dev_out) *dev_out = dev;
+    return EMU_OK;
+}
+
+emu_status_t ensure_buffer(void** buf, size_t* have, size_t need) {
+    if (need <= *have) return EMU_OK;
+    if (*buf) {
+        cudaFree(*buf);   // synchronises the device: no kernel still reads the old buffer
+        *buf = nullptr;
+        *have = 0;
+    }
+    size_t bytes = need + need / 8;   // some headroom against repeated growth
+    if (cudaMalloc(buf, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        *buf = nullptr;
+        return EMU_ERR_ALLOC;
+    }
+    *have = bytes;
+    return EMU_OK;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime so the
+// library needs no link-time dependency on libcuda.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// Tensor map over `planes` row-major planes of rows x cols elements (row
+// stride ld elements, plane stride rows*ld), box of box_cols x box_rows,
+// 128-byte swizzle, zero fill outside the matrix.
+emu_status_t make_plane_map(CUtensorMap* map, const void* base, bool fp32, int64_t rows,
+                            int64_t cols, int64_t ld, int planes, int box_cols, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return EMU_ERR_CUDA;
+    const int esize = fp32 ? 4 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(rows * ld * esize)};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     3, const_cast<void*>(base), dims, strides, box, elem_strides,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? EMU_OK : EMU_ERR_CUDA;
+}
+
+emu_status_t check_gemm_args(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                             const float* A, int64_t lda, const float* B, int64_t ldb,
+                             float beta, float* C, int64_t ldc, int mode) {
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return EMU_ERR_INVALID_VALUE;
+    if (mode != EMU_MODE_BF16X9 && mode != EMU_MODE_TF32X3 && mode != EMU_MODE_FP32_SIMT)
+        return EMU_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0) return EMU_ERR_INVALID_VALUE;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return EMU_ERR_INVALID_VALUE;
+    const int64_t a_cols = transA ? M : K, b_cols = transB ? K : N;
+    if (lda < 1 || lda < a_cols || ldb < 1 || ldb < b_cols || ldc < 1 || ldc < N)
+        return EMU_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return EMU_OK;
+    if (C == nullptr) return EMU_ERR_INVALID_VALUE;
+    if (K > 0 && (A == nullptr || B == nullptr)) return EMU_ERR_INVALID_VALUE;
+    (void)beta;
+    return EMU_OK;
+}
+
+emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N, int64_t K,
+                          float alpha, const float* A, int64_t lda, const float* B, int64_t ldb,
+                          float beta, float* C, int64_t ldc, DeviceState* d, cudaStream_t stream) {
+    const int64_t ldp = plane_ld(K);
+    const int planes = tf32 ? 2 : 3;
+    const int esize = tf32 ? 4 : 2;
+    const size_t a_bytes = (size_t)planes * M * ldp * esize;
+    const size_t b_bytes = (size_t)planes * N * ldp * esize;
+    const size_t a_region = (a_bytes + 1023) / 1024 * 1024;
+    emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, a_region + b_bytes);
+    if (st != EMU_OK) return st;
+    uint8_t* wa = static_cast<uint8_t*>(d->ws);
+    uint8_t* wb = wa + a_region;
+
+    cudaError_t e;
+    {
+        ProfScope ps(0, stream);
+        if (tf32) {
+            float* pa = reinterpret_cast<float*>(wa);
+            e = launch_split_tf32x2(A, M, K, lda, transA, pa, pa + M * ldp, ldp, stream);
+        } else {
+            uint16_t* pa = reinterpret_cast<uint16_t*>(wa);
+            e = launch_split_bf16x3(A, M, K, lda, transA, pa, pa + M * ldp, pa + 2 * M * ldp, ldp,
+                                    stream);
+        }
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    {
+        // op(B)^T is N x K: B itself when transB == 1, B^T otherwise
+        ProfScope ps(0, stream);
+        if (tf32) {
+            float* pb = reinterpret_cast<float*>(wb);
+            e = launch_split_tf32x2(B, N, K, ldb, !transB, pb, pb + N * ldp, ldp, stream);
+        } else {
+            uint16_t* pb = reinterpret_cast<uint16_t*>(wb);
+            e = launch_split_bf16x3(B, N, K, ldb, !transB, pb, pb + N * ldp, pb + 2 * N * ldp, ldp,
+                                    stream);
+        }
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+
+    const int box_cols = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
+    CUtensorMap mapA, mapB;
+    st = make_plane_map(&mapA, wa, tf32, M, K, ldp, planes, box_cols, kTcBM);
+    if (st != EMU_OK) return st;
+    st = make_plane_map(&mapB, wb, tf32, N, K, ldp, planes, box_cols, kTcBN);
+    if (st != EMU_OK) return st;
+
+    TcGemmParams p;
+    p.err = d->err;
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.num_kb = (int)((K + box_cols - 1) / box_cols);
+    p.tiles_m = (int)((M + kTcBM - 1) / kTcBM);
+    p.tiles_n = (int)((N + kTcBN - 1) / kTcBN);
+    p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
+    {
+        ProfScope ps(1, stream);
+        e = launch_gemm_tc(tf32, mapA, mapB, p, stream);
+    }
+    return from_cuda(e);
+}
+
+emu_status_t sgemm_device(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                          const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                          float* C, int64_t ldc, int mode, cudaStream_t stream) {
+    emu_status_t st = check_gemm_args(transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, mode);
+    if (st != EMU_OK) return st;
+    if (M == 0 || N == 0) return EMU_OK;
+    DeviceState* d = nullptr;
+    st = current_device(&d);
+    if (st != EMU_OK) return st;
+    if (K == 0 || alpha == 0.0f) {
+        ProfScope ps(4, stream);
+        return from_cuda(launch_scale(M, N, beta, C, ldc, stream));
+    }
+    if (mode == EMU_MODE_FP32_SIMT) {
+        ProfScope ps(3, stream);
+        return from_cuda(launch_gemm_simt(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                                          ldc, stream));
+    }
+    return run_two_pass(mode == EMU_MODE_TF32X3, transA, transB, M, N, K, alpha, A, lda, B, ldb,
+                        beta, C, ldc, d, stream);
+}
+
+emu_status_t check_split_args(const void* X, int64_t rows, int64_t cols, int64_t ld, int trans,
+                              const void* P0, const void* P1, const void* P2, int64_t ldp) {
+    if (trans != 0 && trans != 1) return EMU_ERR_INVALID_VALUE;
+    if (rows < 0 || cols < 0) return EMU_ERR_INVALID_VALUE;
+    if (ld < 1 || ld < (trans ? rows : cols) || ldp < 1 || ldp < cols) return EMU_ERR_INVALID_VALUE;
+    if (rows == 0 || cols == 0) return EMU_OK;
+    if (!X || !P0 || !P1 || !P2) return EMU_ERR_INVALID_VALUE;
+    return EMU_OK;
+}
+
+}  // namespace
+}  // namespace emu
+
+using namespace emu;
+
+extern "C" {
+
+emu_status_t emu_sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                       const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                       float* C, int64_t ldc, int mode, emu_stream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    return sgemm_device(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, mode,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+emu_status_t emu_sgemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                            const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                            float* C, int64_t ldc, int mode, emu_stream_t stream_) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    emu_status_t st = check_gemm_args(transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, mode);
+    if (st != EMU_OK) return st;
+    if (M == 0 || N == 0) return EMU_OK;
+    DeviceState* d = nullptr;
+    st = current_device(&d);
+    if (st != EMU_OK) return st;
+    // stored extents: A is (transA ? K : M) rows of lda, B is (transB ? N : K) rows of ldb
+    const int64_t a_rows = transA ? K : M, b_rows = transB ? N : K;
+    const size_t a_bytes = K > 0 ? (size_t)((a_rows - 1) * lda + (transA ? M : K)) * 4 : 0;
+    const size_t b_bytes = K > 0 ? (size_t)((b_rows - 1) * ldb + (transB ? K : N)) * 4 : 0;
+    const size_t c_bytes = (size_t)((M - 1) * ldc + N) * 4;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    st = ensure_buffer(&d->stage, &d->stage_bytes, up(a_bytes) + up(b_bytes) + up(c_bytes));
+    if (st != EMU_OK) return st;
+    uint8_t* base = static_cast<uint8_t*>(d->stage);
+    float* dA = reinterpret_cast<float*>(base);
+    float* dB = reinterpret_cast<float*>(base + up(a_bytes));
+    float* dC = reinterpret_cast<float*>(base + up(a_bytes) + up(b_bytes));
+    cudaError_t e = cudaSuccess;
+    if (a_bytes) e = cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess && b_bytes) e = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess && beta != 0.0f)
+        e = cudaMemcpyAsync(dC, C, c_bytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    st = sgemm_device(transA, transB, M, N, K, alpha, K > 0 ? dA : nullptr, lda,
+                      K > 0 ? dB : nullptr, ldb, beta, dC, ldc, mode, stream);
+    if (st != EMU_OK) return st;
+    e = cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    return from_cuda(e);
+}
+
+emu_status_t emu_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
+                              uint16_t* P0, uint16_t* P1, uint16_t* P2, int64_t ldp,
+                              emu_stream_t stream) {
+    emu_status_t st = check_split_args(X, rows, cols, ld, trans, P0, P1, P2, ldp);
+    if (st != EMU_OK || rows == 0 || cols == 0) return st;
+    DeviceState* d = nullptr;
+    st = current_device(&d);
+    if (st != EMU_OK) return st;
+    return from_cuda(launch_split_bf16x3(X, rows, cols, ld, trans, P0, P1, P2, ldp,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+emu_status_t emu_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
+                              float* HI, float* LO, int64_t ldp, emu_stream_t stream) {
+    emu_status_t st = check_split_args(X, rows, cols, ld, trans, HI, LO, LO, ldp);
+    if (st != EMU_OK || rows == 0 || cols == 0) return st;
+    DeviceState* d = nullptr;
+    st = current_device(&d);
+    if (st != EMU_OK) return st;
+    return from_cuda(launch_split_tf32x2(X, rows, cols, ld, trans, HI, LO, ldp,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+emu_status_t emu_set_path(int path) {
+    if (path != EMU_PATH_AUTO && path != EMU_PATH_TWOPASS && path != EMU_PATH_FUSED)
+        return EMU_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_path = path;
+    return EMU_OK;
+}
+
+int emu_get_path(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_path < 0) g_path = read_path_env();
+    return g_path;
+}
+
+size_t emu_workspace_size(int64_t M, int64_t N, int64_t K, int mode) {
+    if (M <= 0 || N <= 0 || K <= 0 || mode == EMU_MODE_FP32_SIMT) return 0;
+    const int tf32 = mode == EMU_MODE_TF32X3;
+    const size_t per = (size_t)(tf32 ? 2 : 3) * plane_ld(K) * (tf32 ? 4 : 2);
+    return (per * M + 1023) / 1024 * 1024 + per * N;
+}
+
+emu_status_t emu_get_last_device_error(void) {
+    int v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return from_cuda(e);
+    e = cudaMemcpyFromSymbol(&v, g_emu_error, sizeof(int));
+    if (e != cudaSuccess) return from_cuda(e);
+    return static_cast<emu_status_t>(v);
+}
+
+emu_status_t emu_clear_device_error(void) {
+    const int zero = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_emu_error, &zero, sizeof(int));
+    return from_cuda(e);
+}
+
+emu_status_t emu_selftest_timeout(int limit_us, emu_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000) return EMU_ERR_INVALID_VALUE;
+    DeviceState* d = nullptr;
+    emu_status_t st = current_device(&d);
+    if (st != EMU_OK) return st;
+    cudaError_t e = launch_timeout_probe(d->err, (uint64_t)limit_us * 1000ull,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    return emu_get_last_device_error();
+}
+
+emu_status_t emu_profile_enable(int on) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto& r : g_prof_pending) {
+        g_event_pool.push_back(r.start);
+        g_event_pool.push_back(r.stop);
+    }
+    g_prof_pending.clear();
+    for (int i = 0; i < 5; ++i) { g_prof_launches[i] = 0; g_prof_ms[i] = 0.0; }
+    g_prof_on = on != 0;
+    return EMU_OK;
+}
+
+emu_status_t emu_profile_read(int kind, int64_t* launches, double* total_ms) {
+    if (kind < 0 || kind >= 5 || !launches || !total_ms) return EMU_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto& r : g_prof_pending) {
+        cudaError_t e = cudaEventSynchronize(r.stop);
+        if (e != cudaSuccess) return from_cuda(e);
+        float ms = 0.0f;
+        cudaEventElapsedTime(&ms, r.start, r.stop);
+        g_prof_launches[r.kind] += 1;
+        g_prof_ms[r.kind] += ms;
+        g_event_pool.push_back(r.start);
+        g_event_pool.push_back(r.stop);
+    }
+    g_prof_pending.clear();
+    *launches = g_prof_launches[kind];
+    *total_ms = g_prof_ms[kind];
+    return EMU_OK;
+}
+
+const char* emu_status_string(emu_status_t s) {
+    switch (s) {
+        case EMU_OK: return "EMU_OK";
+        case EMU_ERR_INVALID_VALUE: return "EMU_ERR_INVALID_VALUE";
+        case EMU_ERR_ARCH: return "EMU_ERR_ARCH";
+        case EMU_ERR_ALLOC: return "EMU_ERR_ALLOC";
+        case EMU_ERR_LAUNCH: return "EMU_ERR_LAUNCH";
+        case EMU_ERR_TIMEOUT: return "EMU_ERR_TIMEOUT";
+        case EMU_ERR_CUDA: return "EMU_ERR_CUDA";
+    }
+    return "EMU_ERR_UNKNOWN";
+}
+
+emu_status_t emu_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (int i = 0; i < kMaxDevices; ++i) {
+        DeviceState& d = g_dev[i];
+        if (!d.ws && !d.stage) continue;
+        cudaSetDevice(i);
+        if (d.ws) cudaFree(d.ws);
+        if (d.stage) cudaFree(d.stage);
+        d.ws = d.stage = nullptr;
+        d.ws_bytes = d.stage_bytes = 0;
+    }
+    cudaSetDevice(cur);
+    return EMU_OK;
+}
+
+int emu_version(void) { return 100; }
+
+}  // extern "C"

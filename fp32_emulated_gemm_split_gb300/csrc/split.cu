@@ -1,0 +1,234 @@
+// split.cu -- the split/pack step of the two-pass path: FP32 op(X) -> BF16
+// pieces (BF16x9) or TF32 pieces (TF32x3), written row-major with a padded
+// row stride so that the GEMM can stage them with TMA.
+//
+// The split itself is x = x0 + 2^-8 x1 + 2^-16 x2 ("Blackwell의 BF16x9"
+// section of the discuss.pytorch.kr page on the method; Figure 1 of the
+// NVIDIA blog post "Unlocking Tensor Core Performance for Machine Learning
+// Interatomic Potentials") and x = hi + lo (Figure 2 of that post).  These
+// kernels are bound by HBM bandwidth: BF16x9 reads 4 bytes and writes 6 bytes
+// per element, TF32x3 reads 4 and writes 8.
+#include "emu_device.cuh"
+
+namespace emu {
+namespace {
+
+// ------------------------------------------------------ row-wise (no transpose)
+
+// Each thread splits 8 consecutive elements of one row: two 16-byte loads,
+// one 16-byte store per piece.  Requires 16-byte aligned rows in and out.
+__global__ void __launch_bounds__(256) split3_rows_vec8(const float* __restrict__ X, int64_t rows,
+                                                        int64_t cols, int64_t ld,
+                                                        uint16_t* __restrict__ P0,
+                                                        uint16_t* __restrict__ P1,
+                                                        uint16_t* __restrict__ P2, int64_t ldp) {
+    const int64_t groups = cols / 8;
+    const int64_t total = rows * groups;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = t / groups;
+        const int64_t c = (t - r * groups) * 8;
+        const float4* src = reinterpret_cast<const float4*>(X + r * ld + c);
+        const float4 a = __ldcs(src);
+        const float4 b = __ldcs(src + 1);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint16_t h0[8], h1[8], h2[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) split_bf16x3(v[i], h0[i], h1[i], h2[i]);
+        uint4 o0, o1, o2;
+        o0.x = h0[0] | (uint32_t(h0[1]) << 16); o0.y = h0[2] | (uint32_t(h0[3]) << 16);
+        o0.z = h0[4] | (uint32_t(h0[5]) << 16); o0.w = h0[6] | (uint32_t(h0[7]) << 16);
+        o1.x = h1[0] | (uint32_t(h1[1]) << 16); o1.y = h1[2] | (uint32_t(h1[3]) << 16);
+        o1.z = h1[4] | (uint32_t(h1[5]) << 16); o1.w = h1[6] | (uint32_t(h1[7]) << 16);
+        o2.x = h2[0] | (uint32_t(h2[1]) << 16); o2.y = h2[2] | (uint32_t(h2[3]) << 16);
+        o2.z = h2[4] | (uint32_t(h2[5]) << 16); o2.w = h2[6] | (uint32_t(h2[7]) << 16);
+        const int64_t o = r * ldp + c;
+        *reinterpret_cast<uint4*>(P0 + o) = o0;
+        *reinterpret_cast<uint4*>(P1 + o) = o1;
+        *reinterpret_cast<uint4*>(P2 + o) = o2;
+    }
+}
+
+// Any shape and alignment: one element per thread.
+__global__ void __launch_bounds__(256) split3_rows_scalar(const float* __restrict__ X, int64_t rows,
+                                                          int64_t cols, int64_t ld,
+                                                          uint16_t* __restrict__ P0,
+                                                          uint16_t* __restrict__ P1,
+                                                          uint16_t* __restrict__ P2, int64_t ldp) {
+    const int64_t total = rows * cols;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = t / cols;
+        const int64_t c = t - r * cols;
+        uint16_t h0, h1, h2;
+        split_bf16x3(X[r * ld + c], h0, h1, h2);
+        const int64_t o = r * ldp + c;
+        P0[o] = h0; P1[o] = h1; P2[o] = h2;
+    }
+}
+
+__global__ void __launch_bounds__(256) split2_rows_vec4(const float* __restrict__ X, int64_t rows,
+                                                        int64_t cols, int64_t ld,
+                                                        float* __restrict__ HI,
+                                                        float* __restrict__ LO, int64_t ldp) {
+    const int64_t groups = cols / 4;
+    const int64_t total = rows * groups;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = t / groups;
+        const int64_t c = (t - r * groups) * 4;
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(X + r * ld + c));
+        float4 h, l;
+        split_tf32x2(a.x, h.x, l.x);
+        split_tf32x2(a.y, h.y, l.y);
+        split_tf32x2(a.z, h.z, l.z);
+        split_tf32x2(a.w, h.w, l.w);
+        *reinterpret_cast<float4*>(HI + r * ldp + c) = h;
+        *reinterpret_cast<float4*>(LO + r * ldp + c) = l;
+    }
+}
+
+__global__ void __launch_bounds__(256) split2_rows_scalar(const float* __restrict__ X, int64_t rows,
+                                                          int64_t cols, int64_t ld,
+                                                          float* __restrict__ HI,
+                                                          float* __restrict__ LO, int64_t ldp) {
+    const int64_t total = rows * cols;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = t / cols;
+        const int64_t c = t - r * cols;
+        float h, l;
+        split_tf32x2(X[r * ld + c], h, l);
+        HI[r * ldp + c] = h;
+        LO[r * ldp + c] = l;
+    }
+}
+
+// ------------------------------------------------------------- transposed
+//
+// op(X) = X^T: op(X)[r][c] = X[c * ld + r].  A 64 x 64 tile goes through
+// shared memory so that both the FP32 reads (along stored rows) and the
+// piece writes (along op rows, two BF16 per 4-byte store) are coalesced.
+constexpr int kT = 64;
+
+__global__ void __launch_bounds__(256) split3_transposed(const float* __restrict__ X, int64_t rows,
+                                                         int64_t cols, int64_t ld,
+                                                         uint16_t* __restrict__ P0,
+                                                         uint16_t* __restrict__ P1,
+                                                         uint16_t* __restrict__ P2, int64_t ldp) {
+    __shared__ float tile[kT][kT + 1];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+    const int64_t r0 = (int64_t)blockIdx.x * kT;              // op rows  = stored columns
+    const int64_t c0 = (int64_t)blockIdx.y * kT;              // op cols  = stored rows
+    // load: stored row (c0 + i), stored columns r0 + tx, r0 + tx + 32
+    for (int i = ty; i < kT; i += 8) {
+        const int64_t sr = c0 + i;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t sc = r0 + tx + 32 * h;
+            tile[i][tx + 32 * h] = (sr < cols && sc < rows) ? __ldcs(X + sr * ld + sc) : 0.0f;
+        }
+    }
+    __syncthreads();
+    // store: op row (r0 + j), op columns c0 + 2*tx, c0 + 2*tx + 1
+    for (int j = ty; j < kT; j += 8) {
+        const int64_t r = r0 + j;
+        if (r >= rows) break;
+        const int64_t c = c0 + 2 * tx;
+        uint16_t a0, a1, a2, b0, b1, b2;
+        split_bf16x3(tile[2 * tx][j], a0, a1, a2);
+        split_bf16x3(tile[2 * tx + 1][j], b0, b1, b2);
+        const int64_t o = r * ldp + c;
+        if (c + 1 < cols && (o & 1) == 0) {
+            *reinterpret_cast<uint32_t*>(P0 + o) = a0 | (uint32_t(b0) << 16);
+            *reinterpret_cast<uint32_t*>(P1 + o) = a1 | (uint32_t(b1) << 16);
+            *reinterpret_cast<uint32_t*>(P2 + o) = a2 | (uint32_t(b2) << 16);
+        } else {
+            if (c < cols) { P0[o] = a0; P1[o] = a1; P2[o] = a2; }
+            if (c + 1 < cols) { P0[o + 1] = b0; P1[o + 1] = b1; P2[o + 1] = b2; }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) split2_transposed(const float* __restrict__ X, int64_t rows,
+                                                         int64_t cols, int64_t ld,
+                                                         float* __restrict__ HI,
+                                                         float* __restrict__ LO, int64_t ldp) {
+    __shared__ float tile[kT][kT + 1];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int64_t r0 = (int64_t)blockIdx.x * kT;
+    const int64_t c0 = (int64_t)blockIdx.y * kT;
+    for (int i = ty; i < kT; i += 8) {
+        const int64_t sr = c0 + i;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t sc = r0 + tx + 32 * h;
+            tile[i][tx + 32 * h] = (sr < cols && sc < rows) ? __ldcs(X + sr * ld + sc) : 0.0f;
+        }
+    }
+    __syncthreads();
+    for (int j = ty; j < kT; j += 8) {
+        const int64_t r = r0 + j;
+        if (r >= rows) break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t c = c0 + tx + 32 * h;
+            if (c < cols) {
+                float hi, lo;
+                split_tf32x2(tile[tx + 32 * h][j], hi, lo);
+                HI[r * ldp + c] = hi;
+                LO[r * ldp + c] = lo;
+            }
+        }
+    }
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int grid_for(int64_t work, int threads) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (work + threads - 1) / threads;
+    const int64_t cap = (int64_t)sms * 8;     // 8 resident 256-thread blocks per SM
+    return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
+                                uint16_t* P0, uint16_t* P1, uint16_t* P2, int64_t ldp,
+                                cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    if (trans) {
+        dim3 grid((unsigned)((rows + kT - 1) / kT), (unsigned)((cols + kT - 1) / kT));
+        split3_transposed<<<grid, 256, 0, stream>>>(X, rows, cols, ld, P0, P1, P2, ldp);
+    } else if (cols % 8 == 0 && ld % 4 == 0 && ldp % 8 == 0 && aligned16(X) && aligned16(P0) &&
+               aligned16(P1) && aligned16(P2)) {
+        split3_rows_vec8<<<grid_for(rows * (cols / 8), 256), 256, 0, stream>>>(X, rows, cols, ld,
+                                                                              P0, P1, P2, ldp);
+    } else {
+        split3_rows_scalar<<<grid_for(rows * cols, 256), 256, 0, stream>>>(X, rows, cols, ld, P0,
+                                                                          P1, P2, ldp);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
+                                float* HI, float* LO, int64_t ldp, cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    if (trans) {
+        dim3 grid((unsigned)((rows + kT - 1) / kT), (unsigned)((cols + kT - 1) / kT));
+        split2_transposed<<<grid, 256, 0, stream>>>(X, rows, cols, ld, HI, LO, ldp);
+    } else if (cols % 4 == 0 && ld % 4 == 0 && ldp % 4 == 0 && aligned16(X) && aligned16(HI) &&
+               aligned16(LO)) {
+        split2_rows_vec4<<<grid_for(rows * (cols / 4), 256), 256, 0, stream>>>(X, rows, cols, ld,
+                                                                              HI, LO, ldp);
+    } else {
+        split2_rows_scalar<<<grid_for(rows * cols, 256), 256, 0, stream>>>(X, rows, cols, ld, HI,
+                                                                          LO, ldp);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace emu

@@ -1,0 +1,212 @@
+/*
+ * emu_sgemm.h -- C ABI of libemusgemm: FP32 matrix multiplication emulated
+ * on the BF16 (or TF32) tensor cores of one GB300 GPU (sm_103a).
+ *
+ * The method is the one described on the web pages about it:
+ *
+ *  - "Unlocking Tensor Core Performance for Machine Learning Interatomic
+ *    Potentials" (NVIDIA technical blog), Figure 1 and its caption (BF16x9:
+ *    three scaled BF16 pieces per FP32 operand, nine pairwise products,
+ *    accumulated in FP32 over five anti-diagonal bands), Figure 2 and the
+ *    equation under it (TF32x3: a leading and a residual TF32 piece, no
+ *    scaling, the residual*residual product dropped);
+ *  - the discuss.pytorch.kr summary of that post, section "Blackwell의
+ *    BF16x9: 세 조각, 아홉 번의 곱" (x = x0 + 2^-8 x1 + 2^-16 x2; the bands are
+ *    added to the FP32 accumulator smallest band first) and section "Ampere의
+ *    TF32x3: 두 조각, 세 번의 곱".
+ *
+ * The interface keeps what the pages require of it: FP32 in, FP32 out, the
+ * caller's code unchanged apart from the call ("FP32 in and out" in the
+ * CUTLASS paragraph of the blog post's TF32x3 section).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Storage   Row major.  op(X) = X when trans == 0, X^T when trans == 1.  The
+ *            leading dimension (ld*) is the distance, in elements, between
+ *            consecutive rows of the matrix AS STORED.  A column-major caller
+ *            computes C^T = op(B)^T op(A)^T instead.
+ *  Pointers  Unless an entry point says otherwise, matrix pointers are CUDA
+ *            device pointers (or managed memory) on the current device, owned
+ *            by the caller; the library never frees them.
+ *  Streams   `stream` is a cudaStream_t (0 = the legacy default stream).
+ *            Work is enqueued asynchronously; a call returns once its kernels
+ *            are launched.
+ *  Errors    Arguments are checked on the host before anything is launched;
+ *            a bad argument returns EMU_ERR_INVALID_VALUE and touches nothing.
+ *            No entry point aborts the process, traps on the device or spins
+ *            without a bound: device-side waits give up after a time limit
+ *            and record EMU_ERR_TIMEOUT in a sticky per-device error word that
+ *            emu_get_last_device_error() returns.
+ *  Scratch   The two-pass path stores the split operands in a workspace that
+ *            the library allocates per device, grows on demand and releases
+ *            in emu_shutdown().  Calls on one device share it, so concurrent
+ *            calls on different streams of one device must be serialised by
+ *            the caller.  Growing it calls cudaMalloc / cudaFree, which must
+ *            not happen during stream capture.
+ */
+#ifndef EMU_SGEMM_H
+#define EMU_SGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared here without the CUDA headers. */
+typedef struct CUstream_st* emu_stream_t;
+
+typedef enum {
+    /* three BF16 pieces per operand, nine products in five bands */
+    EMU_MODE_BF16X9 = 0,
+    /* two TF32 pieces per operand, three products (residual*residual dropped) */
+    EMU_MODE_TF32X3 = 1,
+    /* plain FP32 FMA on the CUDA cores (the library's own baseline) */
+    EMU_MODE_FP32_SIMT = 2
+} emu_mode_t;
+
+typedef enum {
+    EMU_OK = 0,
+    EMU_ERR_INVALID_VALUE = -1,   /* bad argument; nothing was launched */
+    EMU_ERR_ARCH = -2,            /* current device is not compute capability 10.3 */
+    EMU_ERR_ALLOC = -3,           /* workspace or staging allocation failed */
+    EMU_ERR_LAUNCH = -4,          /* a kernel launch failed */
+    EMU_ERR_TIMEOUT = -5,         /* a device-side wait ran out (see the errors note) */
+    EMU_ERR_CUDA = -6             /* another CUDA runtime error */
+} emu_status_t;
+
+/* Which implementation emu_sgemm uses for the tensor-core modes. */
+typedef enum {
+    EMU_PATH_AUTO = 0,     /* the library chooses per call */
+    EMU_PATH_TWOPASS = 1,  /* split kernels write the pieces to the workspace, then the GEMM */
+    EMU_PATH_FUSED = 2     /* one kernel loads FP32 tiles and splits them in shared memory */
+} emu_path_t;
+
+/*
+ * emu_sgemm -- C = alpha * op(A) * op(B) + beta * C.
+ *
+ *  transA, transB  0 or 1 (see Storage above).
+ *  M, N, K         op(A) is M x K, op(B) is K x N, C is M x N; each >= 0.
+ *  A, lda          device FP32; lda >= (transA ? M : K), lda >= 1.
+ *  B, ldb          device FP32; ldb >= (transB ? K : N), ldb >= 1.
+ *  C, ldc          device FP32, read (when beta != 0) and written; ldc >= N.
+ *                  C must not overlap A or B.
+ *  mode            an emu_mode_t.
+ *
+ * BF16X9 (the method of Figure 1 of the blog post): every element of op(A)
+ * and op(B) is split exactly into x = x0 + 2^-8 x1 + 2^-16 x2 (three BF16
+ * pieces, rounding to nearest even, signed residuals).  The nine products
+ * a_i b_j are summed on the tensor cores in FP32, band by band with band
+ * b = i + j taken in the order 4, 3, 2, 1, 0, and the accumulator is scaled
+ * by 2^-8 between bands, so the result is
+ *     sum_b 2^-8b S_b,  S_b = sum_{i+j=b} sum_k a_i[m,k] b_j[k,n],
+ * accumulated smallest band first.  TF32X3 (Figure 2): x = hi + lo (TF32,
+ * nearest even, no scaling); the band hi*lo + lo*hi is accumulated first,
+ * then hi*hi; lo*lo is dropped.  The epilogue is C = alpha*acc + beta*C in
+ * FP32; C is not read when beta == 0, and A, B are not read when alpha == 0
+ * or K == 0 (BLAS convention).  M == 0 or N == 0 is a no-op.
+ *
+ * Accuracy: for BF16X9 every element satisfies
+ *     |C - C_exact| <= (2K + 2) 2^-24 |alpha| sum_k |a_mk||b_kn| + 2^-23 |beta C|
+ * (TF32X3 adds 2^-20 |alpha| sum_k |a_mk||b_kn|), where C_exact is the result
+ * in exact arithmetic.
+ *
+ * Returns EMU_OK once the kernels are enqueued on `stream`.
+ */
+emu_status_t emu_sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                       float alpha, const float* A, int64_t lda,
+                       const float* B, int64_t ldb,
+                       float beta, float* C, int64_t ldc,
+                       int mode, emu_stream_t stream);
+
+/*
+ * emu_sgemm_host -- emu_sgemm on HOST buffers, end to end.
+ *
+ * A, B and C are host pointers (pageable or pinned).  The call copies op's
+ * operands (and C when beta != 0) to library-owned device buffers on
+ * `stream`, runs emu_sgemm there and copies C back, then synchronises the
+ * stream before it returns, so C holds the result on return.  Same
+ * arguments, layout and error codes as emu_sgemm; the device buffers are
+ * grown on demand and released by emu_shutdown().
+ */
+emu_status_t emu_sgemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                            float alpha, const float* A, int64_t lda,
+                            const float* B, int64_t ldb,
+                            float beta, float* C, int64_t ldc,
+                            int mode, emu_stream_t stream);
+
+/*
+ * emu_split_bf16x3 -- the split/pack step of BF16X9 on its own.
+ *
+ * Writes the three BF16 pieces (raw bit patterns) of op(X), rows x cols:
+ * P_i[r * ldp + c] holds piece i of op(X)[r][c] with
+ *     op(X)[r][c] = P0 + 2^-8 P1 + 2^-16 P2   exactly, for every finite value.
+ * This is the same kernel the two-pass GEMM uses to fill its workspace (A is
+ * split as op(A); B as op(B)^T, i.e. with trans = !transB, so that both are
+ * K-major).  X: device FP32 with leading dimension ld (ld >= (trans ? rows :
+ * cols)); P0, P1, P2: device, ldp >= cols; columns cols..ldp-1 are not
+ * written.  Rounding to nearest even; a finite value whose nearest BF16 is
+ * infinite takes the truncated BF16; +-inf -> (x, +0, +0); NaN -> 0x7FC0 in
+ * all three.
+ */
+emu_status_t emu_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_t ld,
+                              int trans, uint16_t* P0, uint16_t* P1, uint16_t* P2,
+                              int64_t ldp, emu_stream_t stream);
+
+/*
+ * emu_split_tf32x2 -- the split step of TF32X3 on its own: HI and LO (FP32
+ * containers with the low 13 mantissa bits zero) with op(X) ~ HI + LO, HI the
+ * nearest TF32 of x (ties even), LO the nearest TF32 of x - HI.  Same layout,
+ * ownership and rules as emu_split_bf16x3.
+ */
+emu_status_t emu_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld,
+                              int trans, float* HI, float* LO, int64_t ldp,
+                              emu_stream_t stream);
+
+/* Select the implementation of the tensor-core modes for later calls on this
+ * process (EMU_PATH_AUTO by default; the environment variable
+ * EMU_SGEMM_PATH=auto|twopass|fused sets the initial value).  Not
+ * thread-safe with respect to concurrent emu_sgemm calls. */
+emu_status_t emu_set_path(int path);
+int emu_get_path(void);
+
+/* Bytes of workspace the two-pass path needs for one call of this shape. */
+size_t emu_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
+
+/* Read the sticky device error word of the current device (synchronises the
+ * device).  Returns EMU_OK when no device-side wait has given up. */
+emu_status_t emu_get_last_device_error(void);
+/* Clear that word (synchronises the device). */
+emu_status_t emu_clear_device_error(void);
+
+/* Exercise the bounded-wait machinery: one tiny kernel waits on an mbarrier
+ * that nothing arrives on, gives up after `limit_us` microseconds (1 to
+ * 1,000,000), records EMU_ERR_TIMEOUT and exits normally.  Returns the
+ * device error word after the kernel (EMU_ERR_TIMEOUT when the machinery
+ * works); the word is left set. */
+emu_status_t emu_selftest_timeout(int limit_us, emu_stream_t stream);
+
+/* Kernel-level timing.  While enabled, every kernel that emu_sgemm launches
+ * is bracketed by CUDA events recorded on the caller's stream.
+ * emu_profile_read synchronises on the recorded events and returns, for
+ * kernel kind `kind` (0 = split/pack, 1 = tensor-core GEMM, 2 = fused GEMM,
+ * 3 = SIMT GEMM, 4 = epilogue-only scale), the number of launches and their
+ * summed duration in milliseconds since the last emu_profile_enable(1). */
+emu_status_t emu_profile_enable(int on);
+emu_status_t emu_profile_read(int kind, int64_t* launches, double* total_ms);
+
+/* Name of a status code (static string). */
+const char* emu_status_string(emu_status_t status);
+
+/* Release the workspace and staging buffers of every device. */
+emu_status_t emu_shutdown(void);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int emu_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EMU_SGEMM_H */

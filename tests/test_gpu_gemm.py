@@ -1,0 +1,238 @@
+"""GPU parity of the emulated GEMM (BF16x9, TF32x3) and the SIMT baseline
+against the CPU oracle.
+
+Criterion (element-wise, from the method's accuracy claim): |C - C_ref| <=
+(2K + 2) 2^-24 |alpha| S_abs + 2^-23 |beta C0| (+2^-20 |alpha| S_abs for
+TF32x3), and a relative Frobenius error <= 2e-6 on normally distributed
+inputs.  Small cases are compared on every element; the full-size workloads
+on 4096 sampled outputs plus the corners, which the oracle computes one by
+one.  Closed-form cases (identity, 8x8x8 integers) must match exactly."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import checks
+from fp32_emulated_gemm_split_gb300 import workloads as W
+from gpu_util import emu_module, to_dev
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["bf16x9", "tf32x3", "fp32_simt"]
+
+
+@pytest.fixture(scope="module")
+def emu():
+    return emu_module()
+
+
+def _run(emu, A, B, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None, mode="bf16x9"):
+    import torch
+    M = A.shape[1] if transA else A.shape[0]
+    N = B.shape[0] if transB else B.shape[1]
+    dC = to_dev(C0) if C0 is not None else torch.full((M, N), float("nan"), device="cuda")
+    emu.emu_sgemm(to_dev(A), to_dev(B), dC, transA=transA, transB=transB, alpha=alpha,
+                  beta=beta, mode=mode)
+    torch.cuda.synchronize()
+    return dC.cpu().numpy()
+
+
+def _bound_mode(mode):
+    return "tf32x3" if mode == "tf32x3" else "bf16x9"
+
+
+# ------------------------------------------------------------ closed forms --
+
+@pytest.mark.parametrize("mode", ["bf16x9", "fp32_simt"])
+def test_identity_gives_the_other_operand_bitwise(emu, mode):
+    X = W.normal(W.rng(31), (256, 256))
+    I = np.eye(256, dtype=np.float32)
+    assert np.array_equal(_run(emu, I, X, mode=mode), X)
+    assert np.array_equal(_run(emu, X, I, mode=mode), X)
+
+
+def test_golden_bruteforce_cases_exact(emu):
+    from test_oracle_gemm import _read_golden
+    path = os.path.join(os.path.dirname(__file__), "golden", "bruteforce_8x8x8.txt")
+    for name, A, B, alpha, beta, C0, expect in _read_golden(path):
+        for mode in ("bf16x9", "fp32_simt"):
+            C = _run(emu, A, B, alpha=alpha, beta=beta, C0=C0, mode=mode)
+            assert np.array_equal(C, expect), (name, mode)
+
+
+def test_ones_gives_K(emu):
+    for mode in MODES:
+        C = _run(emu, np.ones((130, 1000), np.float32), np.ones((1000, 260), np.float32), mode=mode)
+        assert np.all(C == 1000), mode
+
+
+# ------------------------------------------------------- small, every element --
+
+SHAPES = [(1, 1, 1), (7, 13, 5), (128, 256, 64), (129, 257, 65), (200, 300, 136),
+          (300, 513, 1000), (64, 40, 2048)]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_ragged_shapes_every_element(emu, mode, shape, transA, transB):
+    M, N, K = shape
+    r = W.rng(M * 7 + N * 3 + K + 2 * transA + transB)
+    A = W.uniform(r, (K, M) if transA else (M, K))
+    B = W.uniform(r, (N, K) if transB else (K, N))
+    C0 = W.uniform(r, (M, N))
+    C = _run(emu, A, B, transA, transB, 1.5, -0.75, C0, mode)
+    Cref, Sabs = oracle.gemm_ref(A, B, transA, transB, 1.5, -0.75, C0)
+    ratio = checks.error_ratio(C, Cref, Sabs, K, 1.5, -0.75, C0, mode=_bound_mode(mode))
+    assert ratio <= 1.0, ratio
+
+
+def test_strided_operands_and_output(emu):
+    import torch
+    r = W.rng(5)
+    Abig = W.normal(r, (300, 520))
+    Bbig = W.normal(r, (260, 400))
+    Cbig = W.normal(r, (300, 700))
+    A, B = Abig[:, 8:264], Bbig[:256, 16:392]          # rows 16-byte aligned, ld > cols
+    dA, dB, dC = to_dev(Abig)[:, 8:264], to_dev(Bbig)[:256, 16:392], to_dev(Cbig)
+    Cv = dC[:, 100:476]
+    emu.emu_sgemm(dA, dB, Cv, alpha=1.0, beta=0.5)
+    torch.cuda.synchronize()
+    C0 = Cbig[:, 100:476]
+    Cref, Sabs = oracle.gemm_ref(A, B, alpha=1.0, beta=0.5, C0=C0)
+    out = dC.cpu().numpy()
+    assert checks.error_ratio(out[:, 100:476], Cref, Sabs, 256, 1.0, 0.5, C0) <= 1.0
+    untouched = np.ones(700, bool)
+    untouched[100:476] = False
+    assert np.array_equal(out[:, untouched], Cbig[:, untouched])
+
+
+def test_transposed_views_are_handled(emu):
+    import torch
+    r = W.rng(8)
+    A = W.normal(r, (96, 160))
+    B = W.normal(r, (200, 160))                        # used as B^T
+    dC = emu.emu_sgemm(to_dev(A), to_dev(B).t())       # a column-major view of B
+    torch.cuda.synchronize()
+    Cref, Sabs = oracle.gemm_ref(A, B, transB=True)
+    assert checks.error_ratio(dC.cpu().numpy(), Cref, Sabs, 160, 1.0, 0.0) <= 1.0
+
+
+# ------------------------------------------------------------- workloads --
+
+def _sampled_check(emu, g, mode, n=4096):
+    import torch
+    A, B, C0 = W.generate(g)
+    dA, dB = to_dev(A), to_dev(B)
+    dC = to_dev(C0) if C0 is not None else torch.empty((g.M, g.N), device="cuda")
+    emu.emu_sgemm(dA, dB, dC, transA=g.transA, transB=g.transB, alpha=g.alpha, beta=g.beta,
+                  mode=mode)
+    torch.cuda.synchronize()
+    mi, ni = W.sample_pairs(g.M, g.N, n)
+    # whole first and last rows as well
+    mi = np.concatenate([mi, np.zeros(g.N, np.int64), np.full(g.N, g.M - 1, np.int64)])
+    ni = np.concatenate([ni, np.arange(g.N), np.arange(g.N)])
+    got = dC[torch.from_numpy(mi).cuda(), torch.from_numpy(ni).cuda()].cpu().numpy()
+    Cref, Sabs = oracle.gemm_ref(A, B, g.transA, g.transB, g.alpha, g.beta, C0, pairs=(mi, ni))
+    C0s = C0[mi, ni] if C0 is not None else None
+    ratio = checks.error_ratio(got, Cref, Sabs, g.K, g.alpha, g.beta, C0s, mode=_bound_mode(mode))
+    relf = checks.rel_frobenius(got, Cref)
+    return ratio, relf, dC, (A, B, C0)
+
+
+def test_square256_full_and_more_accurate_than_simt(emu):
+    g = W.WORKLOADS["square256_uniform"]
+    A, B, _ = W.generate(g)
+    Cref, Sabs = oracle.gemm_ref(A, B)
+    errs = {}
+    for mode in MODES:
+        C = _run(emu, A, B, mode=mode)
+        assert checks.error_ratio(C, Cref, Sabs, g.K, 1.0, 0.0, mode=_bound_mode(mode)) <= 1.0
+        errs[mode] = checks.rel_frobenius(C, Cref)
+        assert errs[mode] <= checks.FROBENIUS_TOL
+    # the pages: BF16x9 matches or beats native FP32 against an FP64 reference
+    assert errs["bf16x9"] <= errs["fp32_simt"]
+
+
+@pytest.mark.parametrize("name", ["mlip192_k256_n256", "mlip192_k256_n1024", "mlip192_k1024_n256"])
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_mlip192_every_element(emu, name, mode):
+    g = W.WORKLOADS[name]
+    A, B, _ = W.generate(g)
+    C = _run(emu, A, B, transB=g.transB, mode=mode)
+    Cref, Sabs = oracle.gemm_ref(A, B, transB=g.transB)
+    assert checks.error_ratio(C, Cref, Sabs, g.K, 1.0, 0.0, mode=mode) <= 1.0
+    assert checks.rel_frobenius(C, Cref) <= checks.FROBENIUS_TOL
+
+
+@pytest.mark.parametrize("name", ["mlip17280_k256_n256", "mlip17280_k256_n1024",
+                                  "mlip17280_k1024_n256"])
+def test_mlip17280_sampled(emu, name):
+    ratio, relf, _, _ = _sampled_check(emu, W.WORKLOADS[name], "bf16x9")
+    assert ratio <= 1.0 and relf <= checks.FROBENIUS_TOL, (ratio, relf)
+
+
+def test_stress4096_alpha_beta_sampled(emu):
+    ratio, _, _, _ = _sampled_check(emu, W.WORKLOADS["stress4096"], "bf16x9")
+    assert ratio <= 1.0, ratio
+
+
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_square8192_sampled(emu, mode):
+    ratio, relf, _, _ = _sampled_check(emu, W.WORKLOADS["square8192_normal"], mode)
+    assert ratio <= 1.0 and relf <= checks.FROBENIUS_TOL, (ratio, relf)
+
+
+# ------------------------------------------------------------ edge cases --
+
+def test_k_zero_and_alpha_zero(emu):
+    import torch
+    r = W.rng(3)
+    C0 = W.uniform(r, (70, 90))
+    for mode in MODES:
+        dC = to_dev(C0)
+        emu.emu_sgemm(torch.empty((70, 0), device="cuda"), torch.empty((0, 90), device="cuda"), dC,
+                      beta=0.5, mode=mode)
+        torch.cuda.synchronize()
+        assert np.array_equal(dC.cpu().numpy(), np.float32(0.5) * C0)
+        A = torch.full((70, 30), float("nan"), device="cuda")
+        B = torch.ones((30, 90), device="cuda")
+        dC = to_dev(C0)
+        emu.emu_sgemm(A, B, dC, alpha=0.0, beta=2.0, mode=mode)   # A, B not read
+        torch.cuda.synchronize()
+        assert np.array_equal(dC.cpu().numpy(), 2 * C0)
+
+
+def test_beta_zero_does_not_read_c(emu):
+    import torch
+    A = torch.ones((40, 20), device="cuda")
+    B = torch.ones((20, 50), device="cuda")
+    for mode in MODES:
+        C = torch.full((40, 50), float("nan"), device="cuda")
+        emu.emu_sgemm(A, B, C, beta=0.0, mode=mode)
+        torch.cuda.synchronize()
+        assert torch.all(C == 20), mode
+
+
+def test_host_entry_point_matches_device_path(emu):
+    r = W.rng(17)
+    A = W.normal(r, (300, 200))
+    B = W.normal(r, (200, 260))
+    C0 = W.normal(r, (300, 260))
+    dev = _run(emu, A, B, alpha=0.5, beta=1.0, C0=C0)
+    host = emu.emu_sgemm_host(A, B, C0.copy(), alpha=0.5, beta=1.0)
+    assert np.array_equal(dev, host)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(emu):
+    emu.emu_clear_device_error()
+    assert emu.emu_selftest_timeout(2000) == -5          # EMU_ERR_TIMEOUT
+    emu.emu_clear_device_error()
+    assert emu.emu_get_last_device_error() == 0
+    C = _run(emu, np.eye(8, dtype=np.float32), np.ones((8, 8), np.float32))
+    assert np.all(C == 1)
+
+
+def test_no_device_error_recorded(emu):
+    assert emu.emu_get_last_device_error() == 0
