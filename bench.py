@@ -74,7 +74,7 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
@@ -136,7 +136,7 @@ def bench_gpu(args):
     _build.build()
     import fp32_emulated_gemm_split_gb300 as emu
 
-    g = W.with_mode(W.WORKLOADS[args.workload], args.mode or W.WORKLOADS[args.workload].mode)
+    g = pick_workload(W, args)
     A, B, C0 = W.generate(g)
     dA = torch.from_numpy(A).cuda()
     dB = torch.from_numpy(B).cuda()
@@ -230,7 +230,8 @@ def bench_gpu(args):
     out["clocks"] = clocks.summary()
 
     if rank == 0:
-        out["e2e"] = bench_e2e(emu, g, A, B, C0, stream, args)
+        if not args.no_e2e:
+            out["e2e"] = bench_e2e(emu, g, A, B, C0, stream, args)
         if not args.no_simt and g.mode != "fp32_simt":
             out["simt_fp32"] = bench_simt(emu, g, dA, dB, dC, stream)
         if not args.no_cpu:
@@ -240,6 +241,18 @@ def bench_gpu(args):
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def pick_workload(W, args):
+    """The named workload, optionally with another mode or another M,N,K
+    (same value distribution) for small profiling runs."""
+    from dataclasses import replace
+    base = W.WORKLOADS[args.workload]
+    g = W.with_mode(base, args.mode or base.mode)
+    if args.shape:
+        M, N, K = (int(v) for v in args.shape.split(","))
+        g = replace(g, name=f"{base.name}@{M}x{N}x{K}", M=M, N=N, K=K)
+    return g
 
 
 def load_traffic(kernel, workload, mode):
@@ -339,7 +352,7 @@ def bench_reference(args):
     import numpy as np
     from fp32_emulated_gemm_split_gb300 import workloads as W
     import oracle
-    g = W.with_mode(W.WORKLOADS[args.workload], args.mode or W.WORKLOADS[args.workload].mode)
+    g = pick_workload(W, args)
     A, B, C0 = W.generate(g)
     oracle.build()
     fn = {"bf16x9": oracle.gemm_bf16x9, "tf32x3": oracle.gemm_tf32x3,
@@ -381,7 +394,7 @@ def bench_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="square8192_normal")
     ap.add_argument("--mode", default=None, choices=[None, "bf16x9", "tf32x3", "fp32_simt"])
@@ -389,6 +402,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-simt", action="store_true", help="skip the SIMT FP32 context number")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--shape", default=None, help="M,N,K override (same distribution)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps
     if args.impl == "reference":

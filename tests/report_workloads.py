@@ -1,0 +1,159 @@
+"""Accuracy and speed of every workload and mode on the GPU (a report, not a
+test): one JSON line per (workload, mode) with
+
+  tflops        effective 2MNK/t of emu_sgemm (CUDA events, median of runs)
+  pct_p9        that figure as a percentage of the measured BF16 peak / 9
+  max_ratio     max |C - C_ref| / bound over the checked outputs (<= 1 passes)
+  rel_frob      relative Frobenius error over the checked outputs
+  checked       "all" or the number of sampled outputs
+
+plus, per workload, the library's SIMT FP32 kernel and, for context, cuBLAS
+FP32 through torch.matmul with and without CUBLAS_EMULATE_SINGLE_PRECISION=1
+(the cuBLAS BF16x9 path the pages use; run in a child process because cuBLAS
+reads the variable when it starts).
+
+  python tests/report_workloads.py [--workloads a,b] [--out file.jsonl] [--no-cublas]
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+sys.path.insert(0, ROOT)
+sys.path.insert(0, HERE)
+
+import oracle  # noqa: E402
+from oracle import checks  # noqa: E402
+from fp32_emulated_gemm_split_gb300 import workloads as W  # noqa: E402
+
+
+def time_call(fn, reps=10, warm=3):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e))
+    return float(np.median(times))
+
+
+def cublas_child(name, emulate):
+    """Time torch.matmul FP32 on the workload in a child process."""
+    code = f"""
+import sys, json, torch, numpy as np
+sys.path.insert(0, {ROOT!r})
+torch.backends.cuda.matmul.allow_tf32 = False
+from fp32_emulated_gemm_split_gb300 import workloads as W
+g = W.WORKLOADS[{name!r}]
+A, B, C0 = W.generate(g)
+a = torch.from_numpy(A).cuda(); b = torch.from_numpy(B).cuda()
+a = a.t() if g.transA else a
+b = b.t() if g.transB else b
+f = lambda: torch.matmul(a, b)
+for _ in range(3): f()
+torch.cuda.synchronize()
+ts = []
+for _ in range(10):
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(); f(); e.record(); torch.cuda.synchronize(); ts.append(s.elapsed_time(e))
+print(json.dumps({{"ms": float(np.median(ts))}}))
+"""
+    env = dict(os.environ)
+    if emulate:
+        env["CUBLAS_EMULATE_SINGLE_PRECISION"] = "1"
+        env["CUBLAS_EMULATION_STRATEGY"] = "eager"
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=600)
+    if r.returncode != 0:
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])["ms"]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workloads", default=",".join(n for n in W.WORKLOADS if not n.endswith("_tf32x3")))
+    ap.add_argument("--out", default=None)
+    ap.add_argument("--no-cublas", action="store_true")
+    ap.add_argument("--samples", type=int, default=4096)
+    args = ap.parse_args()
+
+    import torch
+    import fp32_emulated_gemm_split_gb300 as emu
+    torch.cuda.set_device(0)
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {"bf16_tflops": 1900.0}
+    p9 = peaks["bf16_tflops"] / 9.0
+    out = open(args.out, "a") if args.out else None
+
+    for name in args.workloads.split(","):
+        g0 = W.WORKLOADS[name]
+        A, B, C0 = W.generate(g0)
+        dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        full = g0.M * g0.N * g0.K <= 4e9
+        if full:
+            Cref, Sabs = oracle.gemm_ref(A, B, g0.transA, g0.transB, g0.alpha, g0.beta, C0)
+            mi = ni = None
+        else:
+            mi, ni = W.sample_pairs(g0.M, g0.N, args.samples)
+            Cref, Sabs = oracle.gemm_ref(A, B, g0.transA, g0.transB, g0.alpha, g0.beta, C0,
+                                         pairs=(mi, ni))
+        modes = ["bf16x9", "tf32x3", "fp32_simt"]
+        for mode in modes:
+            dC = torch.from_numpy(C0).cuda() if C0 is not None else torch.empty((g0.M, g0.N), device="cuda")
+            dC0 = dC.clone() if C0 is not None else None
+
+            def run():
+                if dC0 is not None:
+                    dC.copy_(dC0)
+                emu.emu_sgemm(dA, dB, dC, transA=g0.transA, transB=g0.transB, alpha=g0.alpha,
+                              beta=g0.beta, mode=mode)
+
+            run()
+            torch.cuda.synchronize()
+            if full:
+                got = dC.cpu().numpy()
+                C0s = C0
+            else:
+                got = dC[torch.from_numpy(mi).cuda(), torch.from_numpy(ni).cuda()].cpu().numpy()
+                C0s = C0[mi, ni] if C0 is not None else None
+            bmode = "tf32x3" if mode == "tf32x3" else "bf16x9"
+            ratio = checks.error_ratio(got, Cref, Sabs, g0.K, g0.alpha, g0.beta, C0s, mode=bmode)
+            relf = checks.rel_frobenius(got, Cref)
+            reps = 10 if g0.flops < 2e12 else 5
+            ms = time_call(run, reps=reps)
+            if dC0 is not None:   # subtract the restore copy of C
+                ms -= time_call(lambda: dC.copy_(dC0), reps=reps)
+            tf = g0.flops / (ms * 1e-3) / 1e12
+            rec = {"workload": name, "mode": mode, "M": g0.M, "N": g0.N, "K": g0.K,
+                   "ms": round(ms, 4), "tflops": round(tf, 2), "pct_p9": round(100 * tf / p9, 1),
+                   "max_ratio": ratio, "rel_frob": relf,
+                   "checked": "all" if full else int(mi.size)}
+            print(json.dumps(rec), flush=True)
+            if out:
+                out.write(json.dumps(rec) + "\n")
+        if not args.no_cublas and g0.mode == "bf16x9":
+            for emulate in (False, True):
+                ms = cublas_child(name, emulate)
+                rec = {"workload": name, "mode": "cublas_" + ("bf16x9_env" if emulate else "fp32"),
+                       "ms": ms, "tflops": None if ms is None else round(g0.flops / (ms * 1e-3) / 1e12, 2)}
+                print(json.dumps(rec), flush=True)
+                if out:
+                    out.write(json.dumps(rec) + "\n")
+        del dA, dB
+        torch.cuda.empty_cache()
+    assert emu.emu_get_last_device_error() == 0
+
+
+if __name__ == "__main__":
+    main()
