@@ -83,6 +83,17 @@ emu_status_t from_cuda(cudaError_t e) {
     return EMU_ERR_CUDA;
 }
 
+// Which tensor-core kernel the two-pass path uses: 2 = CTA-pair persistent
+// kernel (default), 1 = one CTA per 128 x 256 tile.  EMU_SGEMM_TC=1|2.
+int tc_variant() {
+    static int v = 0;
+    if (v == 0) {
+        const char* s = std::getenv("EMU_SGEMM_TC");
+        v = (s && s[0] == '1') ? 1 : 2;
+    }
+    return v;
+}
+
 int read_path_env() {
     const char* s = std::getenv("EMU_SGEMM_PATH");
     if (!s) return EMU_PATH_AUTO;
@@ -233,22 +244,26 @@ emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N
     if (e != cudaSuccess) return from_cuda(e);
 
     const int box_cols = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
+    const bool pair = tc_variant() == 2;
+    const int tile_m = pair ? 256 : kTcBM, tile_n = pair ? 256 : kTcBN;
+    const int box_a = pair ? 128 : kTcBM, box_b = pair ? 128 : kTcBN;
     CUtensorMap mapA, mapB;
-    st = make_plane_map(&mapA, wa, tf32, M, K, ldp, planes, box_cols, kTcBM);
+    st = make_plane_map(&mapA, wa, tf32, M, K, ldp, planes, box_cols, box_a);
     if (st != EMU_OK) return st;
-    st = make_plane_map(&mapB, wb, tf32, N, K, ldp, planes, box_cols, kTcBN);
+    st = make_plane_map(&mapB, wb, tf32, N, K, ldp, planes, box_cols, box_b);
     if (st != EMU_OK) return st;
 
     TcGemmParams p;
     p.err = d->err;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
     p.num_kb = (int)((K + box_cols - 1) / box_cols);
-    p.tiles_m = (int)((M + kTcBM - 1) / kTcBM);
-    p.tiles_n = (int)((N + kTcBN - 1) / kTcBN);
+    p.tiles_m = (int)((M + tile_m - 1) / tile_m);
+    p.tiles_n = (int)((N + tile_n - 1) / tile_n);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     {
         ProfScope ps(1, stream);
-        e = launch_gemm_tc(tf32, mapA, mapB, p, stream);
+        e = pair ? launch_gemm_tc2(tf32, mapA, mapB, p, d->sms, stream)
+                 : launch_gemm_tc(tf32, mapA, mapB, p, stream);
     }
     return from_cuda(e);
 }
