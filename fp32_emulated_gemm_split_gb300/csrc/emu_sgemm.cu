@@ -83,13 +83,14 @@ emu_status_t from_cuda(cudaError_t e) {
     return EMU_ERR_CUDA;
 }
 
-// Which tensor-core kernel the two-pass path uses: 2 = CTA-pair persistent
-// kernel (default), 1 = one CTA per 128 x 256 tile.  EMU_SGEMM_TC=1|2.
+// Which tensor-core kernel the two-pass path uses: 3 = CTA pairs with the
+// bands accumulated in FP32 registers (default), 2 = CTA pairs accumulating
+// in tensor memory, 1 = one CTA per 128 x 256 tile.  EMU_SGEMM_TC=1|2|3.
 int tc_variant() {
     static int v = 0;
     if (v == 0) {
         const char* s = std::getenv("EMU_SGEMM_TC");
-        v = (s && s[0] == '1') ? 1 : 2;
+        v = (s && (s[0] == '1' || s[0] == '2')) ? s[0] - '0' : 3;
     }
     return v;
 }
@@ -244,7 +245,8 @@ emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N
     if (e != cudaSuccess) return from_cuda(e);
 
     const int box_cols = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
-    const bool pair = tc_variant() == 2;
+    const int variant = tc_variant();
+    const bool pair = variant >= 2;
     const int tile_m = pair ? 256 : kTcBM, tile_n = pair ? 256 : kTcBN;
     const int box_a = pair ? 128 : kTcBM, box_b = pair ? 128 : kTcBN;
     CUtensorMap mapA, mapB;
@@ -262,8 +264,9 @@ emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     {
         ProfScope ps(1, stream);
-        e = pair ? launch_gemm_tc2(tf32, mapA, mapB, p, d->sms, stream)
-                 : launch_gemm_tc(tf32, mapA, mapB, p, stream);
+        e = variant == 3 ? launch_gemm_promote(tf32, mapA, mapB, p, d->sms, stream)
+            : variant == 2 ? launch_gemm_tc2(tf32, mapA, mapB, p, d->sms, stream)
+                           : launch_gemm_tc(tf32, mapA, mapB, p, stream);
     }
     return from_cuda(e);
 }

@@ -39,78 +39,6 @@ constexpr uint32_t kTmemCols2 = 512;                 // two accumulators
 template <int S>
 constexpr int smem_bytes2() { return S * kStage + 1024 + 1024; }
 
-// ---------------------------------------------------------- cluster PTX --
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
-                 :: "r"(cluster_addr) : "memory");
-}
-
-// Tensor copy into this CTA's shared memory whose completion is counted on
-// an mbarrier that may live in the peer CTA of the pair.
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar_cluster, int32_t c0, int32_t c1,
-                                                 int32_t c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
-        ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-        :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster) : "memory");
-}
-
-template <int TF32>
-__device__ __forceinline__ void mma_cta2(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-    if constexpr (TF32) {
-        asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                     " tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
-                     :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
-    } else {
-        asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                     " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-                     :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
-    }
-}
-
-// D = A*B + 2^-8 D (scale-input-d = 8).
-template <int TF32>
-__device__ __forceinline__ void mma_cta2_scaled8(uint32_t d, uint64_t a, uint64_t b,
-                                                 uint32_t idesc) {
-    if constexpr (TF32) {
-        asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, 1, 0;\n"
-                     " tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p, 8;\n}\n"
-                     :: "r"(d), "l"(a), "l"(b), "r"(idesc) : "memory");
-    } else {
-        asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, 1, 0;\n"
-                     " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p, 8;\n}\n"
-                     :: "r"(d), "l"(a), "l"(b), "r"(idesc) : "memory");
-    }
-}
-
-// Arrive on the barrier at this offset in both CTAs of the pair once the
-// MMAs issued so far have completed.
-__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster"
-                 ".multicast::cluster.b64 [%0], %1;" :: "r"(bar), "h"((uint16_t)3) : "memory");
-}
-
 // ------------------------------------------------------------ schedule --
 
 // Pieces (i, j) in processing order, four bits per pair; band lengths four

@@ -184,6 +184,15 @@ def test_square8192_sampled(emu, mode):
     assert ratio <= 1.0 and relf <= checks.FROBENIUS_TOL, (ratio, relf)
 
 
+def test_bf16x9_at_least_as_accurate_as_fp32_at_long_k(emu):
+    """The pages: BF16x9 matches or beats native FP32 against an FP64
+    reference -- here at K = 8192, where accumulation error dominates."""
+    g = W.Gemm("long_k", 512, 512, 8192, dist="normal", seed=77)
+    _, rel9, _, _ = _sampled_check(emu, g, "bf16x9")
+    _, rel32, _, _ = _sampled_check(emu, g, "fp32_simt")
+    assert rel9 <= rel32, (rel9, rel32)
+
+
 # ------------------------------------------------------------ edge cases --
 
 def test_k_zero_and_alpha_zero(emu):
