@@ -53,6 +53,24 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float) -> float:
+    """The maximum of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, world: int, steps: int, ms_total: float) -> float:
+    """Whole-job TFLOP/s: every rank runs `steps` steps of `flops_per_step`;
+    the job takes as long as its slowest rank (ms_total is that maximum)."""
+    return flops_per_step * world * steps / (ms_total * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------ clocks --
 
 class ClockSampler:
@@ -171,14 +189,10 @@ def bench_gpu(args):
     emu.emu_profile_enable(False)
     assert emu.emu_get_last_device_error() == 0, "device-side wait gave up during the bench"
 
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
-
+    ms_total = max_over_ranks(ms_total)
     ms_step = ms_total / args.steps
     flops = g.flops
-    value = flops * world * args.steps / (ms_total * 1e-3) / 1e12
+    value = job_throughput(flops, world, args.steps, ms_total)
     peaks, peak_src = load_peaks()
     p_bf16 = float(peaks["bf16_tflops"])
     frac9 = value / world / (p_bf16 / 9.0)

@@ -27,7 +27,10 @@ _lib = None
 class EmuError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {emu_status_string(status)} ({status})")
+        detail = ""
+        if status in (-3, -4, -6):
+            detail = f", CUDA: {emu_last_cuda_error()}"
+        super().__init__(f"{where}: {emu_status_string(status)} ({status}){detail}")
 
 
 def lib() -> ctypes.CDLL:
@@ -71,6 +74,8 @@ def _declare(L):
     L.emu_profile_read.restype = _int
     L.emu_status_string.argtypes = [_int]
     L.emu_status_string.restype = ctypes.c_char_p
+    L.emu_last_cuda_error.argtypes = []
+    L.emu_last_cuda_error.restype = ctypes.c_char_p
     L.emu_version.argtypes = []
     L.emu_version.restype = _int
     return L
@@ -231,6 +236,10 @@ def emu_profile_read(kind) -> tuple[int, float]:
     k = PROFILE_KIND[kind] if isinstance(kind, str) else int(kind)
     _check(lib().emu_profile_read(k, ctypes.byref(n), ctypes.byref(ms)), "emu_profile_read")
     return int(n.value), float(ms.value)
+
+
+def emu_last_cuda_error() -> str:
+    return lib().emu_last_cuda_error().decode()
 
 
 def emu_status_string(status: int) -> str:

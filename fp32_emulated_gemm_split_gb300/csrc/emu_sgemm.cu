@@ -73,8 +73,11 @@ struct ProfScope {
 
 // ----------------------------------------------------------- helpers --
 
+cudaError_t g_last_cuda_error = cudaSuccess;
+
 emu_status_t from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return EMU_OK;
+    g_last_cuda_error = e;
     if (e == cudaErrorMemoryAllocation) return EMU_ERR_ALLOC;
     if (e == cudaErrorLaunchFailure || e == cudaErrorInvalidConfiguration ||
         e == cudaErrorLaunchOutOfResources || e == cudaErrorInvalidDeviceFunction ||
@@ -456,6 +459,8 @@ emu_status_t emu_profile_read(int kind, int64_t* launches, double* total_ms) {
     *total_ms = g_prof_ms[kind];
     return EMU_OK;
 }
+
+const char* emu_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 const char* emu_status_string(emu_status_t s) {
     switch (s) {

@@ -22,13 +22,16 @@
 // CTA stages 128 rows of the A piece and 128 rows of the B^T piece per K
 // block and one tcgen05.mma.cta_group::2 (M = N = 256) reads both CTAs'
 // shared memory.  Persistent: one cluster per SM pair walks the tiles.
-// Warps (320 threads per CTA):
-//   warp 0     TMA producer (both CTAs; completion counted on the leader's
-//              barrier) and tensor-memory allocation
-//   warp 1     MMA issuer (leader CTA only)
-//   warps 2-9  accumulators: warp w owns TMEM lanes 32(w%4)..+31 and the
-//              column half (w-2)/4 of the tile: 128 FP32 registers per
-//              thread; they also write C = alpha*acc + beta*C.
+// Warps (576 threads per CTA):
+//   warp 0      TMA producer (both CTAs; completion counted on the leader's
+//               barrier) and tensor-memory allocation
+//   warp 1      MMA issuer (leader CTA only)
+//   warps 2-17  accumulators: warp w owns TMEM lanes 32(w%4)..+31 and the
+//               column quarter (w-2)/4 of the tile: 64 FP32 registers per
+//               thread; they also write C = alpha*acc + beta*C.
+// (Each SM sub-partition has its own 16K-register file, so per-thread
+// registers are capped by the warps that share a sub-partition; 64 columns
+// per thread keeps the accumulators in registers without spilling.)
 #include "emu_device.cuh"
 
 namespace emu {
@@ -40,7 +43,9 @@ constexpr int kStB = kHalfRows * kTcBKBytes;         // 16 KB
 constexpr int kSt = kStA + kStB;                     // 32 KB per CTA per stage
 constexpr int kStages = 6;
 constexpr int kChunk = 4;                            // stages per TMEM chunk (16 MMAs)
-constexpr int kThreadsP = 320;
+constexpr int kAccWarps = 16;                        // 4 lane quadrants x 4 column quarters
+constexpr int kAccCols = kBN / 4;                    // 64 columns per accumulator thread
+constexpr int kThreadsP = (2 + kAccWarps) * 32;
 constexpr uint32_t kBufCols = 256;
 constexpr uint32_t kTmemColsP = 512;
 constexpr int kSmemP = kStages * kSt + 1024 + 1024;
@@ -80,7 +85,7 @@ __device__ __forceinline__ void tile_of(int tile, int tiles_m, int tiles_n, int&
 }
 
 template <int TF32>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreadsP, 1)
 gemm_promote_kernel(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB, const TcGemmParams p) {
     using O = Order<TF32>;
@@ -108,8 +113,8 @@ gemm_promote_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         mbar_init(cfull0, 1);
         mbar_init(cfull0 + 8, 1);
-        mbar_init(cempty0, 16);          // 8 accumulator warps in each CTA of the pair
-        mbar_init(cempty0 + 8, 16);
+        mbar_init(cempty0, 2 * kAccWarps);   // accumulator warps of both CTAs of the pair
+        mbar_init(cempty0 + 8, 2 * kAccWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -211,16 +216,16 @@ gemm_promote_kernel(const __grid_constant__ CUtensorMap mapA,
     } else if (warp >= 2) {
         // ------------------------------------------------ accumulator warps
         const int q = warp & 3;                        // TMEM lane quadrant
-        const int h = (warp - 2) >> 2;                 // column half of the tile
+        const int h = (warp - 2) >> 2;                 // column quarter of the tile
         const uint32_t cempty_leader0 = map_to_rank(cempty0, 0);
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
         uint32_t chunk = 0;
         bool ok = true;
         for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
-            float acc[128];
+            float acc[kAccCols];
 #pragma unroll
-            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < kAccCols; ++j) acc[j] = 0.0f;
             for (int b = 0; b < O::nbands && ok; ++b) {
                 const float w = O::weight(b);
                 const int nst = O::len(b) * p.num_kb;
@@ -231,15 +236,15 @@ gemm_promote_kernel(const __grid_constant__ CUtensorMap mapA,
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t col0 = tmem + buf * kBufCols + h * 128 + lane_off;
+                    const uint32_t col0 = tmem + buf * kBufCols + h * kAccCols + lane_off;
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        uint32_t r[16];
-                        tmem_ld_32x32b_x16(col0 + 16 * g, r);
+                    for (int g = 0; g < kAccCols / 8; ++g) {
+                        uint32_t r[8];
+                        tmem_ld_32x32b_x8(col0 + 8 * g, r);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            acc[16 * g + j] = fmaf(w, __uint_as_float(r[j]), acc[16 * g + j]);
+                        for (int j = 0; j < 8; ++j)
+                            acc[8 * g + j] = fmaf(w, __uint_as_float(r[j]), acc[8 * g + j]);
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -251,12 +256,12 @@ gemm_promote_kernel(const __grid_constant__ CUtensorMap mapA,
             int tm, tn;
             tile_of(tile, p.tiles_m, p.tiles_n, tm, tn);
             const int row = tm * kBM + int(rank) * kHalfRows + q * 32 + lane;
-            const int col_base = tn * kBN + h * 128;
+            const int col_base = tn * kBN + h * kAccCols;
             if (row < p.M && col_base < p.N) {
                 float* crow = p.C + (int64_t)row * p.ldc + col_base;
-                if (vec && col_base + 128 <= p.N) {
+                if (vec && col_base + kAccCols <= p.N) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 32; ++v4) {
+                    for (int v4 = 0; v4 < kAccCols / 4; ++v4) {
                         float4 v;
                         v.x = p.alpha * acc[4 * v4 + 0];
                         v.y = p.alpha * acc[4 * v4 + 1];
@@ -274,7 +279,7 @@ gemm_promote_kernel(const __grid_constant__ CUtensorMap mapA,
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 128; ++j) {
+                    for (int j = 0; j < kAccCols; ++j) {
                         if (col_base + j < p.N) {
                             float v = p.alpha * acc[j];
                             if (p.beta != 0.0f) v = fmaf(p.beta, crow[j], v);

@@ -196,6 +196,11 @@ emu_status_t emu_selftest_timeout(int limit_us, emu_stream_t stream);
 emu_status_t emu_profile_enable(int on);
 emu_status_t emu_profile_read(int kind, int64_t* launches, double* total_ms);
 
+/* Name of the last CUDA runtime error that an entry point of this library
+ * turned into a non-OK status (for example "cudaErrorLaunchOutOfResources"),
+ * or "cudaSuccess" if none; a static string.  Process-wide, not thread-safe. */
+const char* emu_last_cuda_error(void);
+
 /* Name of a status code (static string). */
 const char* emu_status_string(emu_status_t status);
 
