@@ -97,11 +97,12 @@ typedef enum {
  * BF16X9 (the method of Figure 1 of the blog post): every element of op(A)
  * and op(B) is split exactly into x = x0 + 2^-8 x1 + 2^-16 x2 (three BF16
  * pieces, rounding to nearest even, signed residuals).  The nine products
- * a_i b_j are summed on the tensor cores in FP32, band by band with band
- * b = i + j taken in the order 4, 3, 2, 1, 0, and the accumulator is scaled
- * by 2^-8 between bands, so the result is
+ * a_i b_j are formed on the tensor cores and grouped into bands b = i + j,
+ * taken in the order 4, 3, 2, 1, 0; the result is
  *     sum_b 2^-8b S_b,  S_b = sum_{i+j=b} sum_k a_i[m,k] b_j[k,n],
- * accumulated smallest band first.  TF32X3 (Figure 2): x = hi + lo (TF32,
+ * accumulated in FP32 smallest band first: the tensor core sums short runs
+ * of K (16 MMAs) and each partial is added, times 2^-8b, to an FP32
+ * accumulator with round-to-nearest.  TF32X3 (Figure 2): x = hi + lo (TF32,
  * nearest even, no scaling); the band hi*lo + lo*hi is accumulated first,
  * then hi*hi; lo*lo is dropped.  The epilogue is C = alpha*acc + beta*C in
  * FP32; C is not read when beta == 0, and A, B are not read when alpha == 0
