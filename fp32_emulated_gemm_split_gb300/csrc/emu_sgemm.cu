@@ -86,14 +86,16 @@ emu_status_t from_cuda(cudaError_t e) {
     return EMU_ERR_CUDA;
 }
 
-// Which tensor-core kernel the two-pass path uses: 3 = CTA pairs with the
-// bands accumulated in FP32 registers (default), 2 = CTA pairs accumulating
-// in tensor memory, 1 = one CTA per 128 x 256 tile.  EMU_SGEMM_TC=1|2|3.
+// Which tensor-core kernel the two-pass path uses: 3 = CTA pairs, each band
+// over all of K in 16-MMA chunks summed in FP32 registers (default); 4 = CTA
+// pairs, one K block at a time with its bands in TMEM and the blocks summed
+// in FP32 registers; 2 = CTA pairs accumulating all of K in TMEM; 1 = one CTA
+// per 128 x 256 tile accumulating in TMEM.  EMU_SGEMM_TC=1..4.
 int tc_variant() {
     static int v = 0;
     if (v == 0) {
         const char* s = std::getenv("EMU_SGEMM_TC");
-        v = (s && (s[0] == '1' || s[0] == '2')) ? s[0] - '0' : 3;
+        v = (s && s[0] >= '1' && s[0] <= '4') ? s[0] - '0' : 3;
     }
     return v;
 }
@@ -267,7 +269,8 @@ emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     {
         ProfScope ps(1, stream);
-        e = variant == 3 ? launch_gemm_promote(tf32, mapA, mapB, p, d->sms, stream)
+        e = variant == 4 ? launch_gemm_kblock(tf32, mapA, mapB, p, d->sms, stream)
+            : variant == 3 ? launch_gemm_promote(tf32, mapA, mapB, p, d->sms, stream)
             : variant == 2 ? launch_gemm_tc2(tf32, mapA, mapB, p, d->sms, stream)
                            : launch_gemm_tc(tf32, mapA, mapB, p, stream);
     }
