@@ -53,6 +53,8 @@ def _declare(L):
     for name in ("emu_sgemm", "emu_sgemm_host"):
         getattr(L, name).argtypes = gemm
         getattr(L, name).restype = _int
+    L.emu_sgemm_noalloc.argtypes = gemm
+    L.emu_sgemm_noalloc.restype = _int
     L.emu_split_bf16x3.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _vp, _i64, _vp]
     L.emu_split_bf16x3.restype = _int
     L.emu_split_tf32x2.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _i64, _vp]
@@ -138,6 +140,29 @@ def emu_sgemm(A, B, C=None, *, transA=False, transB=False, alpha=1.0, beta=0.0,
                          Bs.data_ptr(), ldb, float(beta), C.data_ptr(), max(ldc, N, 1),
                          _mode(mode), _stream_handle(stream))
     _check(st, "emu_sgemm")
+    return C
+
+
+def emu_sgemm_noalloc(A, B, C, *, transA=False, transB=False, alpha=1.0, beta=0.0,
+                      mode="bf16x9", stream=None):
+    """emu_sgemm without any device allocation by the library: the split
+    pieces go to a fixed 64 MiB device array instead of a workspace grown with
+    cudaMalloc (for callers that cannot allocate).  C must be given; a
+    problem whose pieces do not fit raises EmuError(EMU_ERR_INVALID_VALUE).
+    Calls that overlap on the GPU share that array and must be serialised."""
+    As, tA, lda = _stored(A, transA)
+    Bs, tB, ldb = _stored(B, transB)
+    M, K = (As.size(1), As.size(0)) if tA else (As.size(0), As.size(1))
+    K2, N = (Bs.size(1), Bs.size(0)) if tB else (Bs.size(0), Bs.size(1))
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if C.dim() != 2 or C.shape != (M, N) or (C.stride(1) != 1 and N > 1):
+        raise ValueError("C must be an M x N float32 tensor with unit row stride")
+    ldc = C.stride(0) if M > 1 else max(N, 1)
+    st = lib().emu_sgemm_noalloc(int(tA), int(tB), M, N, K, float(alpha), As.data_ptr(), lda,
+                                 Bs.data_ptr(), ldb, float(beta), C.data_ptr(), max(ldc, N, 1),
+                                 _mode(mode), _stream_handle(stream))
+    _check(st, "emu_sgemm_noalloc")
     return C
 
 

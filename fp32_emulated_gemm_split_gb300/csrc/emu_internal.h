@@ -56,4 +56,7 @@ cudaError_t launch_scale(int64_t M, int64_t N, float beta, float* C, int64_t ldc
                          cudaStream_t stream);
 cudaError_t launch_timeout_probe(int* err, uint64_t limit_ns, cudaStream_t stream);
 
+// Device address of the sticky error word of the current device.
+int* device_error_word();
+
 }  // namespace emu

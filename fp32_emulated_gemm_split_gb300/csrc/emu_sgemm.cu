@@ -310,6 +310,18 @@ emu_status_t check_split_args(const void* X, int64_t rows, int64_t cols, int64_t
 }
 
 }  // namespace
+
+// Device address of the sticky error word on the current device (nullptr if
+// it cannot be resolved).  Used by entry points defined in other files.
+int* device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    DeviceState* d = nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (current_device(&d) != EMU_OK) return nullptr;
+    return d->err;
+}
+
 }  // namespace emu
 
 using namespace emu;

@@ -165,6 +165,38 @@ emu_status_t emu_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_
                               int trans, float* HI, float* LO, int64_t ldp,
                               emu_stream_t stream);
 
+/*
+ * emu_sgemm_noalloc -- emu_sgemm that allocates no device memory.
+ *
+ * The pages have no counterpart: this entry point exists for callers of this
+ * library that cannot let it call cudaMalloc -- code whose device memory is
+ * owned by another allocator or a fixed budget (where an extra allocation
+ * can fail or break that owner's accounting), or code that cannot take the
+ * device-wide synchronisation of cudaMalloc / cudaFree in the middle of its
+ * stream work.  Instead of the growable workspace it keeps the split pieces
+ * in one fixed 64 MiB array in device memory, which every GPU that loads
+ * the library holds until the process exits.
+ *
+ * Same arguments, layout, modes, results and error codes as emu_sgemm, and
+ * the same kernels, with one limit: the pieces must fit in the array,
+ *     BF16X9:  3 * 2 * (M + N) * ldp  bytes  (plus < 1 KB of alignment),
+ *     TF32X3:  2 * 4 * (M + N) * ldp  bytes,   ldp = K rounded up to 8,
+ * at most 64 MiB; a larger request returns EMU_ERR_INVALID_VALUE and
+ * launches nothing (FP32_SIMT and the K == 0 / alpha == 0 cases use no
+ * scratch and have no limit).  The first call on a device, with that device
+ * current, resolves the array's device address (cudaGetSymbolAddress) once;
+ * make that first call before any stream capture.  All calls on a device
+ * share the array: calls whose work overlaps on the GPU (other streams,
+ * unordered host threads) race on it and must be serialised by the caller.
+ * Nothing in the array has to start at zero -- each call writes every piece
+ * its GEMM reads -- so the contents a previous call left do not matter.
+ */
+emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                               float alpha, const float* A, int64_t lda,
+                               const float* B, int64_t ldb,
+                               float beta, float* C, int64_t ldc,
+                               int mode, emu_stream_t stream);
+
 /* Select the implementation of the tensor-core modes for later calls on this
  * process (EMU_PATH_AUTO by default; the environment variable
  * EMU_SGEMM_PATH=auto|twopass|fused sets the initial value).  Not
