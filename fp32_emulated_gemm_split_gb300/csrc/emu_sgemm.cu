@@ -86,16 +86,17 @@ emu_status_t from_cuda(cudaError_t e) {
     return EMU_ERR_CUDA;
 }
 
-// Which tensor-core kernel the two-pass path uses: 3 = CTA pairs, each band
-// over all of K in 16-MMA chunks summed in FP32 registers (default); 4 = CTA
-// pairs, one K block at a time with its bands in TMEM and the blocks summed
-// in FP32 registers; 2 = CTA pairs accumulating all of K in TMEM; 1 = one CTA
-// per 128 x 256 tile accumulating in TMEM.  EMU_SGEMM_TC=1..4.
+// Which tensor-core kernel the two-pass path uses: 4 = CTA pairs, one K
+// block at a time with its bands in TMEM and the blocks summed in FP32
+// registers (default); 3 = CTA pairs, each band over all of K in 16-MMA
+// chunks summed in FP32 registers; 2 = CTA pairs accumulating all of K in
+// TMEM; 1 = one CTA per 128 x 256 tile accumulating in TMEM.
+// EMU_SGEMM_TC=1..4.
 int tc_variant() {
     static int v = 0;
     if (v == 0) {
         const char* s = std::getenv("EMU_SGEMM_TC");
-        v = (s && s[0] >= '1' && s[0] <= '4') ? s[0] - '0' : 3;
+        v = (s && s[0] >= '1' && s[0] <= '4') ? s[0] - '0' : 4;
     }
     return v;
 }
