@@ -270,14 +270,25 @@ def pick_workload(W, args):
 
 
 def load_traffic(kernel, workload, mode):
-    """DRAM bytes per launch of `kernel` from a committed ncu summary, if one
-    matches this kernel, workload and mode (profiles/traffic.json)."""
+    """DRAM bytes per launch of `kernel` from a committed ncu capture
+    (profiles/traffic.json), if one matches this kernel, workload and mode and
+    the kernel's source has not changed since the counters were taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    return d.get(f"{kernel}:{workload}:{mode}")
+    rec = d.get(f"{kernel}:{workload}:{mode}")
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+            return None
+    return rec["bytes"]
 
 
 def bench_e2e(emu, g, A, B, C0, stream, args):
