@@ -153,6 +153,8 @@ def bench_gpu(args):
         torch.cuda.set_device(0)
     _build.build()
     import fp32_emulated_gemm_split_gb300 as emu
+    if args.path:
+        emu.emu_set_path(args.path)
 
     g = pick_workload(W, args)
     A, B, C0 = W.generate(g)
@@ -429,6 +431,8 @@ def main(argv=None):
     ap.add_argument("--no-simt", action="store_true", help="skip the SIMT FP32 context number")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--shape", default=None, help="M,N,K override (same distribution)")
+    ap.add_argument("--path", default=None, choices=[None, "auto", "twopass", "fused"],
+                    help="implementation of the tensor-core modes (default: the library's)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -101,6 +101,17 @@ int tc_variant() {
     return v;
 }
 
+// Tile width of the K-block kernel on the two-pass path: 256 (default) or
+// 128 (EMU_SGEMM_BN=128).
+int kblock_bn() {
+    static int v = 0;
+    if (v == 0) {
+        const char* s = std::getenv("EMU_SGEMM_BN");
+        v = (s && std::strcmp(s, "128") == 0) ? 128 : 256;
+    }
+    return v;
+}
+
 int read_path_env() {
     const char* s = std::getenv("EMU_SGEMM_PATH");
     if (!s) return EMU_PATH_AUTO;
@@ -253,8 +264,9 @@ emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N
     const int box_cols = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
     const int variant = tc_variant();
     const bool pair = variant >= 2;
-    const int tile_m = pair ? 256 : kTcBM, tile_n = pair ? 256 : kTcBN;
-    const int box_a = pair ? 128 : kTcBM, box_b = pair ? 128 : kTcBN;
+    const int bn = variant == 4 ? kblock_bn() : 256;
+    const int tile_m = pair ? 256 : kTcBM, tile_n = pair ? bn : kTcBN;
+    const int box_a = pair ? 128 : kTcBM, box_b = pair ? bn / 2 : kTcBN;
     CUtensorMap mapA, mapB;
     st = make_plane_map(&mapA, wa, tf32, M, K, ldp, planes, box_cols, box_a);
     if (st != EMU_OK) return st;
@@ -270,10 +282,53 @@ emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     {
         ProfScope ps(1, stream);
-        e = variant == 4 ? launch_gemm_kblock(tf32, mapA, mapB, p, d->sms, stream)
+        e = variant == 4 ? launch_gemm_kblock(tf32, bn, 0, mapA, mapB, p, d->sms, stream)
             : variant == 3 ? launch_gemm_promote(tf32, mapA, mapB, p, d->sms, stream)
             : variant == 2 ? launch_gemm_tc2(tf32, mapA, mapB, p, d->sms, stream)
                            : launch_gemm_tc(tf32, mapA, mapB, p, stream);
+    }
+    return from_cuda(e);
+}
+
+// Whether op(A) can be read directly by the fused kernel: K-major rows that
+// start on 16-byte boundaries (a TMA requirement).
+bool fused_ok(int mode, int transA, const float* A, int64_t lda) {
+    return mode == EMU_MODE_BF16X9 && transA == 0 && (lda % 4) == 0 &&
+           (reinterpret_cast<uintptr_t>(A) & 15) == 0;
+}
+
+// Fused path: B's three pieces go to the workspace (one split kernel); A is
+// read as FP32 by the GEMM kernel and split in shared memory.
+emu_status_t run_fused(int transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                       int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                       int64_t ldc, DeviceState* d, cudaStream_t stream) {
+    const int64_t ldp = plane_ld(K);
+    emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, (size_t)3 * N * ldp * 2);
+    if (st != EMU_OK) return st;
+    uint16_t* pb = static_cast<uint16_t*>(d->ws);
+    cudaError_t e;
+    {
+        ProfScope ps(0, stream);
+        e = launch_split_bf16x3(B, N, K, ldb, !transB, pb, pb + N * ldp, pb + 2 * N * ldp, ldp,
+                                stream);
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    constexpr int bn = 128;
+    CUtensorMap mapA, mapB;
+    st = make_plane_map(&mapA, A, true, M, K, lda, 1, 32, 128);   // FP32 A: (K, M, 1)
+    if (st != EMU_OK) return st;
+    st = make_plane_map(&mapB, pb, false, N, K, ldp, 3, 64, bn / 2);
+    if (st != EMU_OK) return st;
+    TcGemmParams p;
+    p.err = d->err;
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.num_kb = (int)((K + 63) / 64);
+    p.tiles_m = (int)((M + 255) / 256);
+    p.tiles_n = (int)((N + bn - 1) / bn);
+    p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
+    {
+        ProfScope ps(2, stream);
+        e = launch_gemm_kblock(0, bn, 1, mapA, mapB, p, d->sms, stream);
     }
     return from_cuda(e);
 }
@@ -296,6 +351,9 @@ emu_status_t sgemm_device(int transA, int transB, int64_t M, int64_t N, int64_t 
         return from_cuda(launch_gemm_simt(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
                                           ldc, stream));
     }
+    if (g_path < 0) g_path = read_path_env();
+    if (g_path == EMU_PATH_FUSED && fused_ok(mode, transA, A, lda))
+        return run_fused(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream);
     return run_two_pass(mode == EMU_MODE_TF32X3, transA, transB, M, N, K, alpha, A, lda, B, ldb,
                         beta, C, ldc, d, stream);
 }

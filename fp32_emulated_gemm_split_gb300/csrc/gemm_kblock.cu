@@ -1,6 +1,8 @@
-// gemm_kblock.cu -- the tensor-core GEMM of the two-pass path: one K block
-// at a time, all bands of the block in the tensor core, the blocks summed in
-// FP32 registers.
+// gemm_kblock.cu -- the tensor-core GEMM: one K block at a time, all bands of
+// the block in the tensor core, the blocks summed in FP32 registers.  Used by
+// the two-pass path (pieces of A and B read from the workspace) and by the
+// fused path (A read as FP32 and split in shared memory; B's pieces from the
+// workspace).
 //
 // Method ("Unlocking Tensor Core Performance for Machine Learning Interatomic
 // Potentials", Figure 1 caption; discuss.pytorch.kr summary, section
@@ -9,54 +11,71 @@
 // first.  TF32x3 (Figure 2 and its equation): residual band hi*lo + lo*hi,
 // then hi*hi, no scaling.
 //
-// Schedule.  For each 64-element K block (32 for TF32x3) the three A pieces
-// and three B pieces are staged once, and the tensor core runs the bands of
-// that block smallest first into a fresh TMEM accumulator: band 4 (a2 b2),
-// then band 3 with its first MMA issued with scale-input-d = 8
-// (D = A*B + 2^-8 D), band 2, band 1, band 0 the same way.  The block's
-// partial sum -- sum_b 2^-8b S_b over the block, shifted by the tensor core's
-// own scaling -- is then added to FP32 registers with a round-to-nearest add.
-// Only the four band-0 MMAs of a block run at full magnitude, so the
-// tensor core's truncating accumulation costs a few 2^-24 per block, and the
-// register sum over blocks rounds to nearest.  Each staged piece tile feeds 3
-// MMA groups on average (6 tile loads per 9 groups), a third of the operand
-// traffic of running every band over the whole K.
+// Schedule.  For each 64-element K block (32 for TF32x3) the pieces of A and
+// B are staged once, and the tensor core runs the bands of that block
+// smallest first into a fresh TMEM accumulator: band 4 (a2 b2), then band 3
+// with its first MMA issued with scale-input-d = 8 (D = A*B + 2^-8 D), band
+// 2, band 1, band 0 the same way.  The block's partial -- sum_b 2^-8b S_b over
+// the block, shifted by the tensor core's own scaling -- is then added to
+// FP32 registers with a round-to-nearest add.  Only the four band-0 MMAs of a
+// block run at full magnitude, so the tensor core's truncating accumulation
+// costs a few 2^-24 per block, and the sum over blocks rounds to nearest.
+// Each staged piece tile feeds three MMA groups on average.
 //
-// Layout: a cluster of two CTAs (an SM pair) owns a 256 x 256 tile of C; per
-// K block each CTA stages 128 rows of the three A pieces and of the three B^T
-// pieces (6 x 16 KB, 128-byte swizzled rows); one tcgen05.mma.cta_group::2
-// (M = N = 256) reads both CTAs' shared memory.  Two stages (K blocks) are in
-// flight; each stage has one "full" barrier per piece index so the band-4
-// MMAs start when pieces 2 land.  Persistent: one cluster per SM pair walks
-// the tiles; two TMEM partial buffers let the tensor core fill one block's
-// partial while the other is added to the registers.
+// Layout: a cluster of two CTAs (an SM pair) owns a 256 x BN tile of C
+// (BN = 256 or 128); per K block each CTA stages 128 rows of each A piece and
+// BN/2 rows of each B^T piece (128-byte swizzled rows); one
+// tcgen05.mma.cta_group::2 (M = 256, N = BN) reads both CTAs' shared memory.
+// Each stage has one "full" barrier per piece index so the band-4 MMAs start
+// when pieces 2 land.  Persistent: one cluster per SM pair walks the tiles;
+// two TMEM partial buffers let the tensor core fill one block's partial while
+// the other is added to the registers.
+//
+// Fused A (BF16x9): the producer loads the FP32 A block (128 rows x 64, two
+// 128-byte-swizzled boxes) into one of two staging buffers; the accumulator
+// warps, idle between promotions, split it (16 elements per thread) straight
+// into the swizzled piece layout the MMA reads, make the writes visible to
+// the tensor core (fence.proxy.async) and signal the leader CTA.  The split
+// of block g+1 runs while the tensor core works on block g.
+//
 // Warps (576 threads per CTA):
 //   warp 0      TMA producer (both CTAs; completion counted on the leader's
 //               barriers) and tensor-memory allocation
 //   warp 1      MMA issuer (leader CTA only)
 //   warps 2-17  accumulators: warp w owns TMEM lanes 32(w%4)..+31 and the
-//               column quarter (w-2)/4 of the tile (64 FP32 registers per
-//               thread) and writes C = alpha*acc + beta*C.
+//               column quarter (w-2)/4 of the tile (BN/4 FP32 registers per
+//               thread), write C = alpha*acc + beta*C, and split A when fused.
 #include "emu_device.cuh"
 
 namespace emu {
 namespace {
 
-constexpr int kBM = 256, kBN = 256, kHalfRows = 128;
-constexpr int kPieceTile = kHalfRows * kTcBKBytes;   // 16 KB: 128 rows x 128 bytes
+constexpr int kBM = 256, kHalfRows = 128;
+constexpr int kATile = kHalfRows * kTcBKBytes;       // 16 KB: 128 rows x 128 bytes
 constexpr int kAccWarps = 16;
-constexpr int kAccCols = kBN / 4;                    // 64 columns per accumulator thread
 constexpr int kThreadsK = (2 + kAccWarps) * 32;
-constexpr uint32_t kBufCols = 256;
-constexpr uint32_t kTmemColsK = 512;
+constexpr int kSmemMax = 232448;                      // dynamic shared memory per CTA
+constexpr int kA32Box = 128 * 128;                    // FP32 box: 128 rows x 32 floats
+constexpr int kA32Buf = 2 * kA32Box;                  // one 64-wide K block of FP32 A
+constexpr int kA32Bufs = 2;
 
-template <int TF32>
+template <int TF32, int BN, int FUSED>
 struct KCfg {
     static constexpr int pieces = TF32 ? 2 : 3;
-    static constexpr int stage_bytes = 2 * pieces * kPieceTile;   // A pieces then B pieces
-    static constexpr int stages = TF32 ? 3 : 2;
+    static constexpr int b_rows = BN / 2;                        // B^T rows per CTA
+    static constexpr int b_tile = b_rows * kTcBKBytes;
+    static constexpr int stage_bytes = pieces * (kATile + b_tile);
+    static constexpr int a32_bytes = FUSED ? kA32Bufs * kA32Buf : 0;
+    static constexpr int avail = kSmemMax - 2048 - a32_bytes;
+    static constexpr int stages = avail / stage_bytes > 4 ? 4 : avail / stage_bytes;
     static constexpr int elems = TF32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
-    static constexpr int smem = stages * stage_bytes + 1024 + 1024;
+    static constexpr int acc_cols = BN / 4;
+    static constexpr uint32_t tmem_cols = 2 * BN <= 256 ? 256 : 512;
+    static constexpr int smem = stages * stage_bytes + a32_bytes + 2048;
+    // bytes a piece barrier waits for (both CTAs)
+    static constexpr uint32_t piece_tx = FUSED ? 2 * b_tile : 2 * (kATile + b_tile);
+    static_assert(stages >= 2, "shared memory too small for two stages");
+    static_assert(!(FUSED && TF32), "the fused path splits BF16x9 pieces only");
 };
 
 __device__ __forceinline__ void tile_pos(int tile, int tiles_m, int tiles_n, int& tm, int& tn) {
@@ -89,20 +108,64 @@ __device__ __forceinline__ void mma_pair(uint32_t d, uint32_t a_tile, uint32_t b
     }
 }
 
-template <int TF32>
+__device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) {
+    return uint32_t(lo) | (uint32_t(hi) << 16);
+}
+
+// Split this thread's 16 elements of a 128 x 64 FP32 A block (two swizzled
+// 128 x 32 boxes at `a32`) into the three BF16 pieces at `pieces` (three
+// 128 x 64 swizzled tiles, 16 KB apart).  Thread t of the 512 handles row
+// t/4, elements 16*(t%4) .. +15.
+__device__ __forceinline__ void split_block(const uint8_t* a32, uint8_t* pieces, int t) {
+    const int r = t >> 2, seg = t & 3, sw = r & 7;
+    const uint8_t* box = a32 + (seg >> 1) * kA32Box + r * 128;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int c4 = (seg & 1) * 4 + 2 * half;          // first float4 chunk of these 8
+        const float4 x0 = *reinterpret_cast<const float4*>(box + ((c4 ^ sw) << 4));
+        const float4 x1 = *reinterpret_cast<const float4*>(box + (((c4 + 1) ^ sw) << 4));
+        const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        uint16_t h0[8], h1[8], h2[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) split_bf16x3(v[i], h0[i], h1[i], h2[i]);
+        const int c8 = seg * 2 + half;                     // 16-byte chunk of 8 BF16
+        const int off = r * 128 + ((c8 ^ sw) << 4);
+        *reinterpret_cast<uint4*>(pieces + off) =
+            make_uint4(pack2(h0[0], h0[1]), pack2(h0[2], h0[3]), pack2(h0[4], h0[5]), pack2(h0[6], h0[7]));
+        *reinterpret_cast<uint4*>(pieces + kATile + off) =
+            make_uint4(pack2(h1[0], h1[1]), pack2(h1[2], h1[3]), pack2(h1[4], h1[5]), pack2(h1[6], h1[7]));
+        *reinterpret_cast<uint4*>(pieces + 2 * kATile + off) =
+            make_uint4(pack2(h2[0], h2[1]), pack2(h2[2], h2[3]), pack2(h2[4], h2[5]), pack2(h2[6], h2[7]));
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int TF32, int BN, int FUSED>
 __global__ void __launch_bounds__(kThreadsK, 1)
 gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB, const TcGemmParams p) {
-    using Cfg = KCfg<TF32>;
-    constexpr int S = Cfg::stages, P = Cfg::pieces;
+    using Cfg = KCfg<TF32, BN, FUSED>;
+    constexpr int S = Cfg::stages, P = Cfg::pieces, kAccCols = Cfg::acc_cols;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::stage_bytes);
-    // [0, S*P) piece full (leader), index s*P + piece | [S*P, S*P+S) stage empty |
-    // then 2 partial full, 2 partial empty (leader)
+    uint8_t* a32 = smem + S * Cfg::stage_bytes;           // FP32 A staging (fused only)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(a32 + Cfg::a32_bytes);
+    // [0, S*P) piece full (leader), index s*P + piece | S stage empty |
+    // 2 partial full | 2 partial empty (leader) | fused: S A-pieces ready
+    // (leader), 2 FP32 full, 2 FP32 free
     const int nb_full = S * P;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nb_full + S + 4);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8 * nb_full;
+    const uint32_t cfull0 = empty0 + 8 * S;
+    const uint32_t cempty0 = cfull0 + 16;
+    const uint32_t aready0 = cempty0 + 16;
+    const uint32_t afull0 = aready0 + 8 * S;
+    const uint32_t afree0 = afull0 + 8 * kA32Bufs;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nb_full + 3 * S + 4 + 2 * kA32Bufs);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -110,10 +173,6 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     const bool leader = rank == 0;
     const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
     const int total = p.tiles_m * p.tiles_n;
-    const uint32_t full0 = smem_u32(bars);
-    const uint32_t empty0 = smem_u32(bars + nb_full);
-    const uint32_t cfull0 = smem_u32(bars + nb_full + S);
-    const uint32_t cempty0 = smem_u32(bars + nb_full + S + 2);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < nb_full; ++i) mbar_init(full0 + 8 * i, 1);
@@ -122,6 +181,13 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         mbar_init(cfull0 + 8, 1);
         mbar_init(cempty0, 2 * kAccWarps);   // accumulator warps of both CTAs
         mbar_init(cempty0 + 8, 2 * kAccWarps);
+        if (FUSED) {
+            for (int s = 0; s < S; ++s) mbar_init(aready0 + 8 * s, 2 * kAccWarps);
+            for (int f = 0; f < kA32Bufs; ++f) {
+                mbar_init(afull0 + 8 * f, 1);
+                mbar_init(afree0 + 8 * f, kAccWarps);
+            }
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -132,7 +198,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         __syncwarp();
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
-                     :: "r"(smem_u32(tmem_slot)), "r"(kTmemColsK) : "memory");
+                     :: "r"(smem_u32(tmem_slot)), "r"(Cfg::tmem_cols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
@@ -149,9 +215,21 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             int tm, tn;
             tile_pos(tile, p.tiles_m, p.tiles_n, tm, tn);
             const int arow = tm * kBM + int(rank) * kHalfRows;
-            const int brow = tn * kBN + int(rank) * kHalfRows;
+            const int brow = tn * BN + int(rank) * Cfg::b_rows;
             for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
                 const uint32_t s = kbg % S, ph = (kbg / S) & 1;
+                if (FUSED) {
+                    const uint32_t f = kbg % kA32Bufs, fph = (kbg / kA32Bufs) & 1;
+                    if (!mbar_wait(afree0 + 8 * f, fph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(afull0 + 8 * f, kA32Buf);
+                    const uint32_t dst = smem_u32(a32 + f * kA32Buf);
+                    // FP32 A map is (K, M, 1): the two 32-wide boxes of this K block
+                    tma_load_3d(dst, &mapA, afull0 + 8 * f, kb * 64, arow, 0);
+                    tma_load_3d(dst + kA32Box, &mapA, afull0 + 8 * f, kb * 64 + 32, arow, 0);
+                }
                 if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
                     ok = false;
                     break;
@@ -159,19 +237,19 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
                 // largest piece index first: the first band needs it first
                 for (int pc = P - 1; pc >= 0; --pc) {
-                    const uint32_t fb = full0 + 8 * (s * P + pc);
-                    if (leader) mbar_arrive_expect_tx(fb, 4 * kPieceTile);
+                    if (leader) mbar_arrive_expect_tx(full0 + 8 * (s * P + pc), Cfg::piece_tx);
                     const uint32_t fbl = full_leader0 + 8 * (s * P + pc);
-                    tma_load_3d_pair(st + pc * kPieceTile, &mapA, fbl, kb * Cfg::elems, arow, pc);
-                    tma_load_3d_pair(st + (P + pc) * kPieceTile, &mapB, fbl, kb * Cfg::elems,
-                                     brow, pc);
+                    if (!FUSED)
+                        tma_load_3d_pair(st + pc * kATile, &mapA, fbl, kb * Cfg::elems, arow, pc);
+                    tma_load_3d_pair(st + P * kATile + pc * Cfg::b_tile, &mapB, fbl,
+                                     kb * Cfg::elems, brow, pc);
                 }
             }
         }
         if (!ok) *abort_flag = 1;
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------ MMA issuer
-        const uint32_t idesc = make_idesc(TF32 ? 2u : 1u, kBM, kBN);
+        const uint32_t idesc = make_idesc(TF32 ? 2u : 1u, kBM, BN);
         uint32_t kbg = 0;
         bool ok = true;
         for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
@@ -182,10 +260,14 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     ok = false;
                     break;
                 }
-                const uint32_t d = tmem + buf * kBufCols;
+                if (FUSED && !mbar_wait(aready0 + 8 * s, ph, p.err, kDevErrTimeout)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t d = tmem + buf * BN;
                 const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
-                auto A = [&](int i) { return st + i * kPieceTile; };
-                auto B = [&](int j) { return st + (P + j) * kPieceTile; };
+                auto A = [&](int i) { return st + i * kATile; };
+                auto B = [&](int j) { return st + P * kATile + j * Cfg::b_tile; };
                 auto ready = [&](int pc) {
                     const bool r = mbar_wait(full0 + 8 * (s * P + pc), ph, p.err, kDevErrTimeout) &&
                                    !*abort_flag;
@@ -220,23 +302,49 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         // ------------------------------------------------ accumulator warps
         const int q = warp & 3;                        // TMEM lane quadrant
         const int h = (warp - 2) >> 2;                 // column quarter of the tile
+        const int t512 = (warp - 2) * 32 + lane;       // index among the 512 threads
         const uint32_t cempty_leader0 = map_to_rank(cempty0, 0);
+        const uint32_t aready_leader0 = map_to_rank(aready0, 0);
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
-        uint32_t kbg = 0;
+        const int my_tiles = cluster_id < total ? (total - 1 - cluster_id) / num_clusters + 1 : 0;
+        const uint32_t my_blocks = uint32_t(my_tiles) * uint32_t(p.num_kb);
         bool ok = true;
+
+        // split K block g of this cluster's sequence into its stage (fused)
+        auto split = [&](uint32_t g) -> bool {
+            const uint32_t f = g % kA32Bufs, fph = (g / kA32Bufs) & 1;
+            const uint32_t s = g % S, ph = (g / S) & 1;
+            if (!mbar_wait(afull0 + 8 * f, fph, p.err, kDevErrTimeout)) return false;
+            if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout)) return false;
+            split_block(a32 + f * kA32Buf, smem + s * Cfg::stage_bytes, t512);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(afree0 + 8 * f);
+                mbar_arrive_remote(aready_leader0 + 8 * s);
+            }
+            return true;
+        };
+
+        if (FUSED && my_blocks > 0) ok = split(0);
+        uint32_t kbg = 0;
         for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
             float acc[kAccCols];
 #pragma unroll
             for (int j = 0; j < kAccCols; ++j) acc[j] = 0.0f;
             for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
+                if (FUSED && kbg + 1 < my_blocks && !split(kbg + 1)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t buf = kbg & 1, cph = (kbg >> 1) & 1;
                 if (!mbar_wait(cfull0 + 8 * buf, cph, p.err, kDevErrTimeout)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t col0 = tmem + buf * kBufCols + h * kAccCols + lane_off;
+                const uint32_t col0 = tmem + buf * BN + h * kAccCols + lane_off;
 #pragma unroll
                 for (int g = 0; g < kAccCols / 8; ++g) {
                     uint32_t r[8];
@@ -254,7 +362,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             int tm, tn;
             tile_pos(tile, p.tiles_m, p.tiles_n, tm, tn);
             const int row = tm * kBM + int(rank) * kHalfRows + q * 32 + lane;
-            const int col_base = tn * kBN + h * kAccCols;
+            const int col_base = tn * BN + h * kAccCols;
             if (row < p.M && col_base < p.N) {
                 float* crow = p.C + (int64_t)row * p.ldc + col_base;
                 if (vec && col_base + kAccCols <= p.N) {
@@ -296,25 +404,25 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
-                     :: "r"(tmem), "r"(kTmemColsK) : "memory");
+                     :: "r"(tmem), "r"(Cfg::tmem_cols) : "memory");
     }
 }
 
-template <int TF32>
+template <int TF32, int BN, int FUSED>
 cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
                             const TcGemmParams& p, int clusters, cudaStream_t stream) {
+    using Cfg = KCfg<TF32, BN, FUSED>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kblock_kernel<TF32>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             KCfg<TF32>::smem);
+        cudaError_t e = cudaFuncSetAttribute(gemm_kblock_kernel<TF32, BN, FUSED>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(kThreadsK);
-    cfg.dynamicSmemBytes = KCfg<TF32>::smem;
+    cfg.dynamicSmemBytes = Cfg::smem;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -323,18 +431,28 @@ cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kblock_kernel<TF32>, mapA, mapB, p);
+    return cudaLaunchKernelEx(&cfg, gemm_kblock_kernel<TF32, BN, FUSED>, mapA, mapB, p);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_kblock(int tf32, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                               const TcGemmParams& p, int sms, cudaStream_t stream) {
+cudaError_t launch_gemm_kblock(int tf32, int bn, int fused, const CUtensorMap& mapA,
+                               const CUtensorMap& mapB, const TcGemmParams& p, int sms,
+                               cudaStream_t stream) {
     const int tiles = p.tiles_m * p.tiles_n;
     if (tiles == 0) return cudaSuccess;
     const int clusters = tiles < sms / 2 ? tiles : sms / 2;
-    cudaError_t e = tf32 ? launch_kblock_t<1>(mapA, mapB, p, clusters, stream)
-                         : launch_kblock_t<0>(mapA, mapB, p, clusters, stream);
+    cudaError_t e;
+    if (fused) {
+        if (tf32 || bn != 128) return cudaErrorInvalidValue;
+        e = launch_kblock_t<0, 128, 1>(mapA, mapB, p, clusters, stream);
+    } else if (tf32) {
+        e = bn == 128 ? launch_kblock_t<1, 128, 0>(mapA, mapB, p, clusters, stream)
+                      : launch_kblock_t<1, 256, 0>(mapA, mapB, p, clusters, stream);
+    } else {
+        e = bn == 128 ? launch_kblock_t<0, 128, 0>(mapA, mapB, p, clusters, stream)
+                      : launch_kblock_t<0, 256, 0>(mapA, mapB, p, clusters, stream);
+    }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -108,8 +108,10 @@ def main():
             mi, ni = W.sample_pairs(g0.M, g0.N, args.samples)
             Cref, Sabs = oracle.gemm_ref(A, B, g0.transA, g0.transB, g0.alpha, g0.beta, C0,
                                          pairs=(mi, ni))
-        modes = ["bf16x9", "tf32x3", "fp32_simt"]
-        for mode in modes:
+        modes = ["bf16x9", "bf16x9_fused", "tf32x3", "fp32_simt"]
+        for mode_name in modes:
+            mode = mode_name.replace("_fused", "")
+            emu.emu_set_path("fused" if mode_name.endswith("_fused") else "twopass")
             dC = torch.from_numpy(C0).cuda() if C0 is not None else torch.empty((g0.M, g0.N), device="cuda")
             dC0 = dC.clone() if C0 is not None else None
 
@@ -135,13 +137,14 @@ def main():
             if dC0 is not None:   # subtract the restore copy of C
                 ms -= time_call(lambda: dC.copy_(dC0), reps=reps)
             tf = g0.flops / (ms * 1e-3) / 1e12
-            rec = {"workload": name, "mode": mode, "M": g0.M, "N": g0.N, "K": g0.K,
+            rec = {"workload": name, "mode": mode_name, "M": g0.M, "N": g0.N, "K": g0.K,
                    "ms": round(ms, 4), "tflops": round(tf, 2), "pct_p9": round(100 * tf / p9, 1),
                    "max_ratio": ratio, "rel_frob": relf,
                    "checked": "all" if full else int(mi.size)}
             print(json.dumps(rec), flush=True)
             if out:
                 out.write(json.dumps(rec) + "\n")
+        emu.emu_set_path("auto")
         if not args.no_cublas and g0.mode == "bf16x9":
             for emulate in (False, True):
                 ms = cublas_child(name, emulate)

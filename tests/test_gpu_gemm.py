@@ -245,3 +245,69 @@ def test_bounded_wait_reports_timeout_and_context_survives(emu):
 
 def test_no_device_error_recorded(emu):
     assert emu.emu_get_last_device_error() == 0
+
+
+# --------------------------------------------------------- the fused path --
+# EMU_PATH_FUSED: A is read as FP32 and split in shared memory by the GEMM
+# kernel (BF16x9, K-major A with 16-byte-aligned rows); otherwise the call
+# falls back to the two-pass path.
+
+class _fused_path:
+    def __init__(self, emu):
+        self.emu = emu
+
+    def __enter__(self):
+        self.old = self.emu.emu_get_path()
+        self.emu.emu_set_path("fused")
+
+    def __exit__(self, *exc):
+        self.emu.emu_set_path(self.old)
+
+
+@pytest.mark.parametrize("shape", SHAPES + [(1000, 700, 300), (257, 129, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("transB", [0, 1])
+def test_fused_path_every_element(emu, shape, transB):
+    M, N, K = shape
+    r = W.rng(M * 11 + N * 5 + K + transB)
+    A = W.normal(r, (M, K))
+    B = W.normal(r, (N, K) if transB else (K, N))
+    C0 = W.uniform(r, (M, N))
+    with _fused_path(emu):
+        C = _run(emu, A, B, False, transB, 1.5, -0.75, C0, "bf16x9")
+    Cref, Sabs = oracle.gemm_ref(A, B, False, transB, 1.5, -0.75, C0)
+    assert checks.error_ratio(C, Cref, Sabs, K, 1.5, -0.75, C0) <= 1.0
+    C2 = _run(emu, A, B, False, transB, 1.5, -0.75, C0, "bf16x9")      # two-pass
+    bound = checks.elementwise_bound(K, 1.5, -0.75, Sabs, C0)
+    assert np.all(np.abs(C.astype(np.float64) - C2) <= bound)
+
+
+def test_fused_path_identity_is_exact_and_falls_back_when_needed(emu):
+    X = W.normal(W.rng(31), (256, 256))
+    I = np.eye(256, dtype=np.float32)
+    with _fused_path(emu):
+        assert np.array_equal(_run(emu, I, X), X)
+        assert np.array_equal(_run(emu, X, I), X)
+        # transposed A and a misaligned row stride take the two-pass path
+        assert np.array_equal(_run(emu, I, X, transA=True), X)
+        C = _run(emu, X[:, :255].copy(), np.ones((255, 64), np.float32))
+        Cref, Sabs = oracle.gemm_ref(X[:, :255].copy(), np.ones((255, 64), np.float32))
+        assert checks.error_ratio(C, Cref, Sabs, 255, 1.0, 0.0) <= 1.0
+
+
+@pytest.mark.parametrize("name", ["mlip17280_k256_n256", "mlip17280_k1024_n256",
+                                  "mlip17280_k256_n1024"])
+def test_fused_path_mlip17280_sampled(emu, name):
+    with _fused_path(emu):
+        ratio, relf, _, _ = _sampled_check(emu, W.WORKLOADS[name], "bf16x9")
+    assert ratio <= 1.0 and relf <= checks.FROBENIUS_TOL, (ratio, relf)
+
+
+def test_fused_path_square8192_sampled(emu):
+    with _fused_path(emu):
+        ratio, relf, _, _ = _sampled_check(emu, W.WORKLOADS["square8192_normal"], "bf16x9")
+    assert ratio <= 1.0 and relf <= checks.FROBENIUS_TOL, (ratio, relf)
+
+
+def test_no_device_error_after_fused(emu):
+    assert emu.emu_get_last_device_error() == 0
