@@ -31,20 +31,21 @@
 // two TMEM partial buffers let the tensor core fill one block's partial while
 // the other is added to the registers.
 //
-// Fused A (BF16x9): the producer loads the FP32 A block (128 rows x 64, two
-// 128-byte-swizzled boxes) into one of two staging buffers; the accumulator
-// warps, idle between promotions, split it (16 elements per thread) straight
-// into the swizzled piece layout the MMA reads, make the writes visible to
-// the tensor core (fence.proxy.async) and signal the leader CTA.  The split
-// of block g+1 runs while the tensor core works on block g.
+// Fused A (BF16x9, BN = 128): the producer loads the FP32 A block (128 rows
+// x 64, two 128-byte-swizzled boxes) into one of two staging buffers; eight
+// split warps turn it (32 elements per thread) straight into the swizzled
+// piece layout the MMA reads, make the writes visible to the tensor core
+// (fence.proxy.async) and signal the leader CTA, running ahead of the tensor
+// core by up to two K blocks.
 //
-// Warps (576 threads per CTA):
+// Warps (576 threads per CTA, 832 when fused):
 //   warp 0      TMA producer (both CTAs; completion counted on the leader's
 //               barriers) and tensor-memory allocation
 //   warp 1      MMA issuer (leader CTA only)
 //   warps 2-17  accumulators: warp w owns TMEM lanes 32(w%4)..+31 and the
 //               column quarter (w-2)/4 of the tile (BN/4 FP32 registers per
-//               thread), write C = alpha*acc + beta*C, and split A when fused.
+//               thread) and write C = alpha*acc + beta*C
+//   warps 18-25 (fused) split warps.
 #include "emu_device.cuh"
 
 namespace emu {
@@ -53,7 +54,9 @@ namespace {
 constexpr int kBM = 256, kHalfRows = 128;
 constexpr int kATile = kHalfRows * kTcBKBytes;       // 16 KB: 128 rows x 128 bytes
 constexpr int kAccWarps = 16;
-constexpr int kThreadsK = (2 + kAccWarps) * 32;
+constexpr int kSplitWarps = 8;                        // fused path only
+template <int FUSED>
+constexpr int threads_k() { return (2 + kAccWarps + (FUSED ? kSplitWarps : 0)) * 32; }
 constexpr int kSmemMax = 232448;                      // dynamic shared memory per CTA
 constexpr int kA32Box = 128 * 128;                    // FP32 box: 128 rows x 32 floats
 constexpr int kA32Buf = 2 * kA32Box;                  // one 64-wide K block of FP32 A
@@ -112,30 +115,37 @@ __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) {
     return uint32_t(lo) | (uint32_t(hi) << 16);
 }
 
-// Split this thread's 16 elements of a 128 x 64 FP32 A block (two swizzled
-// 128 x 32 boxes at `a32`) into the three BF16 pieces at `pieces` (three
-// 128 x 64 swizzled tiles, 16 KB apart).  Thread t of the 512 handles row
-// t/4, elements 16*(t%4) .. +15.
-__device__ __forceinline__ void split_block(const uint8_t* a32, uint8_t* pieces, int t) {
-    const int r = t >> 2, seg = t & 3, sw = r & 7;
-    const uint8_t* box = a32 + (seg >> 1) * kA32Box + r * 128;
+// Split this thread's share of a 128 x 64 FP32 A block (two swizzled 128 x
+// 32 boxes at `a32`) into the three BF16 pieces at `pieces` (three 128 x 64
+// swizzled tiles, 16 KB apart).  Split warp w (0..7) takes rows 16w..16w+15;
+// lane l takes row 16w + 8j + l%8 (j = 0, 1) and elements 16(l/8) .. +15.
+// The 8 lanes of a quarter-warp read and write the same logical 16-byte
+// chunk of 8 consecutive rows, which the 128-byte swizzle spreads over 8
+// distinct bank groups, so the shared-memory accesses are conflict-free.
+__device__ __forceinline__ void split_block(const uint8_t* a32, uint8_t* pieces, int w, int lane) {
+    const int part = lane >> 3;                            // 16-element part of the 64
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int c4 = (seg & 1) * 4 + 2 * half;          // first float4 chunk of these 8
-        const float4 x0 = *reinterpret_cast<const float4*>(box + ((c4 ^ sw) << 4));
-        const float4 x1 = *reinterpret_cast<const float4*>(box + (((c4 + 1) ^ sw) << 4));
-        const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        uint16_t h0[8], h1[8], h2[8];
+    for (int j = 0; j < 2; ++j) {
+        const int r = 16 * w + 8 * j + (lane & 7), sw = r & 7;
+        const uint8_t* box = a32 + (part >> 1) * kA32Box + r * 128;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) split_bf16x3(v[i], h0[i], h1[i], h2[i]);
-        const int c8 = seg * 2 + half;                     // 16-byte chunk of 8 BF16
-        const int off = r * 128 + ((c8 ^ sw) << 4);
-        *reinterpret_cast<uint4*>(pieces + off) =
-            make_uint4(pack2(h0[0], h0[1]), pack2(h0[2], h0[3]), pack2(h0[4], h0[5]), pack2(h0[6], h0[7]));
-        *reinterpret_cast<uint4*>(pieces + kATile + off) =
-            make_uint4(pack2(h1[0], h1[1]), pack2(h1[2], h1[3]), pack2(h1[4], h1[5]), pack2(h1[6], h1[7]));
-        *reinterpret_cast<uint4*>(pieces + 2 * kATile + off) =
-            make_uint4(pack2(h2[0], h2[1]), pack2(h2[2], h2[3]), pack2(h2[4], h2[5]), pack2(h2[6], h2[7]));
+        for (int half = 0; half < 2; ++half) {
+            const int c4 = (part & 1) * 4 + 2 * half;      // first float4 chunk of these 8
+            const float4 x0 = *reinterpret_cast<const float4*>(box + ((c4 ^ sw) << 4));
+            const float4 x1 = *reinterpret_cast<const float4*>(box + (((c4 + 1) ^ sw) << 4));
+            const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            uint16_t h0[8], h1[8], h2[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) split_bf16x3(v[i], h0[i], h1[i], h2[i]);
+            const int c8 = part * 2 + half;                // 16-byte chunk of 8 BF16
+            const int off = r * 128 + ((c8 ^ sw) << 4);
+            *reinterpret_cast<uint4*>(pieces + off) =
+                make_uint4(pack2(h0[0], h0[1]), pack2(h0[2], h0[3]), pack2(h0[4], h0[5]), pack2(h0[6], h0[7]));
+            *reinterpret_cast<uint4*>(pieces + kATile + off) =
+                make_uint4(pack2(h1[0], h1[1]), pack2(h1[2], h1[3]), pack2(h1[4], h1[5]), pack2(h1[6], h1[7]));
+            *reinterpret_cast<uint4*>(pieces + 2 * kATile + off) =
+                make_uint4(pack2(h2[0], h2[1]), pack2(h2[2], h2[3]), pack2(h2[4], h2[5]), pack2(h2[6], h2[7]));
+        }
     }
 }
 
@@ -144,7 +154,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 template <int TF32, int BN, int FUSED>
-__global__ void __launch_bounds__(kThreadsK, 1)
+__global__ void __launch_bounds__(threads_k<FUSED>(), 1)
 gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB, const TcGemmParams p) {
     using Cfg = KCfg<TF32, BN, FUSED>;
@@ -182,10 +192,10 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         mbar_init(cempty0, 2 * kAccWarps);   // accumulator warps of both CTAs
         mbar_init(cempty0 + 8, 2 * kAccWarps);
         if (FUSED) {
-            for (int s = 0; s < S; ++s) mbar_init(aready0 + 8 * s, 2 * kAccWarps);
+            for (int s = 0; s < S; ++s) mbar_init(aready0 + 8 * s, 2 * kSplitWarps);
             for (int f = 0; f < kA32Bufs; ++f) {
                 mbar_init(afull0 + 8 * f, 1);
-                mbar_init(afree0 + 8 * f, kAccWarps);
+                mbar_init(afree0 + 8 * f, kSplitWarps);
             }
         }
         *abort_flag = 0;
@@ -298,46 +308,44 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             }
         }
         if (!ok) *abort_flag = 1;
-    } else if (warp >= 2) {
-        // ------------------------------------------------ accumulator warps
-        const int q = warp & 3;                        // TMEM lane quadrant
-        const int h = (warp - 2) >> 2;                 // column quarter of the tile
-        const int t512 = (warp - 2) * 32 + lane;       // index among the 512 threads
-        const uint32_t cempty_leader0 = map_to_rank(cempty0, 0);
+    } else if (FUSED && warp >= 2 + kAccWarps) {
+        // ------------------------------------------------------ split warps
+        // Split every K block of this cluster's tiles, as soon as its FP32
+        // block has landed and its stage is free, ahead of the tensor core.
+        const int w = warp - 2 - kAccWarps;
         const uint32_t aready_leader0 = map_to_rank(aready0, 0);
-        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
         const int my_tiles = cluster_id < total ? (total - 1 - cluster_id) / num_clusters + 1 : 0;
         const uint32_t my_blocks = uint32_t(my_tiles) * uint32_t(p.num_kb);
-        bool ok = true;
-
-        // split K block g of this cluster's sequence into its stage (fused)
-        auto split = [&](uint32_t g) -> bool {
+        for (uint32_t g = 0; g < my_blocks; ++g) {
             const uint32_t f = g % kA32Bufs, fph = (g / kA32Bufs) & 1;
             const uint32_t s = g % S, ph = (g / S) & 1;
-            if (!mbar_wait(afull0 + 8 * f, fph, p.err, kDevErrTimeout)) return false;
-            if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout)) return false;
-            split_block(a32 + f * kA32Buf, smem + s * Cfg::stage_bytes, t512);
-            fence_proxy_async_smem();
+            if (!mbar_wait(afull0 + 8 * f, fph, p.err, kDevErrTimeout) ||
+                !mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
+                *abort_flag = 1;
+                break;
+            }
+            split_block(a32 + f * kA32Buf, smem + s * Cfg::stage_bytes, w, lane);
+            fence_proxy_async_smem();        // generic-proxy writes -> tensor core
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(afree0 + 8 * f);
                 mbar_arrive_remote(aready_leader0 + 8 * s);
             }
-            return true;
-        };
-
-        if (FUSED && my_blocks > 0) ok = split(0);
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ accumulator warps
+        const int q = warp & 3;                        // TMEM lane quadrant
+        const int h = (warp - 2) >> 2;                 // column quarter of the tile
+        const uint32_t cempty_leader0 = map_to_rank(cempty0, 0);
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
+        bool ok = true;
         uint32_t kbg = 0;
         for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
             float acc[kAccCols];
 #pragma unroll
             for (int j = 0; j < kAccCols; ++j) acc[j] = 0.0f;
             for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
-                if (FUSED && kbg + 1 < my_blocks && !split(kbg + 1)) {
-                    ok = false;
-                    break;
-                }
                 const uint32_t buf = kbg & 1, cph = (kbg >> 1) & 1;
                 if (!mbar_wait(cfull0 + 8 * buf, cph, p.err, kDevErrTimeout)) {
                     ok = false;
@@ -421,7 +429,7 @@ cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
-    cfg.blockDim = dim3(kThreadsK);
+    cfg.blockDim = dim3(threads_k<FUSED>());
     cfg.dynamicSmemBytes = Cfg::smem;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
