@@ -38,14 +38,15 @@
 // (fence.proxy.async) and signal the leader CTA, running ahead of the tensor
 // core by up to two K blocks.
 //
-// Warps (576 threads per CTA, 832 when fused):
+// Warps (576 threads per CTA, 864 when fused):
 //   warp 0      TMA producer (both CTAs; completion counted on the leader's
 //               barriers) and tensor-memory allocation
 //   warp 1      MMA issuer (leader CTA only)
 //   warps 2-17  accumulators: warp w owns TMEM lanes 32(w%4)..+31 and the
 //               column quarter (w-2)/4 of the tile (BN/4 FP32 registers per
 //               thread) and write C = alpha*acc + beta*C
-//   warps 18-25 (fused) split warps.
+//   warp 18     (fused) FP32 A producer
+//   warps 19-26 (fused) split warps.
 #include "emu_device.cuh"
 
 namespace emu {
@@ -55,8 +56,9 @@ constexpr int kBM = 256, kHalfRows = 128;
 constexpr int kATile = kHalfRows * kTcBKBytes;       // 16 KB: 128 rows x 128 bytes
 constexpr int kAccWarps = 16;
 constexpr int kSplitWarps = 8;                        // fused path only
+constexpr int kA32ProducerWarp = 2 + kAccWarps;       // fused path only
 template <int FUSED>
-constexpr int threads_k() { return (2 + kAccWarps + (FUSED ? kSplitWarps : 0)) * 32; }
+constexpr int threads_k() { return (2 + kAccWarps + (FUSED ? 1 + kSplitWarps : 0)) * 32; }
 constexpr int kSmemMax = 232448;                      // dynamic shared memory per CTA
 constexpr int kA32Box = 128 * 128;                    // FP32 box: 128 rows x 32 floats
 constexpr int kA32Buf = 2 * kA32Box;                  // one 64-wide K block of FP32 A
@@ -228,18 +230,6 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             const int brow = tn * BN + int(rank) * Cfg::b_rows;
             for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
                 const uint32_t s = kbg % S, ph = (kbg / S) & 1;
-                if (FUSED) {
-                    const uint32_t f = kbg % kA32Bufs, fph = (kbg / kA32Bufs) & 1;
-                    if (!mbar_wait(afree0 + 8 * f, fph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(afull0 + 8 * f, kA32Buf);
-                    const uint32_t dst = smem_u32(a32 + f * kA32Buf);
-                    // FP32 A map is (K, M, 1): the two 32-wide boxes of this K block
-                    tma_load_3d(dst, &mapA, afull0 + 8 * f, kb * 64, arow, 0);
-                    tma_load_3d(dst + kA32Box, &mapA, afull0 + 8 * f, kb * 64 + 32, arow, 0);
-                }
                 if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
                     ok = false;
                     break;
@@ -308,11 +298,37 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             }
         }
         if (!ok) *abort_flag = 1;
-    } else if (FUSED && warp >= 2 + kAccWarps) {
+    } else if (FUSED && warp == kA32ProducerWarp) {
+        // ------------------------------------------- FP32 A producer (fused)
+        // Its own thread, so each FP32 block is requested as soon as its
+        // staging buffer is free, independently of the B-piece stages.
+        if (lane == 0) {
+            uint32_t kbg = 0;
+            bool ok = true;
+            for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
+                int tm, tn;
+                tile_pos(tile, p.tiles_m, p.tiles_n, tm, tn);
+                const int arow = tm * kBM + int(rank) * kHalfRows;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
+                    const uint32_t f = kbg % kA32Bufs, fph = (kbg / kA32Bufs) & 1;
+                    if (!mbar_wait(afree0 + 8 * f, fph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(afull0 + 8 * f, kA32Buf);
+                    const uint32_t dst = smem_u32(a32 + f * kA32Buf);
+                    // FP32 A map is (K, M, 1): the two 32-wide boxes of this K block
+                    tma_load_3d(dst, &mapA, afull0 + 8 * f, kb * 64, arow, 0);
+                    tma_load_3d(dst + kA32Box, &mapA, afull0 + 8 * f, kb * 64 + 32, arow, 0);
+                }
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else if (FUSED && warp > kA32ProducerWarp) {
         // ------------------------------------------------------ split warps
         // Split every K block of this cluster's tiles, as soon as its FP32
         // block has landed and its stage is free, ahead of the tensor core.
-        const int w = warp - 2 - kAccWarps;
+        const int w = warp - kA32ProducerWarp - 1;
         const uint32_t aready_leader0 = map_to_rank(aready0, 0);
         const int my_tiles = cluster_id < total ? (total - 1 - cluster_id) / num_clusters + 1 : 0;
         const uint32_t my_blocks = uint32_t(my_tiles) * uint32_t(p.num_kb);

@@ -150,6 +150,50 @@ __global__ void __launch_bounds__(256) split3_transposed(const float* __restrict
     }
 }
 
+// Vectorised form for full 64 x 64 tiles with 16-byte aligned rows on both
+// sides: each thread loads four float4 along stored rows; then lanes 4i..4i+3
+// of a warp write the 64 pieces of one op row as 16-byte stores, 128
+// contiguous bytes per piece.  Tiles at the ragged edges use the kernel above.
+__global__ void __launch_bounds__(256) split3_transposed_vec(const float* __restrict__ X, int64_t rows,
+                                                             int64_t cols, int64_t ld,
+                                                             uint16_t* __restrict__ P0,
+                                                             uint16_t* __restrict__ P1,
+                                                             uint16_t* __restrict__ P2, int64_t ldp) {
+    __shared__ float tile[kT][kT + 1];               // [op col (stored row)][op row]
+    const int tid = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.x * kT;     // op rows  = stored columns
+    const int64_t c0 = (int64_t)blockIdx.y * kT;     // op cols  = stored rows
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = tid + 256 * i;               // 0 .. 1023
+        const int k = idx >> 4, r4 = (idx & 15) * 4;
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(X + (c0 + k) * ld + r0 + r4));
+        tile[k][r4 + 0] = v.x;
+        tile[k][r4 + 1] = v.y;
+        tile[k][r4 + 2] = v.z;
+        tile[k][r4 + 3] = v.w;
+    }
+    __syncthreads();
+    const int rr = tid >> 2, cp = tid & 3;           // op row in tile, 16-element part
+    uint16_t h0[16], h1[16], h2[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) split_bf16x3(tile[16 * cp + i][rr], h0[i], h1[i], h2[i]);
+    const int64_t o = (r0 + rr) * ldp + c0 + 16 * cp;
+    uint4* d0 = reinterpret_cast<uint4*>(P0 + o);
+    uint4* d1 = reinterpret_cast<uint4*>(P1 + o);
+    uint4* d2 = reinterpret_cast<uint4*>(P2 + o);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int b = 8 * q;
+        d0[q] = make_uint4(h0[b] | (uint32_t(h0[b + 1]) << 16), h0[b + 2] | (uint32_t(h0[b + 3]) << 16),
+                           h0[b + 4] | (uint32_t(h0[b + 5]) << 16), h0[b + 6] | (uint32_t(h0[b + 7]) << 16));
+        d1[q] = make_uint4(h1[b] | (uint32_t(h1[b + 1]) << 16), h1[b + 2] | (uint32_t(h1[b + 3]) << 16),
+                           h1[b + 4] | (uint32_t(h1[b + 5]) << 16), h1[b + 6] | (uint32_t(h1[b + 7]) << 16));
+        d2[q] = make_uint4(h2[b] | (uint32_t(h2[b + 1]) << 16), h2[b + 2] | (uint32_t(h2[b + 3]) << 16),
+                           h2[b + 4] | (uint32_t(h2[b + 5]) << 16), h2[b + 6] | (uint32_t(h2[b + 7]) << 16));
+    }
+}
+
 __global__ void __launch_bounds__(256) split2_transposed(const float* __restrict__ X, int64_t rows,
                                                          int64_t cols, int64_t ld,
                                                          float* __restrict__ HI,
@@ -202,7 +246,11 @@ cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int6
     if (rows == 0 || cols == 0) return cudaSuccess;
     if (trans) {
         dim3 grid((unsigned)((rows + kT - 1) / kT), (unsigned)((cols + kT - 1) / kT));
-        split3_transposed<<<grid, 256, 0, stream>>>(X, rows, cols, ld, P0, P1, P2, ldp);
+        if (rows % kT == 0 && cols % kT == 0 && ld % 4 == 0 && ldp % 8 == 0 && aligned16(X) &&
+            aligned16(P0) && aligned16(P1) && aligned16(P2))
+            split3_transposed_vec<<<grid, 256, 0, stream>>>(X, rows, cols, ld, P0, P1, P2, ldp);
+        else
+            split3_transposed<<<grid, 256, 0, stream>>>(X, rows, cols, ld, P0, P1, P2, ldp);
     } else if (cols % 8 == 0 && ld % 4 == 0 && ldp % 8 == 0 && aligned16(X) && aligned16(P0) &&
                aligned16(P1) && aligned16(P2)) {
         split3_rows_vec8<<<grid_for(rows * (cols / 8), 256), 256, 0, stream>>>(X, rows, cols, ld,
