@@ -32,13 +32,13 @@
 // the other is added to the registers.
 //
 // Fused A (BF16x9, BN = 128): the producer loads the FP32 A block (128 rows
-// x 64, two 128-byte-swizzled boxes) into one of two staging buffers; eight
-// split warps turn it (32 elements per thread) straight into the swizzled
+// x 64, two 128-byte-swizzled boxes) into one of two staging buffers;
+// sixteen split warps turn it (16 elements per thread) straight into the swizzled
 // piece layout the MMA reads, make the writes visible to the tensor core
 // (fence.proxy.async) and signal the leader CTA, running ahead of the tensor
 // core by up to two K blocks.
 //
-// Warps (576 threads per CTA, 864 when fused):
+// Warps (576 threads per CTA, 1120 when fused):
 //   warp 0      TMA producer (both CTAs; completion counted on the leader's
 //               barriers) and tensor-memory allocation
 //   warp 1      MMA issuer (leader CTA only)
@@ -46,7 +46,7 @@
 //               column quarter (w-2)/4 of the tile (BN/4 FP32 registers per
 //               thread) and write C = alpha*acc + beta*C
 //   warp 18     (fused) FP32 A producer
-//   warps 19-26 (fused) split warps.
+//   warps 19-34 (fused) split warps.
 #include "emu_device.cuh"
 
 namespace emu {
@@ -55,7 +55,7 @@ namespace {
 constexpr int kBM = 256, kHalfRows = 128;
 constexpr int kATile = kHalfRows * kTcBKBytes;       // 16 KB: 128 rows x 128 bytes
 constexpr int kAccWarps = 16;
-constexpr int kSplitWarps = 8;                        // fused path only
+constexpr int kSplitWarps = 16;                       // fused path only
 constexpr int kA32ProducerWarp = 2 + kAccWarps;       // fused path only
 template <int FUSED>
 constexpr int threads_k() { return (2 + kAccWarps + (FUSED ? 1 + kSplitWarps : 0)) * 32; }
@@ -119,16 +119,15 @@ __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) {
 
 // Split this thread's share of a 128 x 64 FP32 A block (two swizzled 128 x
 // 32 boxes at `a32`) into the three BF16 pieces at `pieces` (three 128 x 64
-// swizzled tiles, 16 KB apart).  Split warp w (0..7) takes rows 16w..16w+15;
-// lane l takes row 16w + 8j + l%8 (j = 0, 1) and elements 16(l/8) .. +15.
-// The 8 lanes of a quarter-warp read and write the same logical 16-byte
-// chunk of 8 consecutive rows, which the 128-byte swizzle spreads over 8
-// distinct bank groups, so the shared-memory accesses are conflict-free.
+// swizzled tiles, 16 KB apart).  Split warp w (0..15) takes rows 8w..8w+7;
+// lane l takes row 8w + l%8 and elements 16(l/8) .. +15.  The 8 lanes of a
+// quarter-warp read and write the same logical 16-byte chunk of 8
+// consecutive rows, which the 128-byte swizzle spreads over 8 distinct bank
+// groups, so the shared-memory accesses are conflict-free.
 __device__ __forceinline__ void split_block(const uint8_t* a32, uint8_t* pieces, int w, int lane) {
     const int part = lane >> 3;                            // 16-element part of the 64
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int r = 16 * w + 8 * j + (lane & 7), sw = r & 7;
+    {
+        const int r = 8 * w + (lane & 7), sw = r & 7;
         const uint8_t* box = a32 + (part >> 1) * kA32Box + r * 128;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
