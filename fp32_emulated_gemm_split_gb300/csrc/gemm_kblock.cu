@@ -38,15 +38,15 @@
 // (fence.proxy.async) and signal the leader CTA, running ahead of the tensor
 // core by up to two K blocks.
 //
-// Warps (576 threads per CTA, 1120 when fused):
+// Warps (576 threads per CTA, 832 when fused):
 //   warp 0      TMA producer (both CTAs; completion counted on the leader's
 //               barriers) and tensor-memory allocation
 //   warp 1      MMA issuer (leader CTA only)
-//   warps 2-17  accumulators: warp w owns TMEM lanes 32(w%4)..+31 and the
-//               column quarter (w-2)/4 of the tile (BN/4 FP32 registers per
-//               thread) and write C = alpha*acc + beta*C
-//   warp 18     (fused) FP32 A producer
-//   warps 19-34 (fused) split warps.
+//   warps 2..   accumulators (16, or 8 when fused): warp w owns TMEM lanes
+//               32(w%4)..+31 and column group (w-2)/4 of the tile (BN/4, or
+//               BN/2 when fused, FP32 registers per thread) and writes
+//               C = alpha*acc + beta*C
+//   then        (fused) 16 split warps.
 #include "emu_device.cuh"
 
 namespace emu {
@@ -54,11 +54,14 @@ namespace {
 
 constexpr int kBM = 256, kHalfRows = 128;
 constexpr int kATile = kHalfRows * kTcBKBytes;       // 16 KB: 128 rows x 128 bytes
-constexpr int kAccWarps = 16;
-constexpr int kSplitWarps = 16;                       // fused path only
-constexpr int kA32ProducerWarp = 2 + kAccWarps;       // fused path only
+// Accumulator warps: 16 (a column quarter each) on the two-pass path; 8 (a
+// column half each) on the fused path, which also runs 16 split warps and must
+// stay within 1024 threads.
 template <int FUSED>
-constexpr int threads_k() { return (2 + kAccWarps + (FUSED ? 1 + kSplitWarps : 0)) * 32; }
+constexpr int acc_warps() { return FUSED ? 8 : 16; }
+constexpr int kSplitWarps = 16;                       // fused path only
+template <int FUSED>
+constexpr int threads_k() { return (2 + acc_warps<FUSED>() + (FUSED ? kSplitWarps : 0)) * 32; }
 constexpr int kSmemMax = 232448;                      // dynamic shared memory per CTA
 constexpr int kA32Box = 128 * 128;                    // FP32 box: 128 rows x 32 floats
 constexpr int kA32Buf = 2 * kA32Box;                  // one 64-wide K block of FP32 A
@@ -74,7 +77,11 @@ struct KCfg {
     static constexpr int avail = kSmemMax - 2048 - a32_bytes;
     static constexpr int stages = avail / stage_bytes > 4 ? 4 : avail / stage_bytes;
     static constexpr int elems = TF32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
-    static constexpr int acc_cols = BN / 4;
+    // K blocks summed in one TMEM partial before it is added to the registers:
+    // a TF32x3 block (32 elements, 12 MMAs) is short, so two are combined.
+    static constexpr int kb_per_partial = TF32 ? 2 : 1;
+    static constexpr int acc_warps = ::emu::acc_warps<FUSED>();
+    static constexpr int acc_cols = BN / (acc_warps / 4);         // columns per accumulator thread
     static constexpr uint32_t tmem_cols = 2 * BN <= 256 ? 256 : 512;
     static constexpr int smem = stages * stage_bytes + a32_bytes + 2048;
     // bytes a piece barrier waits for (both CTAs)
@@ -190,8 +197,8 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         for (int s = 0; s < S; ++s) mbar_init(empty0 + 8 * s, 1);
         mbar_init(cfull0, 1);
         mbar_init(cfull0 + 8, 1);
-        mbar_init(cempty0, 2 * kAccWarps);   // accumulator warps of both CTAs
-        mbar_init(cempty0 + 8, 2 * kAccWarps);
+        mbar_init(cempty0, 2 * Cfg::acc_warps);   // accumulator warps of both CTAs
+        mbar_init(cempty0 + 8, 2 * Cfg::acc_warps);
         if (FUSED) {
             for (int s = 0; s < S; ++s) mbar_init(aready0 + 8 * s, 2 * kSplitWarps);
             for (int f = 0; f < kA32Bufs; ++f) {
@@ -229,6 +236,18 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             const int brow = tn * BN + int(rank) * Cfg::b_rows;
             for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
                 const uint32_t s = kbg % S, ph = (kbg / S) & 1;
+                if (FUSED) {
+                    const uint32_t f = kbg % kA32Bufs, fph = (kbg / kA32Bufs) & 1;
+                    if (!mbar_wait(afree0 + 8 * f, fph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(afull0 + 8 * f, kA32Buf);
+                    const uint32_t dst = smem_u32(a32 + f * kA32Buf);
+                    // FP32 A map is (K, M, 1): the two 32-wide boxes of this K block
+                    tma_load_3d(dst, &mapA, afull0 + 8 * f, kb * 64, arow, 0);
+                    tma_load_3d(dst + kA32Box, &mapA, afull0 + 8 * f, kb * 64 + 32, arow, 0);
+                }
                 if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
                     ok = false;
                     break;
@@ -249,13 +268,16 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------ MMA issuer
         const uint32_t idesc = make_idesc(TF32 ? 2u : 1u, kBM, BN);
-        uint32_t kbg = 0;
+        constexpr int KBP = Cfg::kb_per_partial;
+        uint32_t kbg = 0, part = 0;              // K blocks and TMEM partials so far
         bool ok = true;
         for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
             for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
                 const uint32_t s = kbg % S, ph = (kbg / S) & 1;
-                const uint32_t buf = kbg & 1, cph = (kbg >> 1) & 1;
-                if (!mbar_wait(cempty0 + 8 * buf, cph ^ 1, p.err, kDevErrTimeout)) {
+                const uint32_t buf = part & 1, cph = (part >> 1) & 1;
+                const bool fresh = (kb % KBP) == 0;             // first block of a partial
+                const bool close = (kb % KBP) == KBP - 1 || kb == p.num_kb - 1;
+                if (fresh && !mbar_wait(cempty0 + 8 * buf, cph ^ 1, p.err, kDevErrTimeout)) {
                     ok = false;
                     break;
                 }
@@ -288,46 +310,23 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     mma_pair<0>(d, A(0), B(0), idesc, false, true);           // band 0
                 } else {
                     if (!ready(1) || !ready(0)) { ok = false; break; }
-                    mma_pair<1>(d, A(0), B(1), idesc, true, false);           // hi*lo
+                    mma_pair<1>(d, A(0), B(1), idesc, fresh, false);          // hi*lo
                     mma_pair<1>(d, A(1), B(0), idesc, false, false);          // lo*hi
                     mma_pair<1>(d, A(0), B(0), idesc, false, false);          // hi*hi
                 }
                 tc_commit_pair(empty0 + 8 * s);
-                tc_commit_pair(cfull0 + 8 * buf);
+                if (close) {
+                    tc_commit_pair(cfull0 + 8 * buf);
+                    ++part;
+                }
             }
         }
         if (!ok) *abort_flag = 1;
-    } else if (FUSED && warp == kA32ProducerWarp) {
-        // ------------------------------------------- FP32 A producer (fused)
-        // Its own thread, so each FP32 block is requested as soon as its
-        // staging buffer is free, independently of the B-piece stages.
-        if (lane == 0) {
-            uint32_t kbg = 0;
-            bool ok = true;
-            for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
-                int tm, tn;
-                tile_pos(tile, p.tiles_m, p.tiles_n, tm, tn);
-                const int arow = tm * kBM + int(rank) * kHalfRows;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
-                    const uint32_t f = kbg % kA32Bufs, fph = (kbg / kA32Bufs) & 1;
-                    if (!mbar_wait(afree0 + 8 * f, fph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(afull0 + 8 * f, kA32Buf);
-                    const uint32_t dst = smem_u32(a32 + f * kA32Buf);
-                    // FP32 A map is (K, M, 1): the two 32-wide boxes of this K block
-                    tma_load_3d(dst, &mapA, afull0 + 8 * f, kb * 64, arow, 0);
-                    tma_load_3d(dst + kA32Box, &mapA, afull0 + 8 * f, kb * 64 + 32, arow, 0);
-                }
-            }
-            if (!ok) *abort_flag = 1;
-        }
-    } else if (FUSED && warp > kA32ProducerWarp) {
+    } else if (FUSED && warp >= 2 + Cfg::acc_warps) {
         // ------------------------------------------------------ split warps
         // Split every K block of this cluster's tiles, as soon as its FP32
         // block has landed and its stage is free, ahead of the tensor core.
-        const int w = warp - kA32ProducerWarp - 1;
+        const int w = warp - 2 - Cfg::acc_warps;
         const uint32_t aready_leader0 = map_to_rank(aready0, 0);
         const int my_tiles = cluster_id < total ? (total - 1 - cluster_id) / num_clusters + 1 : 0;
         const uint32_t my_blocks = uint32_t(my_tiles) * uint32_t(p.num_kb);
@@ -350,18 +349,20 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     } else if (warp >= 2) {
         // ------------------------------------------------ accumulator warps
         const int q = warp & 3;                        // TMEM lane quadrant
-        const int h = (warp - 2) >> 2;                 // column quarter of the tile
+        const int h = (warp - 2) >> 2;                 // column group of the tile
         const uint32_t cempty_leader0 = map_to_rank(cempty0, 0);
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
         bool ok = true;
-        uint32_t kbg = 0;
+        constexpr int KBP = Cfg::kb_per_partial;
+        const int nparts = (p.num_kb + KBP - 1) / KBP;   // TMEM partials per tile
+        uint32_t part = 0;
         for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
             float acc[kAccCols];
 #pragma unroll
             for (int j = 0; j < kAccCols; ++j) acc[j] = 0.0f;
-            for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
-                const uint32_t buf = kbg & 1, cph = (kbg >> 1) & 1;
+            for (int pi = 0; pi < nparts; ++pi, ++part) {
+                const uint32_t buf = part & 1, cph = (part >> 1) & 1;
                 if (!mbar_wait(cfull0 + 8 * buf, cph, p.err, kDevErrTimeout)) {
                     ok = false;
                     break;
