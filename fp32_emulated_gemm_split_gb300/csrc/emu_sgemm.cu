@@ -352,7 +352,11 @@ emu_status_t sgemm_device(int transA, int transB, int64_t M, int64_t N, int64_t 
                                           ldc, stream));
     }
     if (g_path < 0) g_path = read_path_env();
-    if (g_path == EMU_PATH_FUSED && fused_ok(mode, transA, A, lda))
+    // AUTO: the fused kernel splits A once per 128-column tile, so it pays off
+    // when N is small (measured on GB300: N = 256 MLIP layers 1.16x faster
+    // than two-pass; N = 1024 and square shapes slower).
+    const bool auto_fused = g_path == EMU_PATH_AUTO && N <= 256 && M >= 4096;
+    if ((g_path == EMU_PATH_FUSED || auto_fused) && fused_ok(mode, transA, A, lda))
         return run_fused(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream);
     return run_two_pass(mode == EMU_MODE_TF32X3, transA, transB, M, N, K, alpha, A, lda, B, ldb,
                         beta, C, ldc, d, stream);

@@ -77,9 +77,9 @@ struct KCfg {
     static constexpr int avail = kSmemMax - 2048 - a32_bytes;
     static constexpr int stages = avail / stage_bytes > 4 ? 4 : avail / stage_bytes;
     static constexpr int elems = TF32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
-    // K blocks summed in one TMEM partial before it is added to the registers:
-    // a TF32x3 block (32 elements, 12 MMAs) is short, so two are combined.
-    static constexpr int kb_per_partial = TF32 ? 2 : 1;
+    // K blocks summed in one TMEM partial before it is added to the registers
+    // (fewer promotions; each partial still holds only 8 full-magnitude MMAs).
+    static constexpr int kb_per_partial = 2;
     static constexpr int acc_warps = ::emu::acc_warps<FUSED>();
     static constexpr int acc_cols = BN / (acc_warps / 4);         // columns per accumulator thread
     static constexpr uint32_t tmem_cols = 2 * BN <= 256 ? 256 : 512;
