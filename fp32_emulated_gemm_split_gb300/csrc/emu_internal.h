@@ -14,12 +14,9 @@ enum : int {
     kDevErrTimeout = -5,
 };
 
-// Tile shape of the tensor-core GEMM (cta_group::1, one CTA per SM).
-constexpr int kTcBM = 128;          // rows of C per CTA (MMA M)
-constexpr int kTcBN = 256;          // columns of C per CTA (MMA N)
-constexpr int kTcBKBytes = 128;     // K extent of one stage in bytes (one 128-byte swizzle row)
-constexpr int kTcStages = 4;        // shared-memory pipeline depth
-constexpr int kTcThreads = 192;     // 4 epilogue warps, 1 TMA warp, 1 MMA warp
+// K extent of one staged piece tile in bytes: one 128-byte swizzled row
+// (64 BF16 or 32 TF32 elements).
+constexpr int kTcBKBytes = 128;
 
 // Row stride, in elements, of the split pieces in the workspace: a multiple
 // of 8 so that every row starts on a 16-byte boundary (a TMA requirement).
@@ -41,12 +38,6 @@ cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int6
                                 cudaStream_t stream);
 cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
                                 float* HI, float* LO, int64_t ldp, cudaStream_t stream);
-cudaError_t launch_gemm_tc(int tf32, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                           const TcGemmParams& p, cudaStream_t stream);
-cudaError_t launch_gemm_tc2(int tf32, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                            const TcGemmParams& p, int sms, cudaStream_t stream);
-cudaError_t launch_gemm_promote(int tf32, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                                const TcGemmParams& p, int sms, cudaStream_t stream);
 // tf32: TF32x3 pieces; bn: tile width 128 or 256; fused: mapA is a 2-D FP32
 // map over op(A) (box 32 x 128) split in shared memory (BF16x9, bn 128 only)
 cudaError_t launch_gemm_kblock(int tf32, int bn, int fused, const CUtensorMap& mapA,

@@ -86,21 +86,6 @@ emu_status_t from_cuda(cudaError_t e) {
     return EMU_ERR_CUDA;
 }
 
-// Which tensor-core kernel the two-pass path uses: 4 = CTA pairs, one K
-// block at a time with its bands in TMEM and the blocks summed in FP32
-// registers (default); 3 = CTA pairs, each band over all of K in 16-MMA
-// chunks summed in FP32 registers; 2 = CTA pairs accumulating all of K in
-// TMEM; 1 = one CTA per 128 x 256 tile accumulating in TMEM.
-// EMU_SGEMM_TC=1..4.
-int tc_variant() {
-    static int v = 0;
-    if (v == 0) {
-        const char* s = std::getenv("EMU_SGEMM_TC");
-        v = (s && s[0] >= '1' && s[0] <= '4') ? s[0] - '0' : 4;
-    }
-    return v;
-}
-
 // Tile width of the K-block kernel on the two-pass path: 256 (default) or
 // 128 (EMU_SGEMM_BN=128).
 int kblock_bn() {
@@ -262,30 +247,23 @@ emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N
     if (e != cudaSuccess) return from_cuda(e);
 
     const int box_cols = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
-    const int variant = tc_variant();
-    const bool pair = variant >= 2;
-    const int bn = variant == 4 ? kblock_bn() : 256;
-    const int tile_m = pair ? 256 : kTcBM, tile_n = pair ? bn : kTcBN;
-    const int box_a = pair ? 128 : kTcBM, box_b = pair ? bn / 2 : kTcBN;
+    const int bn = kblock_bn();
     CUtensorMap mapA, mapB;
-    st = make_plane_map(&mapA, wa, tf32, M, K, ldp, planes, box_cols, box_a);
+    st = make_plane_map(&mapA, wa, tf32, M, K, ldp, planes, box_cols, 128);
     if (st != EMU_OK) return st;
-    st = make_plane_map(&mapB, wb, tf32, N, K, ldp, planes, box_cols, box_b);
+    st = make_plane_map(&mapB, wb, tf32, N, K, ldp, planes, box_cols, bn / 2);
     if (st != EMU_OK) return st;
 
     TcGemmParams p;
     p.err = d->err;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
     p.num_kb = (int)((K + box_cols - 1) / box_cols);
-    p.tiles_m = (int)((M + tile_m - 1) / tile_m);
-    p.tiles_n = (int)((N + tile_n - 1) / tile_n);
+    p.tiles_m = (int)((M + 255) / 256);
+    p.tiles_n = (int)((N + bn - 1) / bn);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     {
         ProfScope ps(1, stream);
-        e = variant == 4 ? launch_gemm_kblock(tf32, bn, 0, mapA, mapB, p, d->sms, stream)
-            : variant == 3 ? launch_gemm_promote(tf32, mapA, mapB, p, d->sms, stream)
-            : variant == 2 ? launch_gemm_tc2(tf32, mapA, mapB, p, d->sms, stream)
-                           : launch_gemm_tc(tf32, mapA, mapB, p, stream);
+        e = launch_gemm_kblock(tf32, bn, 0, mapA, mapB, p, d->sms, stream);
     }
     return from_cuda(e);
 }

@@ -28,8 +28,9 @@
 // tcgen05.mma.cta_group::2 (M = 256, N = BN) reads both CTAs' shared memory.
 // Each stage has one "full" barrier per piece index so the band-4 MMAs start
 // when pieces 2 land.  Persistent: one cluster per SM pair walks the tiles;
-// two TMEM partial buffers let the tensor core fill one block's partial while
-// the other is added to the registers.
+// tensor memory holds 512/BN partial buffers, so the tensor core fills the
+// next partials (of this tile or the next) while earlier ones are added to
+// the registers and the epilogue stores C.
 //
 // Fused A (BF16x9, BN = 128): the producer loads the FP32 A block (128 rows
 // x 64, two 128-byte-swizzled boxes) into one of two staging buffers;
@@ -77,12 +78,17 @@ struct KCfg {
     static constexpr int avail = kSmemMax - 2048 - a32_bytes;
     static constexpr int stages = avail / stage_bytes > 4 ? 4 : avail / stage_bytes;
     static constexpr int elems = TF32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
-    // K blocks summed in one TMEM partial before it is added to the registers
-    // (fewer promotions; each partial still holds only 8 full-magnitude MMAs).
-    static constexpr int kb_per_partial = 2;
+    // K blocks summed in one TMEM partial before it is added to the registers.
+    // TF32x3 has no band shift, so two short blocks (12 MMAs each) share a
+    // partial; a BF16x9 partial holds one block, because the 2^-8 shift at a
+    // band change would also shift a previous block's finished sum.
+    static constexpr int kb_per_partial = TF32 ? 2 : 1;
+    // TMEM partial buffers of BN columns each (all 512 columns): 2 at BN = 256,
+    // 4 at BN = 128, so the tensor core can run further ahead of the epilogue.
+    static constexpr int nbuf = 512 / BN;
     static constexpr int acc_warps = ::emu::acc_warps<FUSED>();
     static constexpr int acc_cols = BN / (acc_warps / 4);         // columns per accumulator thread
-    static constexpr uint32_t tmem_cols = 2 * BN <= 256 ? 256 : 512;
+    static constexpr uint32_t tmem_cols = 512;
     static constexpr int smem = stages * stage_bytes + a32_bytes + 2048;
     // bytes a piece barrier waits for (both CTAs)
     static constexpr uint32_t piece_tx = FUSED ? 2 * b_tile : 2 * (kATile + b_tile);
@@ -178,12 +184,13 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     const int nb_full = S * P;
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * nb_full;
+    constexpr int NB = Cfg::nbuf;
     const uint32_t cfull0 = empty0 + 8 * S;
-    const uint32_t cempty0 = cfull0 + 16;
-    const uint32_t aready0 = cempty0 + 16;
+    const uint32_t cempty0 = cfull0 + 8 * NB;
+    const uint32_t aready0 = cempty0 + 8 * NB;
     const uint32_t afull0 = aready0 + 8 * S;
     const uint32_t afree0 = afull0 + 8 * kA32Bufs;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nb_full + 3 * S + 4 + 2 * kA32Bufs);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nb_full + 2 * S + 2 * NB + 2 * kA32Bufs);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -195,10 +202,10 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     if (threadIdx.x == 0) {
         for (int i = 0; i < nb_full; ++i) mbar_init(full0 + 8 * i, 1);
         for (int s = 0; s < S; ++s) mbar_init(empty0 + 8 * s, 1);
-        mbar_init(cfull0, 1);
-        mbar_init(cfull0 + 8, 1);
-        mbar_init(cempty0, 2 * Cfg::acc_warps);   // accumulator warps of both CTAs
-        mbar_init(cempty0 + 8, 2 * Cfg::acc_warps);
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(cfull0 + 8 * b, 1);
+            mbar_init(cempty0 + 8 * b, 2 * Cfg::acc_warps);   // accumulator warps of both CTAs
+        }
         if (FUSED) {
             for (int s = 0; s < S; ++s) mbar_init(aready0 + 8 * s, 2 * kSplitWarps);
             for (int f = 0; f < kA32Bufs; ++f) {
@@ -274,7 +281,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
             for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
                 const uint32_t s = kbg % S, ph = (kbg / S) & 1;
-                const uint32_t buf = part & 1, cph = (part >> 1) & 1;
+                const uint32_t buf = part % NB, cph = (part / NB) & 1;
                 const bool fresh = (kb % KBP) == 0;             // first block of a partial
                 const bool close = (kb % KBP) == KBP - 1 || kb == p.num_kb - 1;
                 if (fresh && !mbar_wait(cempty0 + 8 * buf, cph ^ 1, p.err, kDevErrTimeout)) {
@@ -362,7 +369,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
 #pragma unroll
             for (int j = 0; j < kAccCols; ++j) acc[j] = 0.0f;
             for (int pi = 0; pi < nparts; ++pi, ++part) {
-                const uint32_t buf = part & 1, cph = (part >> 1) & 1;
+                const uint32_t buf = part % NB, cph = (part / NB) & 1;
                 if (!mbar_wait(cfull0 + 8 * buf, cph, p.err, kDevErrTimeout)) {
                     ok = false;
                     break;

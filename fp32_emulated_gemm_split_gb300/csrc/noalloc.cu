@@ -185,5 +185,5 @@ extern "C" emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int
     p.tiles_m = (int)((M + 255) / 256);
     p.tiles_n = (int)((N + 255) / 256);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
-    return status_of(launch_gemm_promote(tf32, mapA, mapB, p, s->sms, stream));
+    return status_of(launch_gemm_kblock(tf32, 256, 0, mapA, mapB, p, s->sms, stream));
 }
