@@ -30,6 +30,7 @@ struct TcGemmParams {
     float alpha, beta;
     float* C;
     int64_t ldc;
+    int tma_store;       // 1: beta == 0 and the C tensor map is valid (bulk tensor stores)
 };
 
 // Launchers (return the launch status; nothing is synchronised).
@@ -41,8 +42,8 @@ cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int6
 // tf32: TF32x3 pieces; bn: tile width 128 or 256; fused: mapA is a 2-D FP32
 // map over op(A) (box 32 x 128) split in shared memory (BF16x9, bn 128 only)
 cudaError_t launch_gemm_kblock(int tf32, int bn, int fused, const CUtensorMap& mapA,
-                               const CUtensorMap& mapB, const TcGemmParams& p, int sms,
-                               cudaStream_t stream);
+                               const CUtensorMap& mapB, const CUtensorMap& mapC,
+                               const TcGemmParams& p, int sms, cudaStream_t stream);
 cudaError_t launch_gemm_simt(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                              const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
                              float* C, int64_t ldc, cudaStream_t stream);

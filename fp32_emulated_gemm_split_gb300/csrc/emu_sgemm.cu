@@ -187,6 +187,22 @@ emu_status_t make_plane_map(CUtensorMap* map, const void* base, bool fp32, int64
     return r == CUDA_SUCCESS ? EMU_OK : EMU_ERR_CUDA;
 }
 
+// 2-D map over C for the bulk tensor stores of the GEMM epilogue (beta == 0):
+// box of 16 columns x 32 rows, 64-byte swizzle.  Returns false (and the
+// kernel stores C directly) when C's rows are not 16-byte aligned.
+bool make_c_map(CUtensorMap* map, float* C, int64_t M, int64_t N, int64_t ldc, float beta) {
+    if (beta != 0.0f || (ldc % 4) != 0 || (reinterpret_cast<uintptr_t>(C) & 15) != 0) return false;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldc * 4)};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t elem_strides[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 emu_status_t check_gemm_args(int transA, int transB, int64_t M, int64_t N, int64_t K,
                              const float* A, int64_t lda, const float* B, int64_t ldb,
                              float beta, float* C, int64_t ldc, int mode) {
@@ -261,9 +277,11 @@ emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N
     p.tiles_m = (int)((M + 255) / 256);
     p.tiles_n = (int)((N + bn - 1) / bn);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
+    CUtensorMap mapC = mapB;                 // placeholder when C is stored directly
+    p.tma_store = make_c_map(&mapC, C, M, N, ldc, beta) ? 1 : 0;
     {
         ProfScope ps(1, stream);
-        e = launch_gemm_kblock(tf32, bn, 0, mapA, mapB, p, d->sms, stream);
+        e = launch_gemm_kblock(tf32, bn, 0, mapA, mapB, mapC, p, d->sms, stream);
     }
     return from_cuda(e);
 }
@@ -304,9 +322,11 @@ emu_status_t run_fused(int transB, int64_t M, int64_t N, int64_t K, float alpha,
     p.tiles_m = (int)((M + 255) / 256);
     p.tiles_n = (int)((N + bn - 1) / bn);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
+    CUtensorMap mapC = mapB;
+    p.tma_store = make_c_map(&mapC, C, M, N, ldc, beta) ? 1 : 0;
     {
         ProfScope ps(2, stream);
-        e = launch_gemm_kblock(0, bn, 1, mapA, mapB, p, d->sms, stream);
+        e = launch_gemm_kblock(0, bn, 1, mapA, mapB, mapC, p, d->sms, stream);
     }
     return from_cuda(e);
 }

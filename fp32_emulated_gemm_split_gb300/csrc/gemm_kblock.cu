@@ -75,7 +75,10 @@ struct KCfg {
     static constexpr int b_tile = b_rows * kTcBKBytes;
     static constexpr int stage_bytes = pieces * (kATile + b_tile);
     static constexpr int a32_bytes = FUSED ? kA32Bufs * kA32Buf : 0;
-    static constexpr int avail = kSmemMax - 2048 - a32_bytes;
+    // epilogue staging for bulk tensor stores: 32 rows x 16 FP32 per
+    // accumulator warp (2 KB)
+    static constexpr int c_bytes = ::emu::acc_warps<FUSED>() * 2048;
+    static constexpr int avail = kSmemMax - 2048 - a32_bytes - c_bytes;
     static constexpr int stages = avail / stage_bytes > 4 ? 4 : avail / stage_bytes;
     static constexpr int elems = TF32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
     // K blocks summed in one TMEM partial before it is added to the registers.
@@ -89,7 +92,7 @@ struct KCfg {
     static constexpr int acc_warps = ::emu::acc_warps<FUSED>();
     static constexpr int acc_cols = BN / (acc_warps / 4);         // columns per accumulator thread
     static constexpr uint32_t tmem_cols = 512;
-    static constexpr int smem = stages * stage_bytes + a32_bytes + 2048;
+    static constexpr int smem = stages * stage_bytes + a32_bytes + c_bytes + 2048;
     // bytes a piece barrier waits for (both CTAs)
     static constexpr uint32_t piece_tx = FUSED ? 2 * b_tile : 2 * (kATile + b_tile);
     static_assert(stages >= 2, "shared memory too small for two stages");
@@ -170,14 +173,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 template <int TF32, int BN, int FUSED>
 __global__ void __launch_bounds__(threads_k<FUSED>(), 1)
 gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
-                   const __grid_constant__ CUtensorMap mapB, const TcGemmParams p) {
+                   const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapC, const TcGemmParams p) {
     using Cfg = KCfg<TF32, BN, FUSED>;
     constexpr int S = Cfg::stages, P = Cfg::pieces, kAccCols = Cfg::acc_cols;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* a32 = smem + S * Cfg::stage_bytes;           // FP32 A staging (fused only)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(a32 + Cfg::a32_bytes);
+    uint8_t* cstage = a32 + Cfg::a32_bytes;               // epilogue staging for C
+    uint64_t* bars = reinterpret_cast<uint64_t*>(cstage + Cfg::c_bytes);
     // [0, S*P) piece full (leader), index s*P + piece | S stage empty |
     // 2 partial full | 2 partial empty (leader) | fused: S A-pieces ready
     // (leader), 2 FP32 full, 2 FP32 free
@@ -392,9 +397,39 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             // ---- epilogue: C = alpha * acc + beta * C
             int tm, tn;
             tile_pos(tile, p.tiles_m, p.tiles_n, tm, tn);
-            const int row = tm * kBM + int(rank) * kHalfRows + q * 32 + lane;
+            const int row0 = tm * kBM + int(rank) * kHalfRows + q * 32;
+            const int row = row0 + lane;
             const int col_base = tn * BN + h * kAccCols;
-            if (row < p.M && col_base < p.N) {
+            if (p.tma_store) {
+                // beta == 0: stage 32 rows x 16 columns at a time in this
+                // warp's 2 KB buffer (64-byte swizzle: conflict-free writes)
+                // and let one bulk tensor store write them, coalesced and
+                // clipped at the matrix edge.
+                const uint32_t cst = smem_u32(cstage + (warp - 2) * 2048);
+                if (row0 < p.M) {
+#pragma unroll
+                    for (int ch = 0; ch < kAccCols / 16; ++ch) {
+                        if (col_base + 16 * ch >= p.N) break;          // warp-uniform
+                        if (lane == 0) bulk_wait_read();                // buffer free again
+                        __syncwarp();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int j = 16 * ch + 4 * c;
+                            const uint32_t a = cst + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4);
+                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                                         :: "r"(a), "f"(p.alpha * acc[j]), "f"(p.alpha * acc[j + 1]),
+                                            "f"(p.alpha * acc[j + 2]), "f"(p.alpha * acc[j + 3])
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&mapC, col_base + 16 * ch, row0, cst);
+                            bulk_commit();
+                        }
+                    }
+                }
+            } else if (row < p.M && col_base < p.N) {
                 float* crow = p.C + (int64_t)row * p.ldc + col_base;
                 if (vec && col_base + kAccCols <= p.N) {
 #pragma unroll
@@ -427,6 +462,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             }
         }
         if (!ok) *abort_flag = 1;
+        if (p.tma_store && lane == 0) bulk_wait_all();        // C written before exit
     }
 
     __syncwarp();
@@ -441,7 +477,8 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
 
 template <int TF32, int BN, int FUSED>
 cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
-                            const TcGemmParams& p, int clusters, cudaStream_t stream) {
+                            const CUtensorMap& mapC, const TcGemmParams& p, int clusters,
+                            cudaStream_t stream) {
     using Cfg = KCfg<TF32, BN, FUSED>;
     static bool attr = false;
     if (!attr) {
@@ -462,27 +499,27 @@ cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kblock_kernel<TF32, BN, FUSED>, mapA, mapB, p);
+    return cudaLaunchKernelEx(&cfg, gemm_kblock_kernel<TF32, BN, FUSED>, mapA, mapB, mapC, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_kblock(int tf32, int bn, int fused, const CUtensorMap& mapA,
-                               const CUtensorMap& mapB, const TcGemmParams& p, int sms,
-                               cudaStream_t stream) {
+                               const CUtensorMap& mapB, const CUtensorMap& mapC,
+                               const TcGemmParams& p, int sms, cudaStream_t stream) {
     const int tiles = p.tiles_m * p.tiles_n;
     if (tiles == 0) return cudaSuccess;
     const int clusters = tiles < sms / 2 ? tiles : sms / 2;
     cudaError_t e;
     if (fused) {
         if (tf32 || bn != 128) return cudaErrorInvalidValue;
-        e = launch_kblock_t<0, 128, 1>(mapA, mapB, p, clusters, stream);
+        e = launch_kblock_t<0, 128, 1>(mapA, mapB, mapC, p, clusters, stream);
     } else if (tf32) {
-        e = bn == 128 ? launch_kblock_t<1, 128, 0>(mapA, mapB, p, clusters, stream)
-                      : launch_kblock_t<1, 256, 0>(mapA, mapB, p, clusters, stream);
+        e = bn == 128 ? launch_kblock_t<1, 128, 0>(mapA, mapB, mapC, p, clusters, stream)
+                      : launch_kblock_t<1, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
     } else {
-        e = bn == 128 ? launch_kblock_t<0, 128, 0>(mapA, mapB, p, clusters, stream)
-                      : launch_kblock_t<0, 256, 0>(mapA, mapB, p, clusters, stream);
+        e = bn == 128 ? launch_kblock_t<0, 128, 0>(mapA, mapB, mapC, p, clusters, stream)
+                      : launch_kblock_t<0, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

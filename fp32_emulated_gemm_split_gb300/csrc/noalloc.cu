@@ -185,5 +185,6 @@ extern "C" emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int
     p.tiles_m = (int)((M + 255) / 256);
     p.tiles_n = (int)((N + 255) / 256);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
-    return status_of(launch_gemm_kblock(tf32, 256, 0, mapA, mapB, p, s->sms, stream));
+    p.tma_store = 0;                         // C stored directly by the epilogue warps
+    return status_of(launch_gemm_kblock(tf32, 256, 0, mapA, mapB, mapB, p, s->sms, stream));
 }
