@@ -90,6 +90,9 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_gemm_tf32x3.restype = None
     L.oracle_gemm_fp32.argtypes = gemm_args + [_vp]
     L.oracle_gemm_fp32.restype = None
+    for name in ("oracle_gemm_bf16x3", "oracle_gemm_tf32"):
+        getattr(L, name).argtypes = gemm_args + [_vp]
+        getattr(L, name).restype = None
     L.oracle_max_threads.argtypes = []
     L.oracle_max_threads.restype = _int
     return L
@@ -225,10 +228,24 @@ def gemm_tf32x3(A, B, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None,
                 pairs, with_bands)
 
 
-def gemm_fp32(A, B, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None, pairs=None, L=None):
-    """Plain FP32 GEMM: sequential accumulation, product and sum rounded separately."""
+def _plain(fn_name, A, B, transA, transB, alpha, beta, C0, pairs, L):
     A, lda, B, ldb, C0, ldc0, M, N, K, mi, ni, full = _gemm_setup(A, B, transA, transB, C0, beta, pairs)
     C = np.empty(mi.size, np.float32)
-    (L or lib()).oracle_gemm_fp32(*_common_args(transA, transB, M, N, K, alpha, A, lda, B, ldb,
-                                         beta, C0, ldc0, mi, ni), _ptr(C))
+    getattr(L or lib(), fn_name)(*_common_args(transA, transB, M, N, K, alpha, A, lda, B, ldb,
+                                               beta, C0, ldc0, mi, ni), _ptr(C))
     return C.reshape(M, N) if full else C
+
+
+def gemm_fp32(A, B, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None, pairs=None, L=None):
+    """Plain FP32 GEMM: sequential accumulation, product and sum rounded separately."""
+    return _plain("oracle_gemm_fp32", A, B, transA, transB, alpha, beta, C0, pairs, L)
+
+
+def gemm_bf16x3(A, B, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None, pairs=None, L=None):
+    """Two BF16 pieces, three products (a0 b0, a0 b1, a1 b0), band 1 first."""
+    return _plain("oracle_gemm_bf16x3", A, B, transA, transB, alpha, beta, C0, pairs, L)
+
+
+def gemm_tf32(A, B, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None, pairs=None, L=None):
+    """Single-pass TF32: one product of the leading TF32 pieces."""
+    return _plain("oracle_gemm_tf32", A, B, transA, transB, alpha, beta, C0, pairs, L)

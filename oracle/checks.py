@@ -14,7 +14,9 @@ criteria below make that concrete:
   land among FP32 subnormals (absolute spacing 2^-149).
 * TF32x3 drops the residual*residual product and its residual is itself
   rounded to TF32, which costs at most 3 * 2^-22 |a||b| < 2^-20 |a||b| per
-  product, so its bound adds 2^-20 |alpha| S_abs.
+  product, so its bound adds 2^-20 |alpha| S_abs.  The cheaper rungs (two
+  BF16 pieces, single-pass TF32) add their own representation error
+  (MODE_EXTRA).
 * relative Frobenius error ||C - C_ref||_F / ||C_ref||_F <= 2e-6 on
   normally distributed inputs.
 """
@@ -27,10 +29,17 @@ SUB = 2.0 ** -149
 FROBENIUS_TOL = 2e-6
 
 
+# Representation error of the cheaper modes, per product, relative to |a||b|.
+# Two BF16 pieces leave |x - x0 - 2^-8 x1| <= 2^-18 |x|, so the kept products
+# miss at most about 2 * 2^-18 and the dropped 2^-16 a1 b1 adds at most about
+# 2^-18 more: below 2^-16 in all.  One TF32 piece leaves |x - hi| <= 2^-11 |x|,
+# so the product misses at most 2 * 2^-11 + 2^-22 < 2^-10 + 2^-21.
+MODE_EXTRA = {"bf16x9": 0.0, "tf32x3": 2.0 ** -20,
+              "bf16x3": 2.0 ** -16, "tf32": 2.0 ** -10 + 2.0 ** -21}
+
+
 def elementwise_bound(K, alpha, beta, Sabs, C0=None, mode="bf16x9"):
-    base = (2 * K + 2) * U
-    if mode == "tf32x3":
-        base += 2.0 ** -20
+    base = (2 * K + 2) * U + MODE_EXTRA[mode]
     b = base * abs(float(alpha)) * np.asarray(Sabs, np.float64)
     if beta != 0.0:
         b = b + 2 * U * abs(float(beta)) * np.abs(np.asarray(C0, np.float64))

@@ -311,6 +311,74 @@ void oracle_gemm_tf32x3(int transA, int transB, int64_t M, int64_t N, int64_t K,
 }
 
 /* ------------------------------------------------------------------------ */
+/* The cheaper rungs the pages set BF16x9 and TF32x3 against.                */
+/* ------------------------------------------------------------------------ */
+
+/* "FP32 as the sum of two BF16" (the discuss.pytorch.kr page, on PyTorch's
+ * "high" matmul precision): the first two pieces of the three-way split,
+ * x ~ x0 + 2^-8 x1, and the three products a0 b0, a0 b1, a1 b0 -- band 1
+ * (a0 b1 then a1 b0 for each k) before band 0, each product scaled by its
+ * band weight; a1 b1 and the third pieces are dropped. */
+void oracle_gemm_bf16x3(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                        float alpha, const float* A, int64_t lda,
+                        const float* B, int64_t ldb,
+                        float beta, const float* C0, int64_t ldc0,
+                        const int64_t* mi, const int64_t* ni, int64_t npairs, float* C) {
+    (void)M; (void)N;
+    #pragma omp parallel
+    {
+        int64_t kk = K > 0 ? K : 1;
+        uint16_t* ap = (uint16_t*)malloc(sizeof(uint16_t) * 3 * kk);
+        uint16_t* bp = (uint16_t*)malloc(sizeof(uint16_t) * 3 * kk);
+        #pragma omp for schedule(dynamic, 16)
+        for (int64_t p = 0; p < npairs; ++p) {
+            int64_t m = mi[p], n = ni[p];
+            float acc = 0.0f;
+            if (alpha != 0.0f) {
+                for (int64_t k = 0; k < K; ++k) {
+                    split3_one(op_at(A, lda, transA, m, k), &ap[k], &ap[kk + k], &ap[2 * kk + k]);
+                    split3_one(op_at(B, ldb, transB, k, n), &bp[k], &bp[kk + k], &bp[2 * kk + k]);
+                }
+                for (int64_t k = 0; k < K; ++k) {
+                    float t1 = oracle_bf16_to_f32(ap[k]) * oracle_bf16_to_f32(bp[kk + k]);
+                    acc += ldexpf(t1, -8);
+                    float t2 = oracle_bf16_to_f32(ap[kk + k]) * oracle_bf16_to_f32(bp[k]);
+                    acc += ldexpf(t2, -8);
+                }
+                for (int64_t k = 0; k < K; ++k)
+                    acc += oracle_bf16_to_f32(ap[k]) * oracle_bf16_to_f32(bp[k]);
+            }
+            C[p] = epilogue(alpha, acc, beta, C0, ldc0, m, n);
+        }
+        free(ap);
+        free(bp);
+    }
+}
+
+/* Single-pass TF32 ([NV] Figures 5-8, "one-pass TF32"): hi_a * hi_b only. */
+void oracle_gemm_tf32(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                      float alpha, const float* A, int64_t lda,
+                      const float* B, int64_t ldb,
+                      float beta, const float* C0, int64_t ldc0,
+                      const int64_t* mi, const int64_t* ni, int64_t npairs, float* C) {
+    (void)M; (void)N;
+    #pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t p = 0; p < npairs; ++p) {
+        int64_t m = mi[p], n = ni[p];
+        float acc = 0.0f;
+        if (alpha != 0.0f) {
+            for (int64_t k = 0; k < K; ++k) {
+                float ah, al, bh, bl;
+                split2_one(op_at(A, lda, transA, m, k), &ah, &al);
+                split2_one(op_at(B, ldb, transB, k, n), &bh, &bl);
+                acc += ah * bh;
+            }
+        }
+        C[p] = epilogue(alpha, acc, beta, C0, ldc0, m, n);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Plain FP32 GEMM (the "native FP32" the pages compare against).            */
 /* ------------------------------------------------------------------------ */
 

@@ -338,3 +338,78 @@ def test_mutant_dropping_tf32_mixed_term_fails_band_pin():
     Cm = oracle.gemm_tf32x3(A, B, L=L)
     Cref, Sabs = oracle.gemm_ref(A, B)
     assert checks.error_ratio(Cm, Cref, Sabs, 16, 1.0, 0.0, mode="tf32x3") > 1.0
+
+
+# --------------------------------------------------------------------------
+# The cheaper rungs: two BF16 pieces (three products) and single-pass TF32
+# --------------------------------------------------------------------------
+
+def test_bf16x3_identity_keeps_the_first_two_pieces():
+    X = W.normal(R(81), (64, 64))
+    I = np.eye(64, dtype=np.float32)
+    p0, p1, _ = oracle.split_bf16x3(X)
+    f = oracle.bf16_bits_to_f32
+    expect = (f(p0).astype(np.float64) + np.ldexp(f(p1), -8)).astype(np.float32)
+    assert np.array_equal(oracle.gemm_bf16x3(I, X), expect)
+    assert np.array_equal(oracle.gemm_bf16x3(X, I), expect)
+
+
+def test_tf32_identity_keeps_the_leading_piece():
+    X = W.normal(R(82), (64, 64))
+    I = np.eye(64, dtype=np.float32)
+    hi, _ = oracle.split_tf32x2(X)
+    assert np.array_equal(oracle.gemm_tf32(I, X), hi)
+    assert np.array_equal(oracle.gemm_tf32(X, I), hi)
+
+
+@pytest.mark.parametrize("mode,fn", [("bf16x3", oracle.gemm_bf16x3), ("tf32", oracle.gemm_tf32)])
+def test_cheaper_rungs_within_their_bounds_and_ordered(mode, fn):
+    r = R(83)
+    A = W.normal(r, (128, 512))
+    B = W.normal(r, (512, 96))
+    Cref, Sabs = oracle.gemm_ref(A, B)
+    C = fn(A, B)
+    assert checks.error_ratio(C, Cref, Sabs, 512, 1.0, 0.0, mode=mode) <= 1.0
+    # the ladder the pages describe: the cheaper rung is less accurate
+    e = checks.rel_frobenius(C, Cref)
+    e9 = checks.rel_frobenius(oracle.gemm_bf16x9(A, B), Cref)
+    e3 = checks.rel_frobenius(oracle.gemm_tf32x3(A, B), Cref)
+    assert e > 5 * max(e9, e3)
+    assert e > checks.FROBENIUS_TOL       # misses the criterion BF16x9 and TF32x3 meet
+
+
+def test_bf16x3_exact_on_16_bit_integers():
+    r = R(84)
+    A = r.integers(-(1 << 15), 1 << 15, (8, 8)).astype(np.float32)   # 16 significant bits
+    B = r.integers(-1, 2, (8, 8)).astype(np.float32)
+    exact = A.astype(np.float64) @ B.astype(np.float64)
+    assert np.array_equal(oracle.gemm_bf16x3(A, B), exact.astype(np.float32))
+
+
+def test_cheaper_rungs_drop_exactly_the_stated_terms():
+    """1x1x1 closed forms: which pieces and products each rung keeps."""
+    def one(fn, a, b):
+        return float(fn(np.array([[a]], np.float32), np.array([[b]], np.float32))[0, 0])
+    x = 1 + 2.0 ** -8                   # pieces (1, 1, 0)
+    y = 1 + 2.0 ** -9 + 2.0 ** -18      # pieces (1, 2^-1, 2^-2)
+    # two pieces: a0 b0 + 2^-8 (a0 b1 + a1 b0); a1 b1 = 2^-16 is dropped
+    assert one(oracle.gemm_bf16x3, x, x) == 1 + 2.0 ** -7
+    assert one(oracle.gemm_bf16x9, x, x) == 1 + 2.0 ** -7 + 2.0 ** -16
+    # the third piece never enters
+    assert one(oracle.gemm_bf16x3, y, y) == 1 + 2.0 ** -8
+    assert one(oracle.gemm_bf16x3, x, y) == 1 + 2.0 ** -8 + 2.0 ** -9
+    # single-pass TF32: 10 explicit mantissa bits kept, the rest rounded away
+    z = 1 + 2.0 ** -10
+    assert one(oracle.gemm_tf32, z, z) == 1 + 2.0 ** -9 + 2.0 ** -20
+    assert one(oracle.gemm_tf32, 1 + 2.0 ** -11, 3.0) == 3.0           # tie to even
+    assert one(oracle.gemm_tf32, 1 + 3 * 2.0 ** -12, 1.0) == 1 + 2.0 ** -10
+    # TF32x3 keeps hi*lo and lo*hi
+    assert one(oracle.gemm_tf32x3, 1 + 2.0 ** -11, 1 + 2.0 ** -11) == 1 + 2.0 ** -10
+
+
+def test_mutant_keeping_a1b1_in_bf16x3_fails_closed_form():
+    L = _mutant(r"acc \+= ldexpf\(t2, -8\);",
+                "acc += ldexpf(t2, -8); acc += ldexpf(oracle_bf16_to_f32(ap[kk + k]) * "
+                "oracle_bf16_to_f32(bp[kk + k]), -16);")
+    x = np.array([[1 + 2.0 ** -8]], np.float32)
+    assert float(oracle.gemm_bf16x3(x, x, L=L)[0, 0]) != 1 + 2.0 ** -7
