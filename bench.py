@@ -11,7 +11,7 @@ Each operand is 256 MiB, larger than the 129 MB L2, so no flush is needed
 between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--mode bf16x9|tf32x3|fp32_simt] [--impl reference]
+                  [--mode bf16x9|tf32x3|bf16x3|tf32|fp32_simt] [--impl reference]
 
 --impl reference times the CPU oracle (the plain reference implementation of
 the method) on the host cores, on a bounded block of rows of the same
@@ -208,7 +208,8 @@ def bench_gpu(args):
     else:
         dom_name, (n_dom, ms_dom) = "gemm_tc", prof["gemm_tc"]
     per_launch_ms = ms_dom / max(n_dom, 1)
-    products = {"bf16x9": 9, "tf32x3": 3, "fp32_simt": 1}[g.mode]
+    products = {"bf16x9": 9, "tf32x3": 3, "bf16x3": 3, "tf32": 1, "fp32_simt": 1}[g.mode]
+    tf32_mode = g.mode in ("tf32x3", "tf32")
     if g.mode == "fp32_simt":
         roofline = {"bound": "alu", "achieved": flops / (per_launch_ms * 1e-3) / 1e12,
                     "peak": None, "unit": "TFLOP/s", "frac": None, "traffic": None}
@@ -216,11 +217,11 @@ def bench_gpu(args):
         # tensor FLOPs per launch: products * 2MNK; TF32 runs at half the BF16 rate
         tensor_flops = products * flops
         achieved = tensor_flops / (per_launch_ms * 1e-3) / 1e12
-        peak = p_bf16 if g.mode == "bf16x9" else p_bf16 / 2.0
+        peak = p_bf16 / 2.0 if tf32_mode else p_bf16
         roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                     "kernel": dom_name,
-                    "peak_source": f"{peak_src} bf16 burst" + (" / 2 (tf32 nominal ratio)" if g.mode == "tf32x3" else ""),
+                    "peak_source": f"{peak_src} bf16 burst" + (" / 2 (tf32 nominal ratio)" if tf32_mode else ""),
                     "kernel_ms": round(per_launch_ms, 4)}
         traffic = load_traffic(dom_name, args.workload, g.mode)
         if traffic is not None:
@@ -341,13 +342,18 @@ def bench_simt(emu, g, dA, dB, dC, stream):
             "ms_per_call": round(ms, 3)}
 
 
+def ORACLE_FN(oracle):
+    return {"bf16x9": oracle.gemm_bf16x9, "tf32x3": oracle.gemm_tf32x3,
+            "bf16x3": oracle.gemm_bf16x3, "tf32": oracle.gemm_tf32,
+            "fp32_simt": oracle.gemm_fp32}
+
+
 def cpu_baseline(g, A, B, C0, seconds):
     """The CPU oracle (plain C, OpenMP over the host cores) on a block of rows
     of the same GEMM, scaled to the metric's unit."""
     import numpy as np
     import oracle
-    fn = {"bf16x9": oracle.gemm_bf16x9, "tf32x3": oracle.gemm_tf32x3,
-          "fp32_simt": oracle.gemm_fp32}[g.mode]
+    fn = ORACLE_FN(oracle)[g.mode]
     threads = oracle.max_threads()
 
     def rows_pairs(r):
@@ -382,8 +388,7 @@ def bench_reference(args):
     g = pick_workload(W, args)
     A, B, C0 = W.generate(g)
     oracle.build()
-    fn = {"bf16x9": oracle.gemm_bf16x9, "tf32x3": oracle.gemm_tf32x3,
-          "fp32_simt": oracle.gemm_fp32}[g.mode]
+    fn = ORACLE_FN(oracle)[g.mode]
     # each step is a block of rows sized so the whole run takes a few minutes
     budget = max(20.0, min(150.0, args.cpu_seconds * 6))
     per_step = budget / (args.steps + args.warmup)
@@ -424,7 +429,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="square8192_normal")
-    ap.add_argument("--mode", default=None, choices=[None, "bf16x9", "tf32x3", "fp32_simt"])
+    ap.add_argument("--mode", default=None,
+                    choices=[None, "bf16x9", "tf32x3", "bf16x3", "tf32", "fp32_simt"])
     ap.add_argument("--impl", default="emu", choices=["emu", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")

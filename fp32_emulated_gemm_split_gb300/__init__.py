@@ -17,7 +17,7 @@ import os
 
 from . import _build
 
-MODE = {"bf16x9": 0, "tf32x3": 1, "fp32_simt": 2}
+MODE = {"bf16x9": 0, "tf32x3": 1, "fp32_simt": 2, "bf16x3": 3, "tf32": 4}
 PATH = {"auto": 0, "twopass": 1, "fused": 2}
 PROFILE_KIND = {"split": 0, "gemm_tc": 1, "gemm_fused": 2, "gemm_simt": 3, "scale": 4}
 

@@ -14,6 +14,19 @@ enum : int {
     kDevErrTimeout = -5,
 };
 
+// Tensor-core GEMM variants (the values of the public emu_mode_t):
+// pieces per operand and the products each K block runs.
+enum : int {
+    kModeBf16x9 = 0,     // 3 BF16 pieces, 9 products in 5 bands
+    kModeTf32x3 = 1,     // 2 TF32 pieces, 3 products
+    kModeFp32Simt = 2,   // no pieces: the CUDA-core FP32 kernel
+    kModeBf16x3 = 3,     // 2 BF16 pieces, 3 products in 2 bands
+    kModeTf32 = 4,       // 1 TF32 piece, 1 product
+};
+constexpr bool valid_mode(int m) { return m >= kModeBf16x9 && m <= kModeTf32; }
+constexpr bool mode_is_tf32(int m) { return m == kModeTf32x3 || m == kModeTf32; }
+constexpr int mode_pieces(int m) { return m == kModeBf16x9 ? 3 : m == kModeTf32 ? 1 : 2; }
+
 // K extent of one staged piece tile in bytes: one 128-byte swizzled row
 // (64 BF16 or 32 TF32 elements).
 constexpr int kTcBKBytes = 128;
@@ -39,9 +52,16 @@ cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int6
                                 cudaStream_t stream);
 cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
                                 float* HI, float* LO, int64_t ldp, cudaStream_t stream);
-// tf32: TF32x3 pieces; bn: tile width 128 or 256; fused: mapA is a 2-D FP32
-// map over op(A) (box 32 x 128) split in shared memory (BF16x9, bn 128 only)
-cudaError_t launch_gemm_kblock(int tf32, int bn, int fused, const CUtensorMap& mapA,
+// The pieces a tensor-core mode reads, as consecutive planes of rows x ldp
+// elements (BF16 bits or TF32-valued FP32) starting at `planes`.
+cudaError_t launch_split_pieces(int mode, const float* X, int64_t rows, int64_t cols, int64_t ld,
+                                int trans, void* planes, int64_t ldp, cudaStream_t stream);
+// Bytes of one piece element of a mode.
+constexpr int mode_piece_bytes(int m) { return mode_is_tf32(m) ? 4 : 2; }
+// mode: one of the kMode* variants; bn: tile width 128 or 256 (the two
+// cheaper modes: 256 only); fused: mapA is an FP32 map over op(A) (box
+// 32 x 128) split in shared memory (BF16x9, bn 128 only)
+cudaError_t launch_gemm_kblock(int mode, int bn, int fused, const CUtensorMap& mapA,
                                const CUtensorMap& mapB, const CUtensorMap& mapC,
                                const TcGemmParams& p, int sms, cudaStream_t stream);
 cudaError_t launch_gemm_simt(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,

@@ -15,6 +15,11 @@ namespace emu {
 
 __device__ int g_emu_error = 0;
 
+static_assert(kModeBf16x9 == EMU_MODE_BF16X9 && kModeTf32x3 == EMU_MODE_TF32X3 &&
+                  kModeFp32Simt == EMU_MODE_FP32_SIMT && kModeBf16x3 == EMU_MODE_BF16X3 &&
+                  kModeTf32 == EMU_MODE_TF32,
+              "kernel variants follow emu_mode_t");
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -207,8 +212,7 @@ emu_status_t check_gemm_args(int transA, int transB, int64_t M, int64_t N, int64
                              const float* A, int64_t lda, const float* B, int64_t ldb,
                              float beta, float* C, int64_t ldc, int mode) {
     if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return EMU_ERR_INVALID_VALUE;
-    if (mode != EMU_MODE_BF16X9 && mode != EMU_MODE_TF32X3 && mode != EMU_MODE_FP32_SIMT)
-        return EMU_ERR_INVALID_VALUE;
+    if (!valid_mode(mode)) return EMU_ERR_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0) return EMU_ERR_INVALID_VALUE;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return EMU_ERR_INVALID_VALUE;
     const int64_t a_cols = transA ? M : K, b_cols = transB ? K : N;
@@ -221,12 +225,13 @@ emu_status_t check_gemm_args(int transA, int transB, int64_t M, int64_t N, int64
     return EMU_OK;
 }
 
-emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N, int64_t K,
+emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
                           float alpha, const float* A, int64_t lda, const float* B, int64_t ldb,
                           float beta, float* C, int64_t ldc, DeviceState* d, cudaStream_t stream) {
     const int64_t ldp = plane_ld(K);
-    const int planes = tf32 ? 2 : 3;
-    const int esize = tf32 ? 4 : 2;
+    const int tf32 = mode_is_tf32(mode);
+    const int planes = mode_pieces(mode);
+    const int esize = mode_piece_bytes(mode);
     const size_t a_bytes = (size_t)planes * M * ldp * esize;
     const size_t b_bytes = (size_t)planes * N * ldp * esize;
     const size_t a_region = (a_bytes + 1023) / 1024 * 1024;
@@ -238,32 +243,19 @@ emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N
     cudaError_t e;
     {
         ProfScope ps(0, stream);
-        if (tf32) {
-            float* pa = reinterpret_cast<float*>(wa);
-            e = launch_split_tf32x2(A, M, K, lda, transA, pa, pa + M * ldp, ldp, stream);
-        } else {
-            uint16_t* pa = reinterpret_cast<uint16_t*>(wa);
-            e = launch_split_bf16x3(A, M, K, lda, transA, pa, pa + M * ldp, pa + 2 * M * ldp, ldp,
-                                    stream);
-        }
+        e = launch_split_pieces(mode, A, M, K, lda, transA, wa, ldp, stream);
     }
     if (e != cudaSuccess) return from_cuda(e);
     {
         // op(B)^T is N x K: B itself when transB == 1, B^T otherwise
         ProfScope ps(0, stream);
-        if (tf32) {
-            float* pb = reinterpret_cast<float*>(wb);
-            e = launch_split_tf32x2(B, N, K, ldb, !transB, pb, pb + N * ldp, ldp, stream);
-        } else {
-            uint16_t* pb = reinterpret_cast<uint16_t*>(wb);
-            e = launch_split_bf16x3(B, N, K, ldb, !transB, pb, pb + N * ldp, pb + 2 * N * ldp, ldp,
-                                    stream);
-        }
+        e = launch_split_pieces(mode, B, N, K, ldb, !transB, wb, ldp, stream);
     }
     if (e != cudaSuccess) return from_cuda(e);
 
     const int box_cols = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
-    const int bn = kblock_bn();
+    // the two cheaper modes are built for 256-wide tiles only
+    const int bn = (mode == kModeBf16x9 || mode == kModeTf32x3) ? kblock_bn() : 256;
     CUtensorMap mapA, mapB;
     st = make_plane_map(&mapA, wa, tf32, M, K, ldp, planes, box_cols, 128);
     if (st != EMU_OK) return st;
@@ -281,7 +273,7 @@ emu_status_t run_two_pass(int tf32, int transA, int transB, int64_t M, int64_t N
     p.tma_store = make_c_map(&mapC, C, M, N, ldc, beta) ? 1 : 0;
     {
         ProfScope ps(1, stream);
-        e = launch_gemm_kblock(tf32, bn, 0, mapA, mapB, mapC, p, d->sms, stream);
+        e = launch_gemm_kblock(mode, bn, 0, mapA, mapB, mapC, p, d->sms, stream);
     }
     return from_cuda(e);
 }
@@ -356,8 +348,8 @@ emu_status_t sgemm_device(int transA, int transB, int64_t M, int64_t N, int64_t 
     const bool auto_fused = g_path == EMU_PATH_AUTO && N <= 256 && M >= 4096;
     if ((g_path == EMU_PATH_FUSED || auto_fused) && fused_ok(mode, transA, A, lda))
         return run_fused(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream);
-    return run_two_pass(mode == EMU_MODE_TF32X3, transA, transB, M, N, K, alpha, A, lda, B, ldb,
-                        beta, C, ldc, d, stream);
+    return run_two_pass(mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d,
+                        stream);
 }
 
 emu_status_t check_split_args(const void* X, int64_t rows, int64_t cols, int64_t ld, int trans,
@@ -473,8 +465,8 @@ int emu_get_path(void) {
 
 size_t emu_workspace_size(int64_t M, int64_t N, int64_t K, int mode) {
     if (M <= 0 || N <= 0 || K <= 0 || mode == EMU_MODE_FP32_SIMT) return 0;
-    const int tf32 = mode == EMU_MODE_TF32X3;
-    const size_t per = (size_t)(tf32 ? 2 : 3) * plane_ld(K) * (tf32 ? 4 : 2);
+    if (!valid_mode(mode)) return 0;
+    const size_t per = (size_t)mode_pieces(mode) * plane_ld(K) * mode_piece_bytes(mode);
     return (per * M + 1023) / 1024 * 1024 + per * N;
 }
 

@@ -9,7 +9,11 @@
 // "Blackwell의 BF16x9"): three BF16 pieces per operand, nine products a_i b_j
 // in five bands b = i + j of weight 2^-8b, accumulated in FP32 smallest band
 // first.  TF32x3 (Figure 2 and its equation): residual band hi*lo + lo*hi,
-// then hi*hi, no scaling.
+// then hi*hi, no scaling.  The two cheaper rungs the pages compare against
+// run on the same pipeline: two BF16 pieces (band 1 = a0 b1 + a1 b0, then
+// band 0 = a0 b0 after a 2^-8 shift; the discuss.pytorch.kr page's "FP32 as
+// the sum of two BF16") and single-pass TF32 (one product, the blog post's
+// one-pass TF32 of Figures 5-8).
 //
 // Schedule.  For each 64-element K block (32 for TF32x3) the pieces of A and
 // B are staged once, and the tensor core runs the bands of that block
@@ -68,9 +72,10 @@ constexpr int kA32Box = 128 * 128;                    // FP32 box: 128 rows x 32
 constexpr int kA32Buf = 2 * kA32Box;                  // one 64-wide K block of FP32 A
 constexpr int kA32Bufs = 2;
 
-template <int TF32, int BN, int FUSED>
+template <int MODE, int BN, int FUSED>
 struct KCfg {
-    static constexpr int pieces = TF32 ? 2 : 3;
+    static constexpr bool tf32 = mode_is_tf32(MODE);
+    static constexpr int pieces = mode_pieces(MODE);
     static constexpr int b_rows = BN / 2;                        // B^T rows per CTA
     static constexpr int b_tile = b_rows * kTcBKBytes;
     static constexpr int stage_bytes = pieces * (kATile + b_tile);
@@ -79,13 +84,16 @@ struct KCfg {
     // accumulator warp (2 KB)
     static constexpr int c_bytes = ::emu::acc_warps<FUSED>() * 2048;
     static constexpr int avail = kSmemMax - 2048 - a32_bytes - c_bytes;
-    static constexpr int stages = avail / stage_bytes > 4 ? 4 : avail / stage_bytes;
-    static constexpr int elems = TF32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
+    static constexpr int max_stages = pieces == 1 ? 6 : 4;
+    static constexpr int stages = avail / stage_bytes > max_stages ? max_stages : avail / stage_bytes;
+    static constexpr int elems = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
     // K blocks summed in one TMEM partial before it is added to the registers.
     // TF32x3 has no band shift, so two short blocks (12 MMAs each) share a
-    // partial; a BF16x9 partial holds one block, because the 2^-8 shift at a
-    // band change would also shift a previous block's finished sum.
-    static constexpr int kb_per_partial = TF32 ? 2 : 1;
+    // partial, and single-pass TF32 eight blocks (32 MMAs; its 2^-11 piece
+    // error dwarfs the tensor core's truncation).  A BF16 partial holds one
+    // block, because the 2^-8 shift at a band change would also shift a
+    // previous block's finished sum.
+    static constexpr int kb_per_partial = MODE == kModeTf32x3 ? 2 : MODE == kModeTf32 ? 8 : 1;
     // TMEM partial buffers of BN columns each (all 512 columns): 2 at BN = 256,
     // 4 at BN = 128, so the tensor core can run further ahead of the epilogue.
     static constexpr int nbuf = 512 / BN;
@@ -96,7 +104,7 @@ struct KCfg {
     // bytes a piece barrier waits for (both CTAs)
     static constexpr uint32_t piece_tx = FUSED ? 2 * b_tile : 2 * (kATile + b_tile);
     static_assert(stages >= 2, "shared memory too small for two stages");
-    static_assert(!(FUSED && TF32), "the fused path splits BF16x9 pieces only");
+    static_assert(!(FUSED && MODE != kModeBf16x9), "the fused path splits BF16x9 pieces only");
 };
 
 __device__ __forceinline__ void tile_pos(int tile, int tiles_m, int tiles_n, int& tm, int& tn) {
@@ -170,12 +178,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <int TF32, int BN, int FUSED>
+template <int MODE, int BN, int FUSED>
 __global__ void __launch_bounds__(threads_k<FUSED>(), 1)
 gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapC, const TcGemmParams p) {
-    using Cfg = KCfg<TF32, BN, FUSED>;
+    using Cfg = KCfg<MODE, BN, FUSED>;
     constexpr int S = Cfg::stages, P = Cfg::pieces, kAccCols = Cfg::acc_cols;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -279,7 +287,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         if (!ok) *abort_flag = 1;
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------ MMA issuer
-        const uint32_t idesc = make_idesc(TF32 ? 2u : 1u, kBM, BN);
+        const uint32_t idesc = make_idesc(Cfg::tf32 ? 2u : 1u, kBM, BN);
         constexpr int KBP = Cfg::kb_per_partial;
         uint32_t kbg = 0, part = 0;              // K blocks and TMEM partials so far
         bool ok = true;
@@ -307,7 +315,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     tc_fence_after();
                     return r;
                 };
-                if constexpr (!TF32) {
+                if constexpr (MODE == kModeBf16x9) {
                     if (!ready(2)) { ok = false; break; }
                     mma_pair<0>(d, A(2), B(2), idesc, true, false);           // band 4
                     if (!ready(1)) { ok = false; break; }
@@ -320,11 +328,19 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     mma_pair<0>(d, A(0), B(1), idesc, false, true);           // band 1
                     mma_pair<0>(d, A(1), B(0), idesc, false, false);
                     mma_pair<0>(d, A(0), B(0), idesc, false, true);           // band 0
-                } else {
+                } else if constexpr (MODE == kModeTf32x3) {
                     if (!ready(1) || !ready(0)) { ok = false; break; }
                     mma_pair<1>(d, A(0), B(1), idesc, fresh, false);          // hi*lo
                     mma_pair<1>(d, A(1), B(0), idesc, false, false);          // lo*hi
                     mma_pair<1>(d, A(0), B(0), idesc, false, false);          // hi*hi
+                } else if constexpr (MODE == kModeBf16x3) {
+                    if (!ready(1) || !ready(0)) { ok = false; break; }
+                    mma_pair<0>(d, A(0), B(1), idesc, true, false);           // band 1
+                    mma_pair<0>(d, A(1), B(0), idesc, false, false);
+                    mma_pair<0>(d, A(0), B(0), idesc, false, true);           // band 0
+                } else {
+                    if (!ready(0)) { ok = false; break; }
+                    mma_pair<1>(d, A(0), B(0), idesc, fresh, false);          // hi*hi
                 }
                 tc_commit_pair(empty0 + 8 * s);
                 if (close) {
@@ -475,14 +491,14 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     }
 }
 
-template <int TF32, int BN, int FUSED>
+template <int MODE, int BN, int FUSED>
 cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
                             const CUtensorMap& mapC, const TcGemmParams& p, int clusters,
                             cudaStream_t stream) {
-    using Cfg = KCfg<TF32, BN, FUSED>;
+    using Cfg = KCfg<MODE, BN, FUSED>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kblock_kernel<TF32, BN, FUSED>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kblock_kernel<MODE, BN, FUSED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::smem);
         if (e != cudaSuccess) return e;
         attr = true;
@@ -499,12 +515,12 @@ cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kblock_kernel<TF32, BN, FUSED>, mapA, mapB, mapC, p);
+    return cudaLaunchKernelEx(&cfg, gemm_kblock_kernel<MODE, BN, FUSED>, mapA, mapB, mapC, p);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_kblock(int tf32, int bn, int fused, const CUtensorMap& mapA,
+cudaError_t launch_gemm_kblock(int mode, int bn, int fused, const CUtensorMap& mapA,
                                const CUtensorMap& mapB, const CUtensorMap& mapC,
                                const TcGemmParams& p, int sms, cudaStream_t stream) {
     const int tiles = p.tiles_m * p.tiles_n;
@@ -512,14 +528,20 @@ cudaError_t launch_gemm_kblock(int tf32, int bn, int fused, const CUtensorMap& m
     const int clusters = tiles < sms / 2 ? tiles : sms / 2;
     cudaError_t e;
     if (fused) {
-        if (tf32 || bn != 128) return cudaErrorInvalidValue;
-        e = launch_kblock_t<0, 128, 1>(mapA, mapB, mapC, p, clusters, stream);
-    } else if (tf32) {
-        e = bn == 128 ? launch_kblock_t<1, 128, 0>(mapA, mapB, mapC, p, clusters, stream)
-                      : launch_kblock_t<1, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+        if (mode != kModeBf16x9 || bn != 128) return cudaErrorInvalidValue;
+        e = launch_kblock_t<kModeBf16x9, 128, 1>(mapA, mapB, mapC, p, clusters, stream);
+    } else if (mode == kModeTf32x3) {
+        e = bn == 128 ? launch_kblock_t<kModeTf32x3, 128, 0>(mapA, mapB, mapC, p, clusters, stream)
+                      : launch_kblock_t<kModeTf32x3, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+    } else if (mode == kModeBf16x9) {
+        e = bn == 128 ? launch_kblock_t<kModeBf16x9, 128, 0>(mapA, mapB, mapC, p, clusters, stream)
+                      : launch_kblock_t<kModeBf16x9, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+    } else if (mode == kModeBf16x3 && bn == 256) {
+        e = launch_kblock_t<kModeBf16x3, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+    } else if (mode == kModeTf32 && bn == 256) {
+        e = launch_kblock_t<kModeTf32, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
     } else {
-        e = bn == 128 ? launch_kblock_t<0, 128, 0>(mapA, mapB, mapC, p, clusters, stream)
-                      : launch_kblock_t<0, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+        return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

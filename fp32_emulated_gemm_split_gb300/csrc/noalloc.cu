@@ -126,8 +126,7 @@ extern "C" emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     // the same argument rules as emu_sgemm
     if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return EMU_ERR_INVALID_VALUE;
-    if (mode != EMU_MODE_BF16X9 && mode != EMU_MODE_TF32X3 && mode != EMU_MODE_FP32_SIMT)
-        return EMU_ERR_INVALID_VALUE;
+    if (!valid_mode(mode)) return EMU_ERR_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
         return EMU_ERR_INVALID_VALUE;
     if (lda < 1 || lda < (transA ? M : K) || ldb < 1 || ldb < (transB ? K : N) || ldc < 1 ||
@@ -136,8 +135,8 @@ extern "C" emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int
     if (M == 0 || N == 0) return EMU_OK;
     if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return EMU_ERR_INVALID_VALUE;
 
-    const bool tf32 = mode == EMU_MODE_TF32X3;
-    const int pieces = tf32 ? 2 : 3, es = tf32 ? 4 : 2;
+    const bool tf32 = mode_is_tf32(mode);
+    const int pieces = mode_pieces(mode), es = mode_piece_bytes(mode);
     const int64_t ldp = plane_ld(K);
     const size_t a_region = ((size_t)pieces * M * ldp * es + 1023) / 1024 * 1024;
     const size_t need = a_region + (size_t)pieces * N * ldp * es;
@@ -155,22 +154,8 @@ extern "C" emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int
 
     uint8_t* wa = static_cast<uint8_t*>(s->scratch);
     uint8_t* wb = wa + a_region;
-    cudaError_t e;
-    if (tf32) {
-        float* pa = reinterpret_cast<float*>(wa);
-        float* pb = reinterpret_cast<float*>(wb);
-        e = launch_split_tf32x2(A, M, K, lda, transA, pa, pa + M * ldp, ldp, stream);
-        if (e == cudaSuccess)
-            e = launch_split_tf32x2(B, N, K, ldb, !transB, pb, pb + N * ldp, ldp, stream);
-    } else {
-        uint16_t* pa = reinterpret_cast<uint16_t*>(wa);
-        uint16_t* pb = reinterpret_cast<uint16_t*>(wb);
-        e = launch_split_bf16x3(A, M, K, lda, transA, pa, pa + M * ldp, pa + 2 * M * ldp, ldp,
-                                stream);
-        if (e == cudaSuccess)
-            e = launch_split_bf16x3(B, N, K, ldb, !transB, pb, pb + N * ldp, pb + 2 * N * ldp, ldp,
-                                    stream);
-    }
+    cudaError_t e = launch_split_pieces(mode, A, M, K, lda, transA, wa, ldp, stream);
+    if (e == cudaSuccess) e = launch_split_pieces(mode, B, N, K, ldb, !transB, wb, ldp, stream);
     if (e != cudaSuccess) return status_of(e);
 
     const int box_k = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
@@ -186,5 +171,5 @@ extern "C" emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int
     p.tiles_n = (int)((N + 255) / 256);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     p.tma_store = 0;                         // C stored directly by the epilogue warps
-    return status_of(launch_gemm_kblock(tf32, 256, 0, mapA, mapB, mapB, p, s->sms, stream));
+    return status_of(launch_gemm_kblock(mode, 256, 0, mapA, mapB, mapB, p, s->sms, stream));
 }

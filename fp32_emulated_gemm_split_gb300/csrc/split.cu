@@ -7,7 +7,8 @@
 // NVIDIA blog post "Unlocking Tensor Core Performance for Machine Learning
 // Interatomic Potentials") and x = hi + lo (Figure 2 of that post).  These
 // kernels are bound by HBM bandwidth: BF16x9 reads 4 bytes and writes 6 bytes
-// per element, TF32x3 reads 4 and writes 8.
+// per element, TF32x3 reads 4 and writes 8.  A null last plane (P2, LO) skips
+// its writes: the two-piece BF16 and single-pass TF32 modes do not read it.
 #include "emu_device.cuh"
 
 namespace emu {
@@ -45,7 +46,7 @@ __global__ void __launch_bounds__(256) split3_rows_vec8(const float* __restrict_
         const int64_t o = r * ldp + c;
         *reinterpret_cast<uint4*>(P0 + o) = o0;
         *reinterpret_cast<uint4*>(P1 + o) = o1;
-        *reinterpret_cast<uint4*>(P2 + o) = o2;
+        if (P2) *reinterpret_cast<uint4*>(P2 + o) = o2;
     }
 }
 
@@ -63,7 +64,8 @@ __global__ void __launch_bounds__(256) split3_rows_scalar(const float* __restric
         uint16_t h0, h1, h2;
         split_bf16x3(X[r * ld + c], h0, h1, h2);
         const int64_t o = r * ldp + c;
-        P0[o] = h0; P1[o] = h1; P2[o] = h2;
+        P0[o] = h0; P1[o] = h1;
+        if (P2) P2[o] = h2;
     }
 }
 
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(256) split2_rows_vec4(const float* __restrict_
         split_tf32x2(a.z, h.z, l.z);
         split_tf32x2(a.w, h.w, l.w);
         *reinterpret_cast<float4*>(HI + r * ldp + c) = h;
-        *reinterpret_cast<float4*>(LO + r * ldp + c) = l;
+        if (LO) *reinterpret_cast<float4*>(LO + r * ldp + c) = l;
     }
 }
 
@@ -100,7 +102,7 @@ __global__ void __launch_bounds__(256) split2_rows_scalar(const float* __restric
         float h, l;
         split_tf32x2(X[r * ld + c], h, l);
         HI[r * ldp + c] = h;
-        LO[r * ldp + c] = l;
+        if (LO) LO[r * ldp + c] = l;
     }
 }
 
@@ -142,10 +144,10 @@ __global__ void __launch_bounds__(256) split3_transposed(const float* __restrict
         if (c + 1 < cols && (o & 1) == 0) {
             *reinterpret_cast<uint32_t*>(P0 + o) = a0 | (uint32_t(b0) << 16);
             *reinterpret_cast<uint32_t*>(P1 + o) = a1 | (uint32_t(b1) << 16);
-            *reinterpret_cast<uint32_t*>(P2 + o) = a2 | (uint32_t(b2) << 16);
+            if (P2) *reinterpret_cast<uint32_t*>(P2 + o) = a2 | (uint32_t(b2) << 16);
         } else {
-            if (c < cols) { P0[o] = a0; P1[o] = a1; P2[o] = a2; }
-            if (c + 1 < cols) { P0[o + 1] = b0; P1[o + 1] = b1; P2[o + 1] = b2; }
+            if (c < cols) { P0[o] = a0; P1[o] = a1; if (P2) P2[o] = a2; }
+            if (c + 1 < cols) { P0[o + 1] = b0; P1[o + 1] = b1; if (P2) P2[o + 1] = b2; }
         }
     }
 }
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(256) split3_transposed_vec(const float* __rest
                            h0[b + 4] | (uint32_t(h0[b + 5]) << 16), h0[b + 6] | (uint32_t(h0[b + 7]) << 16));
         d1[q] = make_uint4(h1[b] | (uint32_t(h1[b + 1]) << 16), h1[b + 2] | (uint32_t(h1[b + 3]) << 16),
                            h1[b + 4] | (uint32_t(h1[b + 5]) << 16), h1[b + 6] | (uint32_t(h1[b + 7]) << 16));
-        d2[q] = make_uint4(h2[b] | (uint32_t(h2[b + 1]) << 16), h2[b + 2] | (uint32_t(h2[b + 3]) << 16),
+        if (P2) d2[q] = make_uint4(h2[b] | (uint32_t(h2[b + 1]) << 16), h2[b + 2] | (uint32_t(h2[b + 3]) << 16),
                            h2[b + 4] | (uint32_t(h2[b + 5]) << 16), h2[b + 6] | (uint32_t(h2[b + 7]) << 16));
     }
 }
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(256) split2_transposed(const float* __restrict
                 float hi, lo;
                 split_tf32x2(tile[tx + 32 * h][j], hi, lo);
                 HI[r * ldp + c] = hi;
-                LO[r * ldp + c] = lo;
+                if (LO) LO[r * ldp + c] = lo;
             }
         }
     }
@@ -277,6 +279,19 @@ cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int6
                                                                           LO, ldp);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_split_pieces(int mode, const float* X, int64_t rows, int64_t cols, int64_t ld,
+                                int trans, void* planes, int64_t ldp, cudaStream_t stream) {
+    const int64_t n = rows * ldp;
+    if (mode_is_tf32(mode)) {
+        float* hi = static_cast<float*>(planes);
+        return launch_split_tf32x2(X, rows, cols, ld, trans, hi,
+                                   mode_pieces(mode) > 1 ? hi + n : nullptr, ldp, stream);
+    }
+    uint16_t* p0 = static_cast<uint16_t*>(planes);
+    return launch_split_bf16x3(X, rows, cols, ld, trans, p0, p0 + n,
+                               mode_pieces(mode) > 2 ? p0 + 2 * n : nullptr, ldp, stream);
 }
 
 }  // namespace emu

@@ -63,7 +63,12 @@ typedef enum {
     /* two TF32 pieces per operand, three products (residual*residual dropped) */
     EMU_MODE_TF32X3 = 1,
     /* plain FP32 FMA on the CUDA cores (the library's own baseline) */
-    EMU_MODE_FP32_SIMT = 2
+    EMU_MODE_FP32_SIMT = 2,
+    /* cheaper, less accurate rungs: two BF16 pieces per operand, three
+       products a0 b0, a0 b1, a1 b0 (about 2^-16 relative per product) */
+    EMU_MODE_BF16X3 = 3,
+    /* one TF32 piece per operand, one product (about 2^-10 per product) */
+    EMU_MODE_TF32 = 4
 } emu_mode_t;
 
 typedef enum {
@@ -104,14 +109,19 @@ typedef enum {
  * of K (16 MMAs) and each partial is added, times 2^-8b, to an FP32
  * accumulator with round-to-nearest.  TF32X3 (Figure 2): x = hi + lo (TF32,
  * nearest even, no scaling); the band hi*lo + lo*hi is accumulated first,
- * then hi*hi; lo*lo is dropped.  The epilogue is C = alpha*acc + beta*C in
+ * then hi*hi; lo*lo is dropped.  BF16X3 keeps the first two BF16 pieces
+ * and runs band 1 (a0 b1 + a1 b0) then band 0 (a0 b0), the way PyTorch's
+ * "high" matmul precision is described on the discuss.pytorch.kr page;
+ * TF32 runs hi*hi alone (one-pass TF32, Figures 5-8 of the blog post).
+ * Neither meets FP32 accuracy; they complete the accuracy ladder the pages
+ * compare BF16X9 with.  The epilogue is C = alpha*acc + beta*C in
  * FP32; C is not read when beta == 0, and A, B are not read when alpha == 0
  * or K == 0 (BLAS convention).  M == 0 or N == 0 is a no-op.
  *
  * Accuracy: for BF16X9 every element satisfies
  *     |C - C_exact| <= (2K + 2) 2^-24 |alpha| sum_k |a_mk||b_kn| + 2^-23 |beta C|
- * (TF32X3 adds 2^-20 |alpha| sum_k |a_mk||b_kn|), where C_exact is the result
- * in exact arithmetic.
+ * (TF32X3 adds 2^-20 |alpha| sum_k |a_mk||b_kn|, BF16X3 2^-16 and TF32
+ * 2^-10 + 2^-21), where C_exact is the result in exact arithmetic.
  *
  * Returns EMU_OK once the kernels are enqueued on `stream`.
  */
@@ -181,6 +191,7 @@ emu_status_t emu_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_
  * the same kernels, with one limit: the pieces must fit in the array,
  *     BF16X9:  3 * 2 * (M + N) * ldp  bytes  (plus < 1 KB of alignment),
  *     TF32X3:  2 * 4 * (M + N) * ldp  bytes,   ldp = K rounded up to 8,
+ *     BF16X3:  2 * 2 * (M + N) * ldp  bytes,   TF32: 1 * 4 * (M + N) * ldp,
  * at most 64 MiB; a larger request returns EMU_ERR_INVALID_VALUE and
  * launches nothing (FP32_SIMT and the K == 0 / alpha == 0 cases use no
  * scratch and have no limit).  The first call on a device, with that device

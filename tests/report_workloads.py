@@ -108,7 +108,7 @@ def main():
             mi, ni = W.sample_pairs(g0.M, g0.N, args.samples)
             Cref, Sabs = oracle.gemm_ref(A, B, g0.transA, g0.transB, g0.alpha, g0.beta, C0,
                                          pairs=(mi, ni))
-        modes = ["bf16x9", "bf16x9_fused", "tf32x3", "fp32_simt"]
+        modes = ["bf16x9", "bf16x9_fused", "tf32x3", "bf16x3", "tf32", "fp32_simt"]
         for mode_name in modes:
             mode = mode_name.replace("_fused", "")
             emu.emu_set_path("fused" if mode_name.endswith("_fused") else "twopass")
@@ -129,7 +129,7 @@ def main():
             else:
                 got = dC[torch.from_numpy(mi).cuda(), torch.from_numpy(ni).cuda()].cpu().numpy()
                 C0s = C0[mi, ni] if C0 is not None else None
-            bmode = "tf32x3" if mode == "tf32x3" else "bf16x9"
+            bmode = mode if mode in checks.MODE_EXTRA else "bf16x9"
             ratio = checks.error_ratio(got, Cref, Sabs, g0.K, g0.alpha, g0.beta, C0s, mode=bmode)
             relf = checks.rel_frobenius(got, Cref)
             reps = 10 if g0.flops < 2e12 else 5
