@@ -76,6 +76,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_split_bf16x3.restype = None
     L.oracle_split_tf32x2.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp]
     L.oracle_split_tf32x2.restype = None
+    L.oracle_split_tf32x2s.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp]
+    L.oracle_split_tf32x2s.restype = None
     L.oracle_split_bf16x3_vec.argtypes = [_vp, _i64, _vp, _vp, _vp]
     L.oracle_split_bf16x3_vec.restype = None
     L.oracle_split_tf32x2_vec.argtypes = [_vp, _i64, _vp, _vp]
@@ -90,7 +92,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_gemm_tf32x3.restype = None
     L.oracle_gemm_fp32.argtypes = gemm_args + [_vp]
     L.oracle_gemm_fp32.restype = None
-    for name in ("oracle_gemm_bf16x3", "oracle_gemm_tf32"):
+    for name in ("oracle_gemm_bf16x3", "oracle_gemm_tf32", "oracle_gemm_tf32x3_oy"):
         getattr(L, name).argtypes = gemm_args + [_vp]
         getattr(L, name).restype = None
     L.oracle_max_threads.argtypes = []
@@ -142,6 +144,16 @@ def split_tf32x2(X, trans: bool = False, L=None):
     hi = np.empty((rows, cols), np.float32)
     lo = np.empty((rows, cols), np.float32)
     (L or lib()).oracle_split_tf32x2(_ptr(X), rows, cols, ld, int(trans), _ptr(hi), _ptr(lo))
+    return hi, lo
+
+
+def split_tf32x2s(X, trans: bool = False, L=None):
+    """TF32 hi and 2^11-scaled lo planes of op(X) (the Ootomo-Yokota split)."""
+    X, ld = _mat(X)
+    rows, cols = (X.shape[1], X.shape[0]) if trans else X.shape
+    hi = np.empty((rows, cols), np.float32)
+    lo = np.empty((rows, cols), np.float32)
+    (L or lib()).oracle_split_tf32x2s(_ptr(X), rows, cols, ld, int(trans), _ptr(hi), _ptr(lo))
     return hi, lo
 
 
@@ -244,6 +256,12 @@ def gemm_fp32(A, B, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None, pa
 def gemm_bf16x3(A, B, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None, pairs=None, L=None):
     """Two BF16 pieces, three products (a0 b0, a0 b1, a1 b0), band 1 first."""
     return _plain("oracle_gemm_bf16x3", A, B, transA, transB, alpha, beta, C0, pairs, L)
+
+
+def gemm_tf32x3_oy(A, B, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None, pairs=None,
+                   L=None):
+    """TF32x3 with the 2^11-scaled residual (Ootomo-Yokota correction)."""
+    return _plain("oracle_gemm_tf32x3_oy", A, B, transA, transB, alpha, beta, C0, pairs, L)
 
 
 def gemm_tf32(A, B, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None, pairs=None, L=None):

@@ -34,7 +34,7 @@ FROBENIUS_TOL = 2e-6
 # miss at most about 2 * 2^-18 and the dropped 2^-16 a1 b1 adds at most about
 # 2^-18 more: below 2^-16 in all.  One TF32 piece leaves |x - hi| <= 2^-11 |x|,
 # so the product misses at most 2 * 2^-11 + 2^-22 < 2^-10 + 2^-21.
-MODE_EXTRA = {"bf16x9": 0.0, "tf32x3": 2.0 ** -20,
+MODE_EXTRA = {"bf16x9": 0.0, "tf32x3": 2.0 ** -20, "tf32x3_oy": 2.0 ** -20,
               "bf16x3": 2.0 ** -16, "tf32": 2.0 ** -10 + 2.0 ** -21}
 
 

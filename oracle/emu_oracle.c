@@ -32,6 +32,8 @@
  *      ascending i (i + j = band); TF32x3 adds the two residual products of
  *      every k first, then the leading products (smallest band first, as for
  *      BF16x9);
+ *  R15 (Ootomo-Yokota variant) the residual is scaled by 2^11 before its
+ *      TF32 rounding and the residual band is scaled back by 2^-11;
  *  R5  C = alpha*acc + beta*C0 in FP32: the product alpha*acc, the product
  *      beta*C0 and their sum are each rounded; C0 is not read when beta == 0
  *      and A, B are not read when alpha == 0 (BLAS convention).
@@ -126,6 +128,25 @@ static void split2_one(float x, float* hi, float* lo) {
     *lo = u2f(oracle_tf32_rne_bits(r));
 }
 
+/* The scaled residual of the Ootomo-Yokota correction (discuss.pytorch.kr
+ * page, section "Ampere의 TF32x3": the paper it links adds scaling and
+ * accumulates outside the tensor core).  Reading R15: hi as above, and the
+ * residual multiplied by 2^11 before it is rounded to TF32, so that it keeps
+ * its 11 bits where the unscaled residual would fall among FP32 subnormals.
+ * x - hi is exact and the power-of-two scaling is exact. */
+static void split2s_one(float x, float* hi, float* lo) {
+    uint32_t u = f2u(x);
+    if ((u & 0x7F800000u) == 0x7F800000u) {
+        if (u & 0x007FFFFFu) { *hi = *lo = u2f(0x7FC00000u); return; }
+        *hi = x; *lo = 0.0f;
+        return;
+    }
+    float h = u2f(oracle_tf32_rne_bits(x));
+    float r = ldexpf(x - h, 11);
+    *hi = h;
+    *lo = u2f(oracle_tf32_rne_bits(r));
+}
+
 /* Planes of op(X), rows x cols, written densely (row r at r*cols). */
 void oracle_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_t ld,
                          int trans, uint16_t* P0, uint16_t* P1, uint16_t* P2) {
@@ -142,6 +163,14 @@ void oracle_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld,
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < cols; ++c)
             split2_one(op_at(X, ld, trans, r, c), &HI[r * cols + c], &LO[r * cols + c]);
+}
+
+void oracle_split_tf32x2s(const float* X, int64_t rows, int64_t cols, int64_t ld,
+                          int trans, float* HI, float* LO) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            split2s_one(op_at(X, ld, trans, r, c), &HI[r * cols + c], &LO[r * cols + c]);
 }
 
 /* Single-threaded vector form, for callers that parallelise themselves. */
@@ -352,6 +381,46 @@ void oracle_gemm_bf16x3(int transA, int transB, int64_t M, int64_t N, int64_t K,
         }
         free(ap);
         free(bp);
+    }
+}
+
+/* Ootomo-Yokota style TF32x3 (R15): the residual band with scaled
+ * residuals, a_hi b_lo' then a_lo' b_hi for every k, each exact product
+ * scaled back by 2^-11 and added to the FP32 accumulator, then a_hi b_hi for
+ * every k; all additions are FP32 round-to-nearest (the accumulation happens
+ * outside the tensor core). */
+void oracle_gemm_tf32x3_oy(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                           float alpha, const float* A, int64_t lda,
+                           const float* B, int64_t ldb,
+                           float beta, const float* C0, int64_t ldc0,
+                           const int64_t* mi, const int64_t* ni, int64_t npairs, float* C) {
+    (void)M; (void)N;
+    #pragma omp parallel
+    {
+        int64_t kk = K > 0 ? K : 1;
+        float* ah = (float*)malloc(sizeof(float) * kk);
+        float* al = (float*)malloc(sizeof(float) * kk);
+        float* bh = (float*)malloc(sizeof(float) * kk);
+        float* bl = (float*)malloc(sizeof(float) * kk);
+        #pragma omp for schedule(dynamic, 16)
+        for (int64_t p = 0; p < npairs; ++p) {
+            int64_t m = mi[p], n = ni[p];
+            float acc = 0.0f;
+            if (alpha != 0.0f) {
+                for (int64_t k = 0; k < K; ++k) {
+                    split2s_one(op_at(A, lda, transA, m, k), &ah[k], &al[k]);
+                    split2s_one(op_at(B, ldb, transB, k, n), &bh[k], &bl[k]);
+                }
+                for (int64_t k = 0; k < K; ++k) {
+                    acc += ldexpf(ah[k] * bl[k], -11);
+                    acc += ldexpf(al[k] * bh[k], -11);
+                }
+                for (int64_t k = 0; k < K; ++k)
+                    acc += ah[k] * bh[k];
+            }
+            C[p] = epilogue(alpha, acc, beta, C0, ldc0, m, n);
+        }
+        free(ah); free(al); free(bh); free(bl);
     }
 }
 

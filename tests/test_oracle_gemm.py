@@ -413,3 +413,55 @@ def test_mutant_keeping_a1b1_in_bf16x3_fails_closed_form():
                 "oracle_bf16_to_f32(bp[kk + k]), -16);")
     x = np.array([[1 + 2.0 ** -8]], np.float32)
     assert float(oracle.gemm_bf16x3(x, x, L=L)[0, 0]) != 1 + 2.0 ** -7
+
+
+# --------------------------------------------------------------------------
+# The Ootomo-Yokota variant: residual scaled by 2^11 before its TF32 rounding
+# --------------------------------------------------------------------------
+
+def test_scaled_split_is_the_unscaled_split_times_2_11_in_the_normal_range():
+    x = W.normal(R(91), (64, 512))
+    hi, lo = oracle.split_tf32x2(x)
+    hs, ls = oracle.split_tf32x2s(x)
+    assert np.array_equal(hs, hi)
+    assert np.array_equal(ls, np.ldexp(lo, 11).astype(np.float32))
+
+
+def test_scaled_split_keeps_residual_bits_below_the_normal_range():
+    x = np.float32(2.0 ** -120 * (1 + 2.0 ** -12 + 2.0 ** -21 + 2.0 ** -23))
+    X = np.array([[x]], np.float32)
+    hs, ls = oracle.split_tf32x2s(X)
+    assert hs[0, 0] == np.float32(2.0 ** -120)
+    assert ls[0, 0] == np.float32(2.0 ** -121 * (1 + 2.0 ** -9))        # tie to even at 2^-11
+    hi, lo = oracle.split_tf32x2(X)
+    assert lo[0, 0] == np.float32(2.0 ** -132)                          # subnormal: bits lost
+    I = np.ones((1, 1), np.float32)
+    assert oracle.gemm_tf32x3_oy(I, X)[0, 0] == np.float32(2.0 ** -120 * (1 + 2.0 ** -12 + 2.0 ** -21))
+    assert oracle.gemm_tf32x3(I, X)[0, 0] == np.float32(2.0 ** -120 * (1 + 2.0 ** -12))
+
+
+def test_oy_equals_tf32x3_bitwise_on_normal_range_data():
+    # the scaling is exact there, so every product and sum is the same
+    r = R(92)
+    A = W.normal(r, (64, 300))
+    B = W.normal(r, (300, 48))
+    C0 = W.uniform(r, (64, 48))
+    assert np.array_equal(oracle.gemm_tf32x3_oy(A, B, alpha=1.5, beta=-0.5, C0=C0),
+                          oracle.gemm_tf32x3(A, B, alpha=1.5, beta=-0.5, C0=C0))
+
+
+def test_oy_within_bound_on_wide_exponent_data():
+    r = R(93)
+    A = W.stress(r, (96, 512))
+    B = W.stress(r, (512, 80))
+    Cref, Sabs = oracle.gemm_ref(A, B)
+    C = oracle.gemm_tf32x3_oy(A, B)
+    assert checks.error_ratio(C, Cref, Sabs, 512, 1.0, 0.0, mode="tf32x3_oy") <= 1.0
+
+
+def test_mutant_unscaled_residual_fails_oy_equality():
+    L = _mutant(r"float r = ldexpf\(x - h, 11\);", "float r = ldexpf(x - h, 10);")
+    r = R(94)
+    A = W.normal(r, (16, 64))
+    B = W.normal(r, (64, 16))
+    assert not np.array_equal(oracle.gemm_tf32x3_oy(A, B, L=L), oracle.gemm_tf32x3(A, B))
