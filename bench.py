@@ -11,7 +11,7 @@ Each operand is 256 MiB, larger than the 129 MB L2, so no flush is needed
 between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--mode bf16x9|tf32x3|bf16x3|tf32|fp32_simt] [--impl reference]
+                  [--mode bf16x9|tf32x3|tf32x3_oy|bf16x3|tf32|fp32_simt] [--impl reference]
 
 --impl reference times the CPU oracle (the plain reference implementation of
 the method) on the host cores, on a bounded block of rows of the same
@@ -208,8 +208,9 @@ def bench_gpu(args):
     else:
         dom_name, (n_dom, ms_dom) = "gemm_tc", prof["gemm_tc"]
     per_launch_ms = ms_dom / max(n_dom, 1)
-    products = {"bf16x9": 9, "tf32x3": 3, "bf16x3": 3, "tf32": 1, "fp32_simt": 1}[g.mode]
-    tf32_mode = g.mode in ("tf32x3", "tf32")
+    products = {"bf16x9": 9, "tf32x3": 3, "tf32x3_oy": 3, "bf16x3": 3, "tf32": 1,
+                "fp32_simt": 1}[g.mode]
+    tf32_mode = g.mode in ("tf32x3", "tf32x3_oy", "tf32")
     if g.mode == "fp32_simt":
         roofline = {"bound": "alu", "achieved": flops / (per_launch_ms * 1e-3) / 1e12,
                     "peak": None, "unit": "TFLOP/s", "frac": None, "traffic": None}
@@ -344,6 +345,7 @@ def bench_simt(emu, g, dA, dB, dC, stream):
 
 def ORACLE_FN(oracle):
     return {"bf16x9": oracle.gemm_bf16x9, "tf32x3": oracle.gemm_tf32x3,
+            "tf32x3_oy": oracle.gemm_tf32x3_oy,
             "bf16x3": oracle.gemm_bf16x3, "tf32": oracle.gemm_tf32,
             "fp32_simt": oracle.gemm_fp32}
 
@@ -430,7 +432,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="square8192_normal")
     ap.add_argument("--mode", default=None,
-                    choices=[None, "bf16x9", "tf32x3", "bf16x3", "tf32", "fp32_simt"])
+                    choices=[None, "bf16x9", "tf32x3", "tf32x3_oy", "bf16x3", "tf32", "fp32_simt"])
     ap.add_argument("--impl", default="emu", choices=["emu", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")

@@ -17,7 +17,7 @@ import os
 
 from . import _build
 
-MODE = {"bf16x9": 0, "tf32x3": 1, "fp32_simt": 2, "bf16x3": 3, "tf32": 4}
+MODE = {"bf16x9": 0, "tf32x3": 1, "fp32_simt": 2, "bf16x3": 3, "tf32": 4, "tf32x3_oy": 5}
 PATH = {"auto": 0, "twopass": 1, "fused": 2}
 PROFILE_KIND = {"split": 0, "gemm_tc": 1, "gemm_fused": 2, "gemm_simt": 3, "scale": 4}
 
@@ -59,6 +59,8 @@ def _declare(L):
     L.emu_split_bf16x3.restype = _int
     L.emu_split_tf32x2.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _i64, _vp]
     L.emu_split_tf32x2.restype = _int
+    L.emu_split_tf32x2_scaled.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _i64, _vp]
+    L.emu_split_tf32x2_scaled.restype = _int
     L.emu_set_path.argtypes = [_int]
     L.emu_set_path.restype = _int
     L.emu_get_path.argtypes = []
@@ -210,17 +212,19 @@ def emu_split_bf16x3(X, trans=False, ldp=None, stream=None):
     return tuple(P)
 
 
-def emu_split_tf32x2(X, trans=False, ldp=None, stream=None):
-    """TF32 hi / lo pieces of op(X) as float32 CUDA tensors (rows x ldp)."""
+def emu_split_tf32x2(X, trans=False, ldp=None, stream=None, scaled=False):
+    """TF32 hi / lo pieces of op(X) as float32 CUDA tensors (rows x ldp);
+    scaled=True gives the 2^11-scaled residual (emu_split_tf32x2_scaled)."""
     import torch
     Xs, t, ld = _stored(X, trans)
     rows, cols = (Xs.size(1), Xs.size(0)) if t else (Xs.size(0), Xs.size(1))
     ldp = cols if ldp is None else ldp
     hi = torch.zeros((rows, max(ldp, 1)), dtype=torch.float32, device=X.device)
     lo = torch.zeros_like(hi)
-    st = lib().emu_split_tf32x2(Xs.data_ptr(), rows, cols, ld, int(t), hi.data_ptr(),
-                                lo.data_ptr(), max(ldp, 1), _stream_handle(stream))
-    _check(st, "emu_split_tf32x2")
+    name = "emu_split_tf32x2_scaled" if scaled else "emu_split_tf32x2"
+    st = getattr(lib(), name)(Xs.data_ptr(), rows, cols, ld, int(t), hi.data_ptr(),
+                              lo.data_ptr(), max(ldp, 1), _stream_handle(stream))
+    _check(st, name)
     return hi, lo
 
 

@@ -210,18 +210,19 @@ __device__ __forceinline__ void mma_cta2(uint32_t d, uint64_t a, uint64_t b, uin
     }
 }
 
-// D = A*B + 2^-8 D (scale-input-d = 8).
-template <int TF32>
-__device__ __forceinline__ void mma_cta2_scaled8(uint32_t d, uint64_t a, uint64_t b,
-                                                 uint32_t idesc) {
+// D = A*B + 2^-SHIFT D (scale-input-d = SHIFT).
+template <int TF32, int SHIFT>
+__device__ __forceinline__ void mma_cta2_scaled(uint32_t d, uint64_t a, uint64_t b,
+                                                uint32_t idesc) {
+    static_assert(SHIFT >= 1 && SHIFT <= 15, "scale-input-d takes 0..15");
     if constexpr (TF32) {
         asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, 1, 0;\n"
-                     " tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p, 8;\n}\n"
-                     :: "r"(d), "l"(a), "l"(b), "r"(idesc) : "memory");
+                     " tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p, %4;\n}\n"
+                     :: "r"(d), "l"(a), "l"(b), "r"(idesc), "n"(SHIFT) : "memory");
     } else {
         asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, 1, 0;\n"
-                     " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p, 8;\n}\n"
-                     :: "r"(d), "l"(a), "l"(b), "r"(idesc) : "memory");
+                     " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p, %4;\n}\n"
+                     :: "r"(d), "l"(a), "l"(b), "r"(idesc), "n"(SHIFT) : "memory");
     }
 }
 
@@ -276,8 +277,10 @@ __device__ __forceinline__ uint32_t tf32_rn_bits(float x) {
     return ((r & 0x7F800000u) == 0x7F800000u) ? (u & 0xFFFFE000u) : r;
 }
 
-// x = hi + lo, both TF32, no scaling.
-__device__ __forceinline__ void split_tf32x2(float x, float& hi, float& lo) {
+// x = hi + lo / lo_scale, both TF32: lo_scale = 1 for TF32x3, 2^11 for the
+// Ootomo-Yokota variant (the residual is scaled before its rounding; the
+// scaling by a power of two is exact).
+__device__ __forceinline__ void split_tf32x2(float x, float& hi, float& lo, float lo_scale = 1.0f) {
     const uint32_t u = __float_as_uint(x);
     if ((u & 0x7F800000u) == 0x7F800000u) {
         const bool nan = (u & 0x007FFFFFu) != 0;
@@ -286,7 +289,7 @@ __device__ __forceinline__ void split_tf32x2(float x, float& hi, float& lo) {
         return;
     }
     hi = __uint_as_float(tf32_rn_bits(x));
-    lo = __uint_as_float(tf32_rn_bits(__fsub_rn(x, hi)));
+    lo = __uint_as_float(tf32_rn_bits(__fmul_rn(__fsub_rn(x, hi), lo_scale)));
 }
 
 }  // namespace emu

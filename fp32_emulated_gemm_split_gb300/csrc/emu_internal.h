@@ -22,9 +22,10 @@ enum : int {
     kModeFp32Simt = 2,   // no pieces: the CUDA-core FP32 kernel
     kModeBf16x3 = 3,     // 2 BF16 pieces, 3 products in 2 bands
     kModeTf32 = 4,       // 1 TF32 piece, 1 product
+    kModeTf32x3Oy = 5,   // 2 TF32 pieces (residual scaled by 2^11), 3 products
 };
-constexpr bool valid_mode(int m) { return m >= kModeBf16x9 && m <= kModeTf32; }
-constexpr bool mode_is_tf32(int m) { return m == kModeTf32x3 || m == kModeTf32; }
+constexpr bool valid_mode(int m) { return m >= kModeBf16x9 && m <= kModeTf32x3Oy; }
+constexpr bool mode_is_tf32(int m) { return m == kModeTf32x3 || m == kModeTf32 || m == kModeTf32x3Oy; }
 constexpr int mode_pieces(int m) { return m == kModeBf16x9 ? 3 : m == kModeTf32 ? 1 : 2; }
 
 // K extent of one staged piece tile in bytes: one 128-byte swizzled row
@@ -50,8 +51,10 @@ struct TcGemmParams {
 cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
                                 uint16_t* P0, uint16_t* P1, uint16_t* P2, int64_t ldp,
                                 cudaStream_t stream);
+// lo_scale: 1 (TF32x3) or 2^11 (the residual scaled before its rounding)
 cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
-                                float* HI, float* LO, int64_t ldp, cudaStream_t stream);
+                                float* HI, float* LO, int64_t ldp, cudaStream_t stream,
+                                float lo_scale = 1.0f);
 // The pieces a tensor-core mode reads, as consecutive planes of rows x ldp
 // elements (BF16 bits or TF32-valued FP32) starting at `planes`.
 cudaError_t launch_split_pieces(int mode, const float* X, int64_t rows, int64_t cols, int64_t ld,

@@ -17,7 +17,7 @@ __device__ int g_emu_error = 0;
 
 static_assert(kModeBf16x9 == EMU_MODE_BF16X9 && kModeTf32x3 == EMU_MODE_TF32X3 &&
                   kModeFp32Simt == EMU_MODE_FP32_SIMT && kModeBf16x3 == EMU_MODE_BF16X3 &&
-                  kModeTf32 == EMU_MODE_TF32,
+                  kModeTf32 == EMU_MODE_TF32 && kModeTf32x3Oy == EMU_MODE_TF32X3_OY,
               "kernel variants follow emu_mode_t");
 
 namespace {
@@ -447,6 +447,18 @@ emu_status_t emu_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_
     if (st != EMU_OK) return st;
     return from_cuda(launch_split_tf32x2(X, rows, cols, ld, trans, HI, LO, ldp,
                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+emu_status_t emu_split_tf32x2_scaled(const float* X, int64_t rows, int64_t cols, int64_t ld,
+                                     int trans, float* HI, float* LO, int64_t ldp,
+                                     emu_stream_t stream) {
+    emu_status_t st = check_split_args(X, rows, cols, ld, trans, HI, LO, LO, ldp);
+    if (st != EMU_OK || rows == 0 || cols == 0) return st;
+    DeviceState* d = nullptr;
+    st = current_device(&d);
+    if (st != EMU_OK) return st;
+    return from_cuda(launch_split_tf32x2(X, rows, cols, ld, trans, HI, LO, ldp,
+                                         reinterpret_cast<cudaStream_t>(stream), 2048.0f));
 }
 
 emu_status_t emu_set_path(int path) {

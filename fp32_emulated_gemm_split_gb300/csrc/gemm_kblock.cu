@@ -13,7 +13,10 @@
 // run on the same pipeline: two BF16 pieces (band 1 = a0 b1 + a1 b0, then
 // band 0 = a0 b0 after a 2^-8 shift; the discuss.pytorch.kr page's "FP32 as
 // the sum of two BF16") and single-pass TF32 (one product, the blog post's
-// one-pass TF32 of Figures 5-8).
+// one-pass TF32 of Figures 5-8).  The Ootomo-Yokota variant of TF32x3
+// (linked from the discuss.pytorch.kr page's TF32x3 section: scaling, and
+// accumulation outside the tensor core) stores the residual times 2^11 and
+// runs the residual band, then hi*hi with scale-input-d = 11.
 //
 // Schedule.  For each 64-element K block (32 for TF32x3) the pieces of A and
 // B are staged once, and the tensor core runs the bands of that block
@@ -94,6 +97,7 @@ struct KCfg {
     // block, because the 2^-8 shift at a band change would also shift a
     // previous block's finished sum.
     static constexpr int kb_per_partial = MODE == kModeTf32x3 ? 2 : MODE == kModeTf32 ? 8 : 1;
+    static_assert(MODE != kModeTf32x3Oy || kb_per_partial == 1, "the 2^-11 shift needs fresh partials");
     // TMEM partial buffers of BN columns each (all 512 columns): 2 at BN = 256,
     // 4 at BN = 128, so the tensor core can run further ahead of the epilogue.
     static constexpr int nbuf = 512 / BN;
@@ -121,8 +125,8 @@ __device__ __forceinline__ void tile_pos(int tile, int tiles_m, int tiles_n, int
 // The MMAs of one piece pair (i, j) for one K block: four K=16 (BF16) or
 // K=8 (TF32) steps inside the 128-byte swizzled rows.  `first` marks the
 // first MMA of a fresh accumulator; `shift` asks the first step to scale the
-// accumulator by 2^-8 (start of a new, larger band).
-template <int TF32>
+// accumulator by 2^-SHIFT (start of a new, larger band).
+template <int TF32, int SHIFT = 8>
 __device__ __forceinline__ void mma_pair(uint32_t d, uint32_t a_tile, uint32_t b_tile,
                                          uint32_t idesc, bool first, bool shift) {
     const uint64_t adesc = make_sw128_kmajor_desc(a_tile);
@@ -131,7 +135,7 @@ __device__ __forceinline__ void mma_pair(uint32_t d, uint32_t a_tile, uint32_t b
     for (int k = 0; k < 4; ++k) {
         const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
         if (k == 0 && shift)
-            mma_cta2_scaled8<TF32>(d, adesc + koff, bdesc + koff, idesc);
+            mma_cta2_scaled<TF32, SHIFT>(d, adesc + koff, bdesc + koff, idesc);
         else
             mma_cta2<TF32>(d, adesc + koff, bdesc + koff, idesc, (k == 0 && first) ? 0u : 1u);
     }
@@ -338,6 +342,11 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     mma_pair<0>(d, A(0), B(1), idesc, true, false);           // band 1
                     mma_pair<0>(d, A(1), B(0), idesc, false, false);
                     mma_pair<0>(d, A(0), B(0), idesc, false, true);           // band 0
+                } else if constexpr (MODE == kModeTf32x3Oy) {
+                    if (!ready(1) || !ready(0)) { ok = false; break; }
+                    mma_pair<1>(d, A(0), B(1), idesc, true, false);           // hi*lo'
+                    mma_pair<1>(d, A(1), B(0), idesc, false, false);          // lo'*hi
+                    mma_pair<1, 11>(d, A(0), B(0), idesc, false, true);       // hi*hi + 2^-11 D
                 } else {
                     if (!ready(0)) { ok = false; break; }
                     mma_pair<1>(d, A(0), B(0), idesc, fresh, false);          // hi*hi
@@ -540,6 +549,8 @@ cudaError_t launch_gemm_kblock(int mode, int bn, int fused, const CUtensorMap& m
         e = launch_kblock_t<kModeBf16x3, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
     } else if (mode == kModeTf32 && bn == 256) {
         e = launch_kblock_t<kModeTf32, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+    } else if (mode == kModeTf32x3Oy && bn == 256) {
+        e = launch_kblock_t<kModeTf32x3Oy, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
     } else {
         return cudaErrorInvalidValue;
     }

@@ -9,6 +9,8 @@
 // kernels are bound by HBM bandwidth: BF16x9 reads 4 bytes and writes 6 bytes
 // per element, TF32x3 reads 4 and writes 8.  A null last plane (P2, LO) skips
 // its writes: the two-piece BF16 and single-pass TF32 modes do not read it.
+// The Ootomo-Yokota variant scales the TF32 residual by 2^11 (lo_scale)
+// before rounding it.
 #include "emu_device.cuh"
 
 namespace emu {
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(256) split3_rows_scalar(const float* __restric
 __global__ void __launch_bounds__(256) split2_rows_vec4(const float* __restrict__ X, int64_t rows,
                                                         int64_t cols, int64_t ld,
                                                         float* __restrict__ HI,
-                                                        float* __restrict__ LO, int64_t ldp) {
+                                                        float* __restrict__ LO, int64_t ldp, float lo_scale) {
     const int64_t groups = cols / 4;
     const int64_t total = rows * groups;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
@@ -81,10 +83,10 @@ __global__ void __launch_bounds__(256) split2_rows_vec4(const float* __restrict_
         const int64_t c = (t - r * groups) * 4;
         const float4 a = __ldcs(reinterpret_cast<const float4*>(X + r * ld + c));
         float4 h, l;
-        split_tf32x2(a.x, h.x, l.x);
-        split_tf32x2(a.y, h.y, l.y);
-        split_tf32x2(a.z, h.z, l.z);
-        split_tf32x2(a.w, h.w, l.w);
+        split_tf32x2(a.x, h.x, l.x, lo_scale);
+        split_tf32x2(a.y, h.y, l.y, lo_scale);
+        split_tf32x2(a.z, h.z, l.z, lo_scale);
+        split_tf32x2(a.w, h.w, l.w, lo_scale);
         *reinterpret_cast<float4*>(HI + r * ldp + c) = h;
         if (LO) *reinterpret_cast<float4*>(LO + r * ldp + c) = l;
     }
@@ -93,14 +95,14 @@ __global__ void __launch_bounds__(256) split2_rows_vec4(const float* __restrict_
 __global__ void __launch_bounds__(256) split2_rows_scalar(const float* __restrict__ X, int64_t rows,
                                                           int64_t cols, int64_t ld,
                                                           float* __restrict__ HI,
-                                                          float* __restrict__ LO, int64_t ldp) {
+                                                          float* __restrict__ LO, int64_t ldp, float lo_scale) {
     const int64_t total = rows * cols;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
          t += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = t / cols;
         const int64_t c = t - r * cols;
         float h, l;
-        split_tf32x2(X[r * ld + c], h, l);
+        split_tf32x2(X[r * ld + c], h, l, lo_scale);
         HI[r * ldp + c] = h;
         if (LO) LO[r * ldp + c] = l;
     }
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(256) split3_transposed_vec(const float* __rest
 __global__ void __launch_bounds__(256) split2_transposed(const float* __restrict__ X, int64_t rows,
                                                          int64_t cols, int64_t ld,
                                                          float* __restrict__ HI,
-                                                         float* __restrict__ LO, int64_t ldp) {
+                                                         float* __restrict__ LO, int64_t ldp, float lo_scale) {
     __shared__ float tile[kT][kT + 1];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     const int64_t r0 = (int64_t)blockIdx.x * kT;
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(256) split2_transposed(const float* __restrict
             const int64_t c = c0 + tx + 32 * h;
             if (c < cols) {
                 float hi, lo;
-                split_tf32x2(tile[tx + 32 * h][j], hi, lo);
+                split_tf32x2(tile[tx + 32 * h][j], hi, lo, lo_scale);
                 HI[r * ldp + c] = hi;
                 if (LO) LO[r * ldp + c] = lo;
             }
@@ -265,18 +267,20 @@ cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int6
 }
 
 cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
-                                float* HI, float* LO, int64_t ldp, cudaStream_t stream) {
+                                float* HI, float* LO, int64_t ldp, cudaStream_t stream,
+                                float lo_scale) {
     if (rows == 0 || cols == 0) return cudaSuccess;
     if (trans) {
         dim3 grid((unsigned)((rows + kT - 1) / kT), (unsigned)((cols + kT - 1) / kT));
-        split2_transposed<<<grid, 256, 0, stream>>>(X, rows, cols, ld, HI, LO, ldp);
+        split2_transposed<<<grid, 256, 0, stream>>>(X, rows, cols, ld, HI, LO, ldp, lo_scale);
     } else if (cols % 4 == 0 && ld % 4 == 0 && ldp % 4 == 0 && aligned16(X) && aligned16(HI) &&
                aligned16(LO)) {
         split2_rows_vec4<<<grid_for(rows * (cols / 4), 256), 256, 0, stream>>>(X, rows, cols, ld,
-                                                                              HI, LO, ldp);
+                                                                              HI, LO, ldp,
+                                                                              lo_scale);
     } else {
         split2_rows_scalar<<<grid_for(rows * cols, 256), 256, 0, stream>>>(X, rows, cols, ld, HI,
-                                                                          LO, ldp);
+                                                                          LO, ldp, lo_scale);
     }
     return cudaGetLastError();
 }
@@ -287,7 +291,8 @@ cudaError_t launch_split_pieces(int mode, const float* X, int64_t rows, int64_t 
     if (mode_is_tf32(mode)) {
         float* hi = static_cast<float*>(planes);
         return launch_split_tf32x2(X, rows, cols, ld, trans, hi,
-                                   mode_pieces(mode) > 1 ? hi + n : nullptr, ldp, stream);
+                                   mode_pieces(mode) > 1 ? hi + n : nullptr, ldp, stream,
+                                   mode == kModeTf32x3Oy ? 2048.0f : 1.0f);
     }
     uint16_t* p0 = static_cast<uint16_t*>(planes);
     return launch_split_bf16x3(X, rows, cols, ld, trans, p0, p0 + n,

@@ -68,7 +68,10 @@ typedef enum {
        products a0 b0, a0 b1, a1 b0 (about 2^-16 relative per product) */
     EMU_MODE_BF16X3 = 3,
     /* one TF32 piece per operand, one product (about 2^-10 per product) */
-    EMU_MODE_TF32 = 4
+    EMU_MODE_TF32 = 4,
+    /* TF32X3 with the Ootomo-Yokota correction: the residual is scaled by
+       2^11 before its TF32 rounding and the residual band by 2^-11 */
+    EMU_MODE_TF32X3_OY = 5
 } emu_mode_t;
 
 typedef enum {
@@ -113,6 +116,13 @@ typedef enum {
  * and runs band 1 (a0 b1 + a1 b0) then band 0 (a0 b0), the way PyTorch's
  * "high" matmul precision is described on the discuss.pytorch.kr page;
  * TF32 runs hi*hi alone (one-pass TF32, Figures 5-8 of the blog post).
+ * TF32X3_OY is the variant of the Ootomo-Yokota paper that the
+ * discuss.pytorch.kr page's TF32x3 section links (scaling, accumulation
+ * outside the tensor core): lo' = tf32(2^11 (x - hi)), the residual band
+ * hi*lo' + lo'*hi first, then hi*hi with the band scaled by 2^-11, each
+ * 32-element K block's partial added to FP32 registers with round to
+ * nearest.  It equals TF32X3 wherever x - hi is a normal FP32 number and
+ * keeps 11 residual bits below that range.
  * Neither meets FP32 accuracy; they complete the accuracy ladder the pages
  * compare BF16X9 with.  The epilogue is C = alpha*acc + beta*C in
  * FP32; C is not read when beta == 0, and A, B are not read when alpha == 0
@@ -120,7 +130,7 @@ typedef enum {
  *
  * Accuracy: for BF16X9 every element satisfies
  *     |C - C_exact| <= (2K + 2) 2^-24 |alpha| sum_k |a_mk||b_kn| + 2^-23 |beta C|
- * (TF32X3 adds 2^-20 |alpha| sum_k |a_mk||b_kn|, BF16X3 2^-16 and TF32
+ * (TF32X3 and TF32X3_OY add 2^-20 |alpha| sum_k |a_mk||b_kn|, BF16X3 2^-16 and TF32
  * 2^-10 + 2^-21), where C_exact is the result in exact arithmetic.
  *
  * Returns EMU_OK once the kernels are enqueued on `stream`.
@@ -176,6 +186,16 @@ emu_status_t emu_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_
                               emu_stream_t stream);
 
 /*
+ * emu_split_tf32x2_scaled -- the split step of TF32X3_OY on its own: HI as
+ * in emu_split_tf32x2, LO the nearest TF32 of 2^11 (x - HI), so that
+ * op(X) ~ HI + 2^-11 LO.  Same layout, ownership and rules as
+ * emu_split_tf32x2.
+ */
+emu_status_t emu_split_tf32x2_scaled(const float* X, int64_t rows, int64_t cols, int64_t ld,
+                                     int trans, float* HI, float* LO, int64_t ldp,
+                                     emu_stream_t stream);
+
+/*
  * emu_sgemm_noalloc -- emu_sgemm that allocates no device memory.
  *
  * The pages have no counterpart: this entry point exists for callers of this
@@ -192,6 +212,7 @@ emu_status_t emu_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_
  *     BF16X9:  3 * 2 * (M + N) * ldp  bytes  (plus < 1 KB of alignment),
  *     TF32X3:  2 * 4 * (M + N) * ldp  bytes,   ldp = K rounded up to 8,
  *     BF16X3:  2 * 2 * (M + N) * ldp  bytes,   TF32: 1 * 4 * (M + N) * ldp,
+ *     TF32X3_OY: as TF32X3,
  * at most 64 MiB; a larger request returns EMU_ERR_INVALID_VALUE and
  * launches nothing (FP32_SIMT and the K == 0 / alpha == 0 cases use no
  * scratch and have no limit).  The first call on a device, with that device

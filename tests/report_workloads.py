@@ -108,7 +108,7 @@ def main():
             mi, ni = W.sample_pairs(g0.M, g0.N, args.samples)
             Cref, Sabs = oracle.gemm_ref(A, B, g0.transA, g0.transB, g0.alpha, g0.beta, C0,
                                          pairs=(mi, ni))
-        modes = ["bf16x9", "bf16x9_fused", "tf32x3", "bf16x3", "tf32", "fp32_simt"]
+        modes = ["bf16x9", "bf16x9_fused", "tf32x3", "tf32x3_oy", "bf16x3", "tf32", "fp32_simt"]
         for mode_name in modes:
             mode = mode_name.replace("_fused", "")
             emu.emu_set_path("fused" if mode_name.endswith("_fused") else "twopass")

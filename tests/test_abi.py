@@ -53,7 +53,7 @@ def _sgemm(L, transA=0, transB=0, M=4, N=4, K=4, lda=4, ldb=4, ldc=4, mode=0,
 
 
 @pytest.mark.parametrize("kw", [
-    dict(M=-1), dict(N=-2), dict(K=-1), dict(transA=2), dict(transB=-1), dict(mode=7), dict(mode=5), dict(mode=-1),
+    dict(M=-1), dict(N=-2), dict(K=-1), dict(transA=2), dict(transB=-1), dict(mode=7), dict(mode=6), dict(mode=-1),
     dict(lda=3), dict(ldb=3), dict(ldc=3), dict(transA=1, M=8, lda=4),
     dict(transB=1, K=8, ldb=4), dict(C=None), dict(A=None), dict(B=None),
     dict(M=1 << 31),
@@ -90,7 +90,8 @@ def test_path_selection_and_workspace_size(emu):
     # the cheaper rungs: two BF16 pieces, one TF32 piece
     assert emu.emu_workspace_size(100, 60, 13, "bf16x3") == (2 * 16 * 2 * 100 + 1023) // 1024 * 1024 + 2 * 16 * 2 * 60
     assert emu.emu_workspace_size(100, 60, 13, "tf32") == (1 * 16 * 4 * 100 + 1023) // 1024 * 1024 + 1 * 16 * 4 * 60
-    assert emu.lib().emu_workspace_size(100, 60, 13, 5) == 0
+    assert emu.emu_workspace_size(100, 60, 13, "tf32x3_oy") == emu.emu_workspace_size(100, 60, 13, "tf32x3")
+    assert emu.lib().emu_workspace_size(100, 60, 13, 6) == 0
     assert emu.emu_workspace_size(100, 60, 13, "fp32_simt") == 0
     assert emu.emu_workspace_size(0, 60, 13, "bf16x9") == 0
 

@@ -1,10 +1,11 @@
 """GPU parity of the two cheaper rungs of the accuracy ladder -- two BF16
-pieces with three products (BF16x3) and single-pass TF32 -- against the CPU
+pieces with three products (BF16x3) and single-pass TF32 -- and of the
+Ootomo-Yokota variant of TF32x3 (residual scaled by 2^11) against the CPU
 oracle.
 
 Two criteria per result: the element-wise bound against the FP64 reference,
 with the rung's own representation term (2^-16 |alpha| S_abs for BF16x3,
-2^-10 + 2^-21 for TF32), and closeness to the oracle's emulation of the same
+2^-10 + 2^-21 for TF32, 2^-20 for the Ootomo-Yokota TF32x3), and closeness to the oracle's emulation of the same
 rung, which keeps the same products: the two differ only in summation order,
 so |C_gpu - C_oracle| <= 2 (2K + 2) 2^-24 |alpha| S_abs + 2^-22 |beta C0|.
 The second catches a wrong piece or a wrong product that the looser first
@@ -19,7 +20,8 @@ from gpu_util import emu_module, to_dev
 
 pytestmark = pytest.mark.gpu
 
-RUNGS = {"bf16x3": oracle.gemm_bf16x3, "tf32": oracle.gemm_tf32}
+RUNGS = {"bf16x3": oracle.gemm_bf16x3, "tf32": oracle.gemm_tf32,
+         "tf32x3_oy": oracle.gemm_tf32x3_oy}
 
 
 @pytest.fixture(scope="module")
@@ -79,11 +81,12 @@ def test_ladder_order_on_mlip192(emu):
     A, B, C0 = W.generate(g)
     Cref, Sabs = oracle.gemm_ref(A, B)
     err = {m: checks.rel_frobenius(_run(emu, A, B, mode=m), Cref)
-           for m in ("bf16x9", "tf32x3", "bf16x3", "tf32")}
+           for m in ("bf16x9", "tf32x3", "tf32x3_oy", "bf16x3", "tf32")}
     assert err["bf16x9"] <= checks.FROBENIUS_TOL and err["tf32x3"] <= checks.FROBENIUS_TOL
+    assert err["tf32x3_oy"] <= checks.FROBENIUS_TOL
     assert err["tf32"] > err["bf16x3"] > 5 * max(err["bf16x9"], err["tf32x3"])
     mi, ni = W.sample_pairs(g.M, g.N, 4096, seed=6)
-    for m in ("bf16x3", "tf32"):
+    for m in ("bf16x3", "tf32", "tf32x3_oy"):
         C = _run(emu, A, B, mode=m)[mi, ni]
         Cemu = RUNGS[m](A, B, pairs=(mi, ni))
         assert _same_rung_ratio(C, Cemu, Sabs[mi, ni], g.K, 1.0, 0.0, None) <= 1.0
@@ -117,3 +120,16 @@ def test_noalloc_entry_takes_the_rungs(emu):
 
 def test_no_device_error_after_the_rungs(emu):
     assert emu.emu_get_last_device_error() == 0
+
+
+def test_oy_on_wide_exponent_data_every_element(emu):
+    """Values from 2^-30 to 2^30, zeros and subnormals (the stress recipe)."""
+    r = W.rng(73)
+    A = W.stress(r, (300, 700))
+    B = W.stress(r, (700, 260))
+    C0 = W.uniform(r, (300, 260))
+    C = _run(emu, A, B, alpha=1.5, beta=0.5, C0=C0, mode="tf32x3_oy")
+    Cref, Sabs = oracle.gemm_ref(A, B, alpha=1.5, beta=0.5, C0=C0)
+    assert checks.error_ratio(C, Cref, Sabs, 700, 1.5, 0.5, C0, mode="tf32x3_oy") <= 1.0
+    Cemu = oracle.gemm_tf32x3_oy(A, B, alpha=1.5, beta=0.5, C0=C0)
+    assert _same_rung_ratio(C, Cemu, Sabs, 700, 1.5, 0.5, C0) <= 1.0

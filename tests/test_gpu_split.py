@@ -42,6 +42,24 @@ def _check_tf32(emu, X, trans=False, ldp=None, cols_slice=None):
     assert np.array_equal(lo.cpu().numpy()[:, :cols].view(np.uint32), l.view(np.uint32))
 
 
+def _check_tf32_scaled(emu, X, trans=False):
+    hi, lo = emu.emu_split_tf32x2(to_dev(X), trans=trans, scaled=True)
+    h, l = oracle.split_tf32x2s(X, trans=trans)
+    cols = h.shape[1]
+    assert np.array_equal(hi.cpu().numpy()[:, :cols].view(np.uint32), h.view(np.uint32))
+    assert np.array_equal(lo.cpu().numpy()[:, :cols].view(np.uint32), l.view(np.uint32))
+
+
+def test_tf32x2_scaled_residual_bit_patterns(emu):
+    """The Ootomo-Yokota split: residual times 2^11 before its rounding."""
+    x = stratified_patterns()
+    _check_tf32_scaled(emu, x.reshape(-1, 4096))
+    X = stratified_patterns(low_per_high=8, n_random=0)[: 1 << 19].reshape(512, 1024)
+    _check_tf32_scaled(emu, X, trans=True)
+    _check_tf32_scaled(emu, W.stress(W.rng(8), (37, 53)), trans=True)
+    _check_tf32_scaled(emu, W.stress(W.rng(9), (37, 53)))
+
+
 def test_bf16x3_stratified_bit_patterns(emu):
     x = stratified_patterns()
     _check_bf16(emu, x.reshape(-1, 4096))            # vectorised row path
