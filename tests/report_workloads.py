@@ -19,6 +19,7 @@ import json
 import os
 import subprocess
 import sys
+import time
 
 import numpy as np
 
@@ -80,12 +81,41 @@ print(json.dumps({{"ms": float(np.median(ts))}}))
     return json.loads(r.stdout.strip().splitlines()[-1])["ms"]
 
 
+def cpu_oracle_time(g, A, B, C0, seconds):
+    """The oracle's BF16x9 (plain C, OpenMP over the host cores) on whole rows
+    of C: one row to calibrate, then a block of rows sized to `seconds`;
+    the whole GEMM's time is extrapolated linearly in rows."""
+    import numpy as np
+
+    def rows(r):
+        mi = np.repeat(np.arange(r, dtype=np.int64), g.N)
+        ni = np.tile(np.arange(g.N, dtype=np.int64), r)
+        t = time.perf_counter()
+        oracle.gemm_bf16x9(A, B, g.transA, g.transB, g.alpha, g.beta, C0, pairs=(mi, ni))
+        return time.perf_counter() - t
+
+    r, t = 1, rows(1)
+    for _ in range(3):          # thread start-up makes one row a poor guess
+        if t >= seconds / 2 or r >= g.M:
+            break
+        r = int(max(1, min(g.M, r * seconds / max(t, 1e-6))))
+        t = rows(r)
+    full = t * g.M / r
+    return {"workload": g.name, "mode": "cpu_oracle_bf16x9", "rows_timed": r,
+            "seconds_timed": round(t, 3), "seconds_full": round(full, 3),
+            "extrapolated": r < g.M, "threads": oracle.max_threads(),
+            "tflops": round(g.flops / full / 1e12, 7)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workloads", default=",".join(n for n in W.WORKLOADS if not n.endswith("_tf32x3")))
     ap.add_argument("--out", default=None)
     ap.add_argument("--no-cublas", action="store_true")
     ap.add_argument("--samples", type=int, default=4096)
+    ap.add_argument("--cpu-seconds", type=float, default=0.0,
+                    help="also time the CPU oracle's BF16x9 on a block of rows of about "
+                         "this many seconds per workload and extrapolate to the whole GEMM")
     args = ap.parse_args()
 
     import torch
@@ -153,6 +183,11 @@ def main():
                 print(json.dumps(rec), flush=True)
                 if out:
                     out.write(json.dumps(rec) + "\n")
+        if args.cpu_seconds > 0:
+            rec = cpu_oracle_time(g0, A, B, C0, args.cpu_seconds)
+            print(json.dumps(rec), flush=True)
+            if out:
+                out.write(json.dumps(rec) + "\n")
         del dA, dB
         torch.cuda.empty_cache()
     assert emu.emu_get_last_device_error() == 0
