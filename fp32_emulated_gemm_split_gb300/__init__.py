@@ -59,6 +59,14 @@ def _declare(L):
     L.emu_split_bf16x3.restype = _int
     L.emu_split_tf32x2.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _i64, _vp]
     L.emu_split_tf32x2.restype = _int
+    L.emu_set_strategy.argtypes = [_int]
+    L.emu_set_strategy.restype = _int
+    L.emu_get_strategy.argtypes = []
+    L.emu_get_strategy.restype = _int
+    L.emu_choose_mode.argtypes = [_i64, _i64, _i64, _int, _int, _int]
+    L.emu_choose_mode.restype = _int
+    L.emu_predict_us.argtypes = [_i64, _i64, _i64, _int, _int]
+    L.emu_predict_us.restype = ctypes.c_double
     L.emu_split_tf32x2_scaled.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _i64, _vp]
     L.emu_split_tf32x2_scaled.restype = _int
     L.emu_set_path.argtypes = [_int]
@@ -232,6 +240,33 @@ def emu_split_tf32x2(X, trans=False, ldp=None, stream=None, scaled=False):
 
 def emu_set_path(path) -> None:
     _check(lib().emu_set_path(PATH[path] if isinstance(path, str) else int(path)), "emu_set_path")
+
+
+STRATEGY = {"eager": 0, "performant": 1}
+
+
+def emu_set_strategy(strategy) -> None:
+    """'eager' (every call runs the mode it asks for) or 'performant' (the FP32
+    SIMT kernel where it is predicted faster than the emulation)."""
+    v = STRATEGY[strategy] if isinstance(strategy, str) else int(strategy)
+    _check(lib().emu_set_strategy(v), "emu_set_strategy")
+
+
+def emu_get_strategy() -> str:
+    return {0: "eager", 1: "performant"}[lib().emu_get_strategy()]
+
+
+def emu_choose_mode(M, N, K, mode="bf16x9", strategy=None, sms=0) -> str:
+    """The mode emu_sgemm would run for this shape (sms 0: the current GPU's)."""
+    st = -1 if strategy is None else (STRATEGY[strategy] if isinstance(strategy, str) else int(strategy))
+    v = lib().emu_choose_mode(M, N, K, _mode(mode), st, sms)
+    if v < 0:
+        raise EmuError(-1, "emu_choose_mode")
+    return {m: n for n, m in MODE.items()}[v]
+
+
+def emu_predict_us(M, N, K, mode="bf16x9", sms=152) -> float:
+    return float(lib().emu_predict_us(M, N, K, _mode(mode), sms))
 
 
 def emu_get_path() -> str:

@@ -74,6 +74,13 @@ cudaError_t launch_scale(int64_t M, int64_t N, float beta, float* C, int64_t ldc
                          cudaStream_t stream);
 cudaError_t launch_timeout_probe(int* err, uint64_t limit_ns, cudaStream_t stream);
 
+// PERFORMANT strategy (chooser.cu): the mode that runs for a requested mode
+// (the FP32 SIMT kernel where it is predicted faster), and the two time
+// estimates in microseconds; sms is the device's SM count.
+int choose_mode(int64_t M, int64_t N, int64_t K, int mode, int performant, int sms);
+double predict_tc_us(int64_t M, int64_t N, int64_t K, int mode, int sms);
+double predict_simt_us(int64_t M, int64_t N, int64_t K, int sms);
+
 // Device address of the sticky error word of the current device.
 int* device_error_word();
 

@@ -37,6 +37,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_path = -1;               // -1: not yet read from the environment
+int g_strategy = -1;           // same
 
 // ------------------------------------------------------------ profiling --
 struct ProfRecord { int kind; cudaEvent_t start, stop; };
@@ -100,6 +101,12 @@ int kblock_bn() {
         v = (s && std::strcmp(s, "128") == 0) ? 128 : 256;
     }
     return v;
+}
+
+int read_strategy_env() {
+    const char* s = std::getenv("EMU_SGEMM_STRATEGY");
+    if (s && !std::strcmp(s, "performant")) return EMU_STRATEGY_PERFORMANT;
+    return EMU_STRATEGY_EAGER;
 }
 
 int read_path_env() {
@@ -336,6 +343,9 @@ emu_status_t sgemm_device(int transA, int transB, int64_t M, int64_t N, int64_t 
         ProfScope ps(4, stream);
         return from_cuda(launch_scale(M, N, beta, C, ldc, stream));
     }
+    if (g_strategy < 0) g_strategy = read_strategy_env();
+    // PERFORMANT: the plain FP32 kernel where it is predicted faster
+    mode = choose_mode(M, N, K, mode, g_strategy == EMU_STRATEGY_PERFORMANT, d->sms);
     if (mode == EMU_MODE_FP32_SIMT) {
         ProfScope ps(3, stream);
         return from_cuda(launch_gemm_simt(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
@@ -473,6 +483,38 @@ int emu_get_path(void) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_path < 0) g_path = read_path_env();
     return g_path;
+}
+
+emu_status_t emu_set_strategy(int strategy) {
+    if (strategy != EMU_STRATEGY_EAGER && strategy != EMU_STRATEGY_PERFORMANT)
+        return EMU_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_strategy = strategy;
+    return EMU_OK;
+}
+
+int emu_get_strategy(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_strategy < 0) g_strategy = read_strategy_env();
+    return g_strategy;
+}
+
+int emu_choose_mode(int64_t M, int64_t N, int64_t K, int mode, int strategy, int sms) {
+    if (!valid_mode(mode) || M < 0 || N < 0 || K < 0) return -1;
+    if (strategy < 0) strategy = emu_get_strategy();
+    if (strategy != EMU_STRATEGY_EAGER && strategy != EMU_STRATEGY_PERFORMANT) return -1;
+    if (sms <= 0) {
+        DeviceState* d = nullptr;
+        if (current_device(&d) != EMU_OK) return -1;
+        sms = d->sms;
+    }
+    return choose_mode(M, N, K, mode, strategy == EMU_STRATEGY_PERFORMANT, sms);
+}
+
+double emu_predict_us(int64_t M, int64_t N, int64_t K, int mode, int sms) {
+    if (!valid_mode(mode) || M < 0 || N < 0 || K < 0 || sms <= 0) return -1.0;
+    return mode == EMU_MODE_FP32_SIMT ? predict_simt_us(M, N, K, sms)
+                                      : predict_tc_us(M, N, K, mode, sms);
 }
 
 size_t emu_workspace_size(int64_t M, int64_t N, int64_t K, int mode) {

@@ -93,11 +93,16 @@ struct KCfg {
     // K blocks summed in one TMEM partial before it is added to the registers.
     // TF32x3 has no band shift, so two short blocks (12 MMAs each) share a
     // partial, and single-pass TF32 eight blocks (32 MMAs; its 2^-11 piece
-    // error dwarfs the tensor core's truncation).  A BF16 partial holds one
+    // error dwarfs the tensor core's truncation).  A BF16x9 partial holds one
     // block, because the 2^-8 shift at a band change would also shift a
-    // previous block's finished sum.
-    static constexpr int kb_per_partial = MODE == kModeTf32x3 ? 2 : MODE == kModeTf32 ? 8 : 1;
-    static_assert(MODE != kModeTf32x3Oy || kb_per_partial == 1, "the 2^-11 shift needs fresh partials");
+    // previous block's finished sum.  The two-band modes (BF16x3 and the
+    // Ootomo-Yokota TF32x3) run two blocks band-major instead: band 1 of
+    // both, then band 0 of both, the shift at the first band-0 MMA, so both
+    // stages stay held until band 0 (band_major below).
+    static constexpr bool band_major = MODE == kModeBf16x3 || MODE == kModeTf32x3Oy;
+    static constexpr int band_shift = MODE == kModeTf32x3Oy ? 11 : 8;
+    static constexpr int kb_per_partial =
+        MODE == kModeTf32x3 || band_major ? 2 : MODE == kModeTf32 ? 8 : 1;
     // TMEM partial buffers of BN columns each (all 512 columns): 2 at BN = 256,
     // 4 at BN = 128, so the tensor core can run further ahead of the epilogue.
     static constexpr int nbuf = 512 / BN;
@@ -294,6 +299,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         const uint32_t idesc = make_idesc(Cfg::tf32 ? 2u : 1u, kBM, BN);
         constexpr int KBP = Cfg::kb_per_partial;
         uint32_t kbg = 0, part = 0;              // K blocks and TMEM partials so far
+        uint32_t prev_s = 0;                     // band-major: stage of the pair's first block
         bool ok = true;
         for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
             for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
@@ -337,16 +343,26 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     mma_pair<1>(d, A(0), B(1), idesc, fresh, false);          // hi*lo
                     mma_pair<1>(d, A(1), B(0), idesc, false, false);          // lo*hi
                     mma_pair<1>(d, A(0), B(0), idesc, false, false);          // hi*hi
-                } else if constexpr (MODE == kModeBf16x3) {
+                } else if constexpr (Cfg::band_major) {
+                    // BF16x3: band 1 = a0 b1 + a1 b0, band 0 = a0 b0, shift 2^-8.
+                    // Ootomo-Yokota: hi lo' + lo' hi, then hi hi, shift 2^-11.
+                    constexpr int T = Cfg::tf32 ? 1 : 0, SH = Cfg::band_shift;
                     if (!ready(1) || !ready(0)) { ok = false; break; }
-                    mma_pair<0>(d, A(0), B(1), idesc, true, false);           // band 1
-                    mma_pair<0>(d, A(1), B(0), idesc, false, false);
-                    mma_pair<0>(d, A(0), B(0), idesc, false, true);           // band 0
-                } else if constexpr (MODE == kModeTf32x3Oy) {
-                    if (!ready(1) || !ready(0)) { ok = false; break; }
-                    mma_pair<1>(d, A(0), B(1), idesc, true, false);           // hi*lo'
-                    mma_pair<1>(d, A(1), B(0), idesc, false, false);          // lo'*hi
-                    mma_pair<1, 11>(d, A(0), B(0), idesc, false, true);       // hi*hi + 2^-11 D
+                    mma_pair<T>(d, A(0), B(1), idesc, fresh, false);          // band 1
+                    mma_pair<T>(d, A(1), B(0), idesc, false, false);
+                    if (!close) {
+                        prev_s = s;                  // band 0 after the next block's band 1
+                        continue;                    // stage held: no empty commit yet
+                    }
+                    if (!fresh) {
+                        // band 0 of the pair's first block (shift), free its stage
+                        const uint32_t pst = smem_u32(smem + prev_s * Cfg::stage_bytes);
+                        mma_pair<T, SH>(d, pst, pst + P * kATile, idesc, false, true);
+                        tc_commit_pair(empty0 + 8 * prev_s);
+                        mma_pair<T>(d, A(0), B(0), idesc, false, false);
+                    } else {
+                        mma_pair<T, SH>(d, A(0), B(0), idesc, false, true);
+                    }
                 } else {
                     if (!ready(0)) { ok = false; break; }
                     mma_pair<1>(d, A(0), B(0), idesc, fresh, false);          // hi*hi

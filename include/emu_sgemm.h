@@ -236,6 +236,36 @@ emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int64_t N, int
 emu_status_t emu_set_path(int path);
 int emu_get_path(void);
 
+/* Whether an emulated mode always runs as asked.  The discuss.pytorch.kr
+ * page (section "PyTorch에서 직접 써 보려면") and the blog post's MD-step
+ * results contrast cuBLAS's two strategies for its BF16x9: "eager" uses the
+ * emulation wherever it applies, "performant" only where it is expected to be
+ * faster than native FP32.  This library's strategies: */
+typedef enum {
+    EMU_STRATEGY_EAGER = 0,       /* every call runs the mode it asks for (default) */
+    EMU_STRATEGY_PERFORMANT = 1   /* a call in a tensor-core mode runs the FP32 SIMT
+                                     kernel instead where that is predicted faster */
+} emu_strategy_t;
+
+/* Select the strategy of later emu_sgemm / emu_sgemm_host calls in this
+ * process (EMU_STRATEGY_EAGER by default; EMU_SGEMM_STRATEGY=performant sets
+ * the initial value).  emu_sgemm_noalloc always runs the mode it is given.
+ * Under PERFORMANT a result meets the FP32 SIMT kernel's accuracy (the
+ * BF16X9 bound) where the kernel is swapped.  Returns EMU_ERR_INVALID_VALUE
+ * for another value.  Not thread-safe with respect to concurrent calls. */
+emu_status_t emu_set_strategy(int strategy);
+int emu_get_strategy(void);
+
+/* The mode emu_sgemm would run for an M x N x K request in `mode` under
+ * `strategy` (-1: the current one) on a GPU with `sms` SMs (<= 0: the
+ * current device's, which needs a device).  A pure host function; -1 for
+ * invalid arguments.  The choice compares two time estimates of this
+ * library's kernels, fitted to measurements on GB300: */
+int emu_choose_mode(int64_t M, int64_t N, int64_t K, int mode, int strategy, int sms);
+/* ... the estimated device time of one call in microseconds (-1 on invalid
+ * arguments; sms must be > 0). */
+double emu_predict_us(int64_t M, int64_t N, int64_t K, int mode, int sms);
+
 /* Bytes of workspace the two-pass path needs for one call of this shape. */
 size_t emu_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
 
