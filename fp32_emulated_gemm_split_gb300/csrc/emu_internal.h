@@ -44,7 +44,7 @@ struct TcGemmParams {
     float alpha, beta;
     float* C;
     int64_t ldc;
-    int tma_store;       // 1: beta == 0 and the C tensor map is valid (bulk tensor stores)
+    int tma_store;       // 1: the C tensor map is valid (bulk tensor stores of C)
 };
 
 // Launchers (return the launch status; nothing is synchronised).

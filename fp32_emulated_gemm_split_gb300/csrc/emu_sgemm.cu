@@ -199,11 +199,12 @@ emu_status_t make_plane_map(CUtensorMap* map, const void* base, bool fp32, int64
     return r == CUDA_SUCCESS ? EMU_OK : EMU_ERR_CUDA;
 }
 
-// 2-D map over C for the bulk tensor stores of the GEMM epilogue (beta == 0):
-// box of 16 columns x 32 rows, 64-byte swizzle.  Returns false (and the
+// 2-D map over C for the bulk tensor stores of the GEMM epilogue (any beta;
+// with beta != 0 the epilogue reads C itself first): box of 16 columns x 32
+// rows, 64-byte swizzle.  Returns false (and the
 // kernel stores C directly) when C's rows are not 16-byte aligned.
-bool make_c_map(CUtensorMap* map, float* C, int64_t M, int64_t N, int64_t ldc, float beta) {
-    if (beta != 0.0f || (ldc % 4) != 0 || (reinterpret_cast<uintptr_t>(C) & 15) != 0) return false;
+bool make_c_map(CUtensorMap* map, float* C, int64_t M, int64_t N, int64_t ldc) {
+    if ((ldc % 4) != 0 || (reinterpret_cast<uintptr_t>(C) & 15) != 0) return false;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
@@ -277,7 +278,7 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
     p.tiles_n = (int)((N + bn - 1) / bn);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     CUtensorMap mapC = mapB;                 // placeholder when C is stored directly
-    p.tma_store = make_c_map(&mapC, C, M, N, ldc, beta) ? 1 : 0;
+    p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
     {
         ProfScope ps(1, stream);
         e = launch_gemm_kblock(mode, bn, 0, mapA, mapB, mapC, p, d->sms, stream);
@@ -322,7 +323,7 @@ emu_status_t run_fused(int transB, int64_t M, int64_t N, int64_t K, float alpha,
     p.tiles_n = (int)((N + bn - 1) / bn);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     CUtensorMap mapC = mapB;
-    p.tma_store = make_c_map(&mapC, C, M, N, ldc, beta) ? 1 : 0;
+    p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
     {
         ProfScope ps(2, stream);
         e = launch_gemm_kblock(0, bn, 1, mapA, mapB, mapC, p, d->sms, stream);

@@ -442,10 +442,11 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             const int row = row0 + lane;
             const int col_base = tn * BN + h * kAccCols;
             if (p.tma_store) {
-                // beta == 0: stage 32 rows x 16 columns at a time in this
-                // warp's 2 KB buffer (64-byte swizzle: conflict-free writes)
-                // and let one bulk tensor store write them, coalesced and
-                // clipped at the matrix edge.
+                // Stage 32 rows x 16 columns at a time in this warp's 2 KB
+                // buffer (64-byte swizzle: conflict-free writes) and let one
+                // bulk tensor store write them, coalesced and clipped at the
+                // matrix edge.  With beta != 0 each lane first reads its own
+                // row's 16 values of C (16-byte loads where they fit).
                 const uint32_t cst = smem_u32(cstage + (warp - 2) * 2048);
                 if (row0 < p.M) {
 #pragma unroll
@@ -456,10 +457,26 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             const int j = 16 * ch + 4 * c;
+                            float4 v = make_float4(p.alpha * acc[j], p.alpha * acc[j + 1],
+                                                   p.alpha * acc[j + 2], p.alpha * acc[j + 3]);
+                            const int gc = col_base + j;
+                            if (p.beta != 0.0f && row < p.M && gc < p.N) {
+                                const float* src = p.C + (int64_t)row * p.ldc + gc;
+                                if (gc + 3 < p.N) {
+                                    const float4 o = *reinterpret_cast<const float4*>(src);
+                                    v.x = fmaf(p.beta, o.x, v.x);
+                                    v.y = fmaf(p.beta, o.y, v.y);
+                                    v.z = fmaf(p.beta, o.z, v.z);
+                                    v.w = fmaf(p.beta, o.w, v.w);
+                                } else {
+                                    v.x = fmaf(p.beta, src[0], v.x);
+                                    if (gc + 1 < p.N) v.y = fmaf(p.beta, src[1], v.y);
+                                    if (gc + 2 < p.N) v.z = fmaf(p.beta, src[2], v.z);
+                                }
+                            }
                             const uint32_t a = cst + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4);
                             asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
-                                         :: "r"(a), "f"(p.alpha * acc[j]), "f"(p.alpha * acc[j + 1]),
-                                            "f"(p.alpha * acc[j + 2]), "f"(p.alpha * acc[j + 3])
+                                         :: "r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                                          : "memory");
                         }
                         fence_proxy_async_smem();
