@@ -23,6 +23,7 @@ static_assert(kModeBf16x9 == EMU_MODE_BF16X9 && kModeTf32x3 == EMU_MODE_TF32X3 &
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kHostChunksMax = 8;        // row chunks of emu_sgemm_host's copy/compute pipeline
 
 struct DeviceState {
     int checked = 0;           // 0 unknown, 1 supported, -1 unsupported
@@ -32,6 +33,10 @@ struct DeviceState {
     size_t ws_bytes = 0;
     void* stage = nullptr;     // device staging for emu_sgemm_host
     size_t stage_bytes = 0;
+    // emu_sgemm_host's pipeline: host->device and device->host copy streams
+    // and per-chunk events (created on first use, kept until exit)
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_in[kHostChunksMax] = {}, ev_done[kHostChunksMax] = {};
 };
 
 std::mutex g_mu;
@@ -233,20 +238,26 @@ emu_status_t check_gemm_args(int transA, int transB, int64_t M, int64_t N, int64
     return EMU_OK;
 }
 
+// Workspace layout: op(B)^T's pieces first (at offset 0, so that they stay
+// where they are for any M), then op(A)'s at a 1 KB boundary.  b_ready: B's
+// pieces for this B, mode and K are already there (an earlier row chunk of
+// the same emu_sgemm_host call put them) and are not split again.
 emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
                           float alpha, const float* A, int64_t lda, const float* B, int64_t ldb,
-                          float beta, float* C, int64_t ldc, DeviceState* d, cudaStream_t stream) {
+                          float beta, float* C, int64_t ldc, DeviceState* d, cudaStream_t stream,
+                          bool b_ready = false) {
     const int64_t ldp = plane_ld(K);
     const int tf32 = mode_is_tf32(mode);
     const int planes = mode_pieces(mode);
     const int esize = mode_piece_bytes(mode);
     const size_t a_bytes = (size_t)planes * M * ldp * esize;
     const size_t b_bytes = (size_t)planes * N * ldp * esize;
-    const size_t a_region = (a_bytes + 1023) / 1024 * 1024;
-    emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, a_region + b_bytes);
+    const size_t b_region = (b_bytes + 1023) / 1024 * 1024;
+    if (b_ready && d->ws_bytes < b_region + a_bytes) return EMU_ERR_INVALID_VALUE;  // caller's bug
+    emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, b_region + a_bytes);
     if (st != EMU_OK) return st;
-    uint8_t* wa = static_cast<uint8_t*>(d->ws);
-    uint8_t* wb = wa + a_region;
+    uint8_t* wb = static_cast<uint8_t*>(d->ws);
+    uint8_t* wa = wb + b_region;
 
     cudaError_t e;
     {
@@ -254,7 +265,7 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
         e = launch_split_pieces(mode, A, M, K, lda, transA, wa, ldp, stream);
     }
     if (e != cudaSuccess) return from_cuda(e);
-    {
+    if (!b_ready) {
         // op(B)^T is N x K: B itself when transB == 1, B^T otherwise
         ProfScope ps(0, stream);
         e = launch_split_pieces(mode, B, N, K, ldb, !transB, wb, ldp, stream);
@@ -297,13 +308,14 @@ bool fused_ok(int mode, int transA, const float* A, int64_t lda) {
 // read as FP32 by the GEMM kernel and split in shared memory.
 emu_status_t run_fused(int transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                        int64_t lda, const float* B, int64_t ldb, float beta, float* C,
-                       int64_t ldc, DeviceState* d, cudaStream_t stream) {
+                       int64_t ldc, DeviceState* d, cudaStream_t stream, bool b_ready = false) {
     const int64_t ldp = plane_ld(K);
+    if (b_ready && d->ws_bytes < (size_t)3 * N * ldp * 2) return EMU_ERR_INVALID_VALUE;
     emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, (size_t)3 * N * ldp * 2);
     if (st != EMU_OK) return st;
     uint16_t* pb = static_cast<uint16_t*>(d->ws);
-    cudaError_t e;
-    {
+    cudaError_t e = cudaSuccess;
+    if (!b_ready) {
         ProfScope ps(0, stream);
         e = launch_split_bf16x3(B, N, K, ldb, !transB, pb, pb + N * ldp, pb + 2 * N * ldp, ldp,
                                 stream);
@@ -331,6 +343,44 @@ emu_status_t run_fused(int transB, int64_t M, int64_t N, int64_t K, float alpha,
     return from_cuda(e);
 }
 
+// What one call runs: the kernel mode after the strategy's choice, and
+// whether the fused path takes it.
+struct Plan {
+    int mode;
+    bool fused;
+};
+
+Plan plan_call(int transA, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, int mode,
+               const DeviceState* d) {
+    if (g_strategy < 0) g_strategy = read_strategy_env();
+    if (g_path < 0) g_path = read_path_env();
+    Plan pl;
+    // PERFORMANT: the plain FP32 kernel where it is predicted faster
+    pl.mode = choose_mode(M, N, K, mode, g_strategy == EMU_STRATEGY_PERFORMANT, d->sms);
+    // AUTO: the fused kernel splits A once per 128-column tile, so it pays off
+    // when N is small (measured on GB300: N = 256 MLIP layers 1.16x faster
+    // than two-pass; N = 1024 and square shapes slower).
+    const bool auto_fused = g_path == EMU_PATH_AUTO && N <= 256 && M >= 4096;
+    pl.fused = pl.mode != EMU_MODE_FP32_SIMT && (g_path == EMU_PATH_FUSED || auto_fused) &&
+               fused_ok(pl.mode, transA, A, lda);
+    return pl;
+}
+
+emu_status_t run_planned(const Plan& pl, int transA, int transB, int64_t M, int64_t N, int64_t K,
+                         float alpha, const float* A, int64_t lda, const float* B, int64_t ldb,
+                         float beta, float* C, int64_t ldc, DeviceState* d, cudaStream_t stream,
+                         bool b_ready) {
+    if (pl.mode == EMU_MODE_FP32_SIMT) {
+        ProfScope ps(3, stream);
+        return from_cuda(launch_gemm_simt(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                                          ldc, stream));
+    }
+    if (pl.fused)
+        return run_fused(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream, b_ready);
+    return run_two_pass(pl.mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d,
+                        stream, b_ready);
+}
+
 emu_status_t sgemm_device(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                           const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
                           float* C, int64_t ldc, int mode, cudaStream_t stream) {
@@ -344,23 +394,9 @@ emu_status_t sgemm_device(int transA, int transB, int64_t M, int64_t N, int64_t 
         ProfScope ps(4, stream);
         return from_cuda(launch_scale(M, N, beta, C, ldc, stream));
     }
-    if (g_strategy < 0) g_strategy = read_strategy_env();
-    // PERFORMANT: the plain FP32 kernel where it is predicted faster
-    mode = choose_mode(M, N, K, mode, g_strategy == EMU_STRATEGY_PERFORMANT, d->sms);
-    if (mode == EMU_MODE_FP32_SIMT) {
-        ProfScope ps(3, stream);
-        return from_cuda(launch_gemm_simt(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
-                                          ldc, stream));
-    }
-    if (g_path < 0) g_path = read_path_env();
-    // AUTO: the fused kernel splits A once per 128-column tile, so it pays off
-    // when N is small (measured on GB300: N = 256 MLIP layers 1.16x faster
-    // than two-pass; N = 1024 and square shapes slower).
-    const bool auto_fused = g_path == EMU_PATH_AUTO && N <= 256 && M >= 4096;
-    if ((g_path == EMU_PATH_FUSED || auto_fused) && fused_ok(mode, transA, A, lda))
-        return run_fused(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream);
-    return run_two_pass(mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d,
-                        stream);
+    const Plan pl = plan_call(transA, M, N, K, A, lda, mode, d);
+    return run_planned(pl, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream,
+                       false);
 }
 
 emu_status_t check_split_args(const void* X, int64_t rows, int64_t cols, int64_t ld, int trans,
@@ -400,6 +436,86 @@ emu_status_t emu_sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K, 
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+// emu_sgemm_host for large problems: B goes first, then op(A) (and C when
+// beta != 0) in row chunks on a copy stream; each chunk's GEMM runs on the
+// caller's stream as soon as its rows have landed (B's pieces are split once,
+// by the first chunk), and each chunk of C goes back on a second copy stream
+// while the next chunk computes.  Host->device copies, the GEMM and
+// device->host copies overlap; the result is the same as one call's, as row
+// chunks of C are independent.
+emu_status_t host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                            const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                            float* C, int64_t ldc, int mode, DeviceState* d, float* dA, float* dB,
+                            float* dC, size_t b_bytes, cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    if (!d->s_in) {
+        e = cudaStreamCreateWithFlags(&d->s_in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d->s_out, cudaStreamNonBlocking);
+        for (int i = 0; i < kHostChunksMax && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&d->ev_in[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d->ev_done[i], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    // row chunks: a multiple of 256 rows (whole tile rows), about 64 MB of
+    // op(A) each, 2 to kHostChunksMax of them
+    const int64_t row_bytes = (transA ? 1 : lda) * 4 * (transA ? K : 1) + N * 4;
+    int64_t nch = (M * row_bytes) / (int64_t(64) << 20);
+    nch = nch < 2 ? 2 : (nch > kHostChunksMax ? kHostChunksMax : nch);
+    const int64_t mc = (((M + nch - 1) / nch) + 255) / 256 * 256;
+    nch = (M + mc - 1) / mc;
+
+    const Plan pl = plan_call(transA, M, N, K, dA, lda, mode, d);
+    // size the workspace for the largest chunk now: no reallocation (and no
+    // loss of B's pieces) inside the loop
+    if (pl.mode != EMU_MODE_FP32_SIMT) {
+        const int64_t ldp = plane_ld(K);
+        const size_t pb = (size_t)mode_pieces(pl.mode) * mode_piece_bytes(pl.mode) * ldp;
+        const size_t need = pl.fused ? (size_t)3 * N * ldp * 2
+                                     : (pb * N + 1023) / 1024 * 1024 + pb * mc;
+        emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, need);
+        if (st != EMU_OK) return st;
+    }
+    // the copy streams start after the caller's earlier work on its stream
+    e = cudaEventRecord(d->ev_done[0], stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->s_in, d->ev_done[0], 0);
+    if (e == cudaSuccess && b_bytes)
+        e = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, d->s_in);
+    emu_status_t st = EMU_OK;
+    for (int64_t i = 0; i < nch && e == cudaSuccess && st == EMU_OK; ++i) {
+        const int64_t m0 = i * mc, rows = (M - m0 < mc) ? M - m0 : mc;
+        if (transA == 0) {
+            e = cudaMemcpyAsync(dA + m0 * lda, A + m0 * lda, size_t((rows - 1) * lda + K) * 4,
+                                cudaMemcpyHostToDevice, d->s_in);
+        } else {   // op(A)'s rows m0.. are columns of the stored K x M matrix
+            e = cudaMemcpy2DAsync(dA + m0, size_t(lda) * 4, A + m0, size_t(lda) * 4,
+                                  size_t(rows) * 4, size_t(K), cudaMemcpyHostToDevice, d->s_in);
+        }
+        const size_t c_chunk = size_t((rows - 1) * ldc + N) * 4;
+        if (e == cudaSuccess && beta != 0.0f)
+            e = cudaMemcpyAsync(dC + m0 * ldc, C + m0 * ldc, c_chunk, cudaMemcpyHostToDevice,
+                                d->s_in);
+        if (e == cudaSuccess) e = cudaEventRecord(d->ev_in[i], d->s_in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, d->ev_in[i], 0);
+        if (e != cudaSuccess) break;
+        st = run_planned(pl, transA, transB, rows, N, K, alpha, transA ? dA + m0 : dA + m0 * lda,
+                         lda, dB, ldb, beta, dC + m0 * ldc, ldc, d, stream, i > 0);
+        if (st != EMU_OK) break;
+        e = cudaEventRecord(d->ev_done[i], stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(d->s_out, d->ev_done[i], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(C + m0 * ldc, dC + m0 * ldc, c_chunk, cudaMemcpyDeviceToHost,
+                                d->s_out);
+    }
+    // wait for everything issued, whatever failed
+    const cudaError_t e1 = cudaStreamSynchronize(d->s_in);
+    const cudaError_t e2 = cudaStreamSynchronize(stream);
+    const cudaError_t e3 = cudaStreamSynchronize(d->s_out);
+    if (st != EMU_OK) return st;
+    if (e == cudaSuccess) e = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+    return from_cuda(e);
+}
+
 emu_status_t emu_sgemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                             const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
                             float* C, int64_t ldc, int mode, emu_stream_t stream_) {
@@ -423,6 +539,10 @@ emu_status_t emu_sgemm_host(int transA, int transB, int64_t M, int64_t N, int64_
     float* dA = reinterpret_cast<float*>(base);
     float* dB = reinterpret_cast<float*>(base + up(a_bytes));
     float* dC = reinterpret_cast<float*>(base + up(a_bytes) + up(b_bytes));
+    const size_t moved = a_bytes + b_bytes + c_bytes * (beta != 0.0f ? 2 : 1);
+    if (K > 0 && alpha != 0.0f && M >= 512 && moved >= (size_t(64) << 20))
+        return host_pipelined(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, mode,
+                              d, dA, dB, dC, b_bytes, stream);
     cudaError_t e = cudaSuccess;
     if (a_bytes) e = cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess && b_bytes) e = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, stream);
@@ -604,12 +724,22 @@ emu_status_t emu_shutdown(void) {
     cudaGetDevice(&cur);
     for (int i = 0; i < kMaxDevices; ++i) {
         DeviceState& d = g_dev[i];
-        if (!d.ws && !d.stage) continue;
+        if (!d.ws && !d.stage && !d.s_in) continue;
         cudaSetDevice(i);
         if (d.ws) cudaFree(d.ws);
         if (d.stage) cudaFree(d.stage);
         d.ws = d.stage = nullptr;
         d.ws_bytes = d.stage_bytes = 0;
+        if (d.s_in) {
+            cudaStreamDestroy(d.s_in);
+            cudaStreamDestroy(d.s_out);
+            for (int j = 0; j < kHostChunksMax; ++j) {
+                if (d.ev_in[j]) cudaEventDestroy(d.ev_in[j]);
+                if (d.ev_done[j]) cudaEventDestroy(d.ev_done[j]);
+                d.ev_in[j] = d.ev_done[j] = nullptr;
+            }
+            d.s_in = d.s_out = nullptr;
+        }
     }
     cudaSetDevice(cur);
     return EMU_OK;

@@ -43,8 +43,8 @@
 // x 64, two 128-byte-swizzled boxes) into one of two staging buffers;
 // sixteen split warps turn it (16 elements per thread) straight into the swizzled
 // piece layout the MMA reads, make the writes visible to the tensor core
-// (fence.proxy.async) and signal the leader CTA, running ahead of the tensor
-// core by up to two K blocks.
+// (fence.proxy.async), meet at a named barrier, and one thread signals the
+// leader CTA, running ahead of the tensor core by up to two K blocks.
 //
 // Warps (576 threads per CTA, 832 when fused):
 //   warp 0      TMA producer (both CTAs; completion counted on the leader's
@@ -187,6 +187,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Named barrier `id` over `nthreads` threads that also ANDs a predicate: every
+// participating warp reaches it once per use, whatever its predicate, so a
+// warp whose wait gave up still meets the others and all leave together.
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n"
+                 " bar.red.and.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(r) : "r"(uint32_t(v)), "r"(id), "r"(nthreads) : "memory");
+    return r != 0;
+}
+constexpr int kSplitBarrier = 1;                      // named barrier of the split warps
+
 template <int MODE, int BN, int FUSED>
 __global__ void __launch_bounds__(threads_k<FUSED>(), 1)
 gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
@@ -229,10 +241,10 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             mbar_init(cempty0 + 8 * b, 2 * Cfg::acc_warps);   // accumulator warps of both CTAs
         }
         if (FUSED) {
-            for (int s = 0; s < S; ++s) mbar_init(aready0 + 8 * s, 2 * kSplitWarps);
+            for (int s = 0; s < S; ++s) mbar_init(aready0 + 8 * s, 2);   // one per CTA
             for (int f = 0; f < kA32Bufs; ++f) {
                 mbar_init(afull0 + 8 * f, 1);
-                mbar_init(afree0 + 8 * f, kSplitWarps);
+                mbar_init(afree0 + 8 * f, 1);
             }
         }
         *abort_flag = 0;
@@ -386,15 +398,20 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         for (uint32_t g = 0; g < my_blocks; ++g) {
             const uint32_t f = g % kA32Bufs, fph = (g / kA32Bufs) & 1;
             const uint32_t s = g % S, ph = (g / S) & 1;
-            if (!mbar_wait(afull0 + 8 * f, fph, p.err, kDevErrTimeout) ||
-                !mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
+            const bool ok = mbar_wait(afull0 + 8 * f, fph, p.err, kDevErrTimeout) &&
+                            mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) &&
+                            !*abort_flag;
+            if (ok) {
+                split_block(a32 + f * kA32Buf, smem + s * Cfg::stage_bytes, w, lane);
+                fence_proxy_async_smem();    // generic-proxy writes -> tensor core
+            }
+            // all 16 split warps done with this block; one thread signals, so
+            // one cluster-scope release per block instead of sixteen
+            if (!bar_and(kSplitBarrier, kSplitWarps * 32, ok)) {
                 *abort_flag = 1;
                 break;
             }
-            split_block(a32 + f * kA32Buf, smem + s * Cfg::stage_bytes, w, lane);
-            fence_proxy_async_smem();        // generic-proxy writes -> tensor core
-            __syncwarp();
-            if (lane == 0) {
+            if (w == 0 && lane == 0) {
                 mbar_arrive(afree0 + 8 * f);
                 mbar_arrive_remote(aready_leader0 + 8 * s);
             }

@@ -149,7 +149,13 @@ emu_status_t emu_sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
  * `stream`, runs emu_sgemm there and copies C back, then synchronises the
  * stream before it returns, so C holds the result on return.  Same
  * arguments, layout and error codes as emu_sgemm; the device buffers are
- * grown on demand and released by emu_shutdown().
+ * grown on demand and released by emu_shutdown().  When more than 64 MB
+ * move (and M >= 512), the copies are pipelined with the GEMM: B first, then
+ * op(A) and C in row chunks of whole 256-row tiles on a library-owned copy
+ * stream, each chunk's GEMM on `stream` as its rows land (B's pieces split
+ * once), and C's chunks back on a second library-owned stream; the result is
+ * element for element that of one emu_sgemm call.  Host buffers in pinned
+ * memory let the copies overlap; pageable ones work too.
  */
 emu_status_t emu_sgemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K,
                             float alpha, const float* A, int64_t lda,

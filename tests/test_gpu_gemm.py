@@ -234,6 +234,41 @@ def test_host_entry_point_matches_device_path(emu):
     assert np.array_equal(dev, host)
 
 
+@pytest.mark.parametrize("transA,transB,beta,mode",
+                         [(0, 0, 0.0, "bf16x9"), (1, 1, 0.5, "bf16x9"), (0, 1, -1.0, "tf32x3"),
+                          (1, 0, 0.0, "fp32_simt")])
+def test_host_entry_pipelined_rows_match_one_call(emu, transA, transB, beta, mode):
+    """Large enough for the chunked copy/compute pipeline (row chunks of C on
+    three streams): every element equals the one-call device result, since
+    row chunks of C are computed independently by the same kernels."""
+    M, N, K = 8300, 1024, 1024                       # ragged last chunk
+    r = W.rng(18 + transA + 2 * transB)
+    A = W.normal(r, (K, M) if transA else (M, K))
+    B = W.normal(r, (N, K) if transB else (K, N))
+    C0 = W.normal(r, (M, N))
+    dev = _run(emu, A, B, transA, transB, alpha=0.75, beta=beta, C0=C0, mode=mode)
+    host = emu.emu_sgemm_host(A, B, C0.copy(), transA=transA, transB=transB, alpha=0.75,
+                              beta=beta, mode=mode)
+    assert np.array_equal(dev, host)
+    mi, ni = W.sample_pairs(M, N, 1024, seed=3)
+    Cref, Sabs = oracle.gemm_ref(A, B, transA, transB, 0.75, beta, C0, pairs=(mi, ni))
+    assert checks.error_ratio(host[mi, ni], Cref, Sabs, K, 0.75, beta, C0[mi, ni],
+                              mode=_bound_mode(mode)) <= 1.0
+
+
+def test_host_entry_pipelined_fused_shape(emu):
+    """N = 256 rows of an MLIP layer: the fused path in every chunk, B's
+    pieces split once and reused."""
+    g = W.WORKLOADS["mlip192_k256_n256"]
+    M = 70000
+    r = W.rng(19)
+    A = W.normal(r, (M, g.K))
+    B = W.normal(r, (g.N, g.K), std=g.K ** -0.5)
+    dev = _run(emu, A, B, transB=True)
+    host = emu.emu_sgemm_host(A, B, transB=True)
+    assert np.array_equal(dev, host)
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(emu):
     emu.emu_clear_device_error()
     assert emu.emu_selftest_timeout(2000) == -5          # EMU_ERR_TIMEOUT
@@ -311,3 +346,25 @@ def test_fused_path_square8192_sampled(emu):
 
 def test_no_device_error_after_fused(emu):
     assert emu.emu_get_last_device_error() == 0
+
+
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3", "tf32x3_oy", "bf16x3", "tf32", "fp32_simt"])
+def test_subnormal_operands_through_the_tensor_core(emu, mode):
+    """FP32 subnormals in B (every element), identity A, and the transpose:
+    BF16x9 and SIMT reproduce B exactly, so the tensor core neither flushes
+    subnormal BF16 pieces nor subnormal FP32 partial sums; every mode equals
+    the oracle's emulation of the same mode bit for bit (one nonzero product
+    per output, so no rounding order is involved)."""
+    r = W.rng(77)
+    u = r.integers(1, 1 << 23, (256, 256)).astype(np.uint32) | \
+        (r.integers(0, 2, (256, 256)).astype(np.uint32) << 31)
+    Bs = u.view(np.float32)
+    I = np.eye(256, dtype=np.float32)
+    emul = {"bf16x9": oracle.gemm_bf16x9, "tf32x3": oracle.gemm_tf32x3,
+            "tf32x3_oy": oracle.gemm_tf32x3_oy, "bf16x3": oracle.gemm_bf16x3,
+            "tf32": oracle.gemm_tf32, "fp32_simt": oracle.gemm_fp32}[mode]
+    for X, Y in ((I, Bs), (Bs, I)):
+        C = _run(emu, X, Y, mode=mode)
+        assert np.array_equal(C.view(np.uint32), emul(X, Y).view(np.uint32))
+        if mode in ("bf16x9", "fp32_simt"):
+            assert np.array_equal(C.view(np.uint32), u)
