@@ -277,6 +277,19 @@ __device__ __forceinline__ uint32_t tf32_rn_bits(float x) {
     return ((r & 0x7F800000u) == 0x7F800000u) ? (u & 0xFFFFE000u) : r;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start before the kernel ahead of it in the stream has
+// finished; griddep_wait() makes the calling thread wait until that kernel
+// has completed and its writes are visible (it returns at once when nothing
+// is pending), and griddep_launch_dependents() lets the next such kernel
+// start launching now.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // x = hi + lo / lo_scale, both TF32: lo_scale = 1 for TF32x3, 2^11 for the
 // Ootomo-Yokota variant (the residual is scaled before its rounding; the
 // scaling by a power of two is exact).

@@ -50,23 +50,30 @@ struct TcGemmParams {
 // Launchers (return the launch status; nothing is synchronised).
 cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
                                 uint16_t* P0, uint16_t* P1, uint16_t* P2, int64_t ldp,
-                                cudaStream_t stream);
+                                cudaStream_t stream, bool pdl = false);
 // lo_scale: 1 (TF32x3) or 2^11 (the residual scaled before its rounding)
 cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
                                 float* HI, float* LO, int64_t ldp, cudaStream_t stream,
-                                float lo_scale = 1.0f);
+                                float lo_scale = 1.0f, bool pdl = false);
 // The pieces a tensor-core mode reads, as consecutive planes of rows x ldp
 // elements (BF16 bits or TF32-valued FP32) starting at `planes`.
+// pdl: launch as a programmatic dependent of the kernel ahead in the stream
+// (only where the two are independent); the split still completes after it.
 cudaError_t launch_split_pieces(int mode, const float* X, int64_t rows, int64_t cols, int64_t ld,
-                                int trans, void* planes, int64_t ldp, cudaStream_t stream);
+                                int trans, void* planes, int64_t ldp, cudaStream_t stream,
+                                bool pdl = false);
 // Bytes of one piece element of a mode.
 constexpr int mode_piece_bytes(int m) { return mode_is_tf32(m) ? 4 : 2; }
 // mode: one of the kMode* variants; bn: tile width 128 or 256 (the two
 // cheaper modes: 256 only); fused: mapA is an FP32 map over op(A) (box
 // 32 x 128) split in shared memory (BF16x9, bn 128 only)
+// pdl: the GEMM may start (prologue: barriers, tensor memory, descriptor
+// prefetch) while the split ahead of it runs; its producer waits for that
+// split before the first piece load.
 cudaError_t launch_gemm_kblock(int mode, int bn, int fused, const CUtensorMap& mapA,
                                const CUtensorMap& mapB, const CUtensorMap& mapC,
-                               const TcGemmParams& p, int sms, cudaStream_t stream);
+                               const TcGemmParams& p, int sms, cudaStream_t stream,
+                               bool pdl = false);
 cudaError_t launch_gemm_simt(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                              const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
                              float* C, int64_t ldc, cudaStream_t stream);

@@ -268,7 +268,8 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
     if (!b_ready) {
         // op(B)^T is N x K: B itself when transB == 1, B^T otherwise
         ProfScope ps(0, stream);
-        e = launch_split_pieces(mode, B, N, K, ldb, !transB, wb, ldp, stream);
+        // independent of A's split: may run beside it (programmatic launch)
+        e = launch_split_pieces(mode, B, N, K, ldb, !transB, wb, ldp, stream, true);
     }
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -292,7 +293,7 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
     p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
     {
         ProfScope ps(1, stream);
-        e = launch_gemm_kblock(mode, bn, 0, mapA, mapB, mapC, p, d->sms, stream);
+        e = launch_gemm_kblock(mode, bn, 0, mapA, mapB, mapC, p, d->sms, stream, true);
     }
     return from_cuda(e);
 }
@@ -338,7 +339,7 @@ emu_status_t run_fused(int transB, int64_t M, int64_t N, int64_t K, float alpha,
     p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
     {
         ProfScope ps(2, stream);
-        e = launch_gemm_kblock(0, bn, 1, mapA, mapB, mapC, p, d->sms, stream);
+        e = launch_gemm_kblock(0, bn, 1, mapA, mapB, mapC, p, d->sms, stream, true);
     }
     return from_cuda(e);
 }

@@ -267,6 +267,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------- TMA producer
+        griddep_wait();                           // the split ahead has written the pieces
         const uint32_t full_leader0 = map_to_rank(full0, 0);
         uint32_t kbg = 0;                         // K blocks staged so far (all tiles)
         bool ok = true;
@@ -553,7 +554,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
 template <int MODE, int BN, int FUSED>
 cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
                             const CUtensorMap& mapC, const TcGemmParams& p, int clusters,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool pdl) {
     using Cfg = KCfg<MODE, BN, FUSED>;
     static bool attr = false;
     if (!attr) {
@@ -567,13 +568,15 @@ cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
     cfg.blockDim = dim3(threads_k<FUSED>());
     cfg.dynamicSmemBytes = Cfg::smem;
     cfg.stream = stream;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, gemm_kblock_kernel<MODE, BN, FUSED>, mapA, mapB, mapC, p);
 }
 
@@ -581,26 +584,26 @@ cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
 
 cudaError_t launch_gemm_kblock(int mode, int bn, int fused, const CUtensorMap& mapA,
                                const CUtensorMap& mapB, const CUtensorMap& mapC,
-                               const TcGemmParams& p, int sms, cudaStream_t stream) {
+                               const TcGemmParams& p, int sms, cudaStream_t stream, bool pdl) {
     const int tiles = p.tiles_m * p.tiles_n;
     if (tiles == 0) return cudaSuccess;
     const int clusters = tiles < sms / 2 ? tiles : sms / 2;
     cudaError_t e;
     if (fused) {
         if (mode != kModeBf16x9 || bn != 128) return cudaErrorInvalidValue;
-        e = launch_kblock_t<kModeBf16x9, 128, 1>(mapA, mapB, mapC, p, clusters, stream);
+        e = launch_kblock_t<kModeBf16x9, 128, 1>(mapA, mapB, mapC, p, clusters, stream, pdl);
     } else if (mode == kModeTf32x3) {
-        e = bn == 128 ? launch_kblock_t<kModeTf32x3, 128, 0>(mapA, mapB, mapC, p, clusters, stream)
-                      : launch_kblock_t<kModeTf32x3, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+        e = bn == 128 ? launch_kblock_t<kModeTf32x3, 128, 0>(mapA, mapB, mapC, p, clusters, stream, pdl)
+                      : launch_kblock_t<kModeTf32x3, 256, 0>(mapA, mapB, mapC, p, clusters, stream, pdl);
     } else if (mode == kModeBf16x9) {
-        e = bn == 128 ? launch_kblock_t<kModeBf16x9, 128, 0>(mapA, mapB, mapC, p, clusters, stream)
-                      : launch_kblock_t<kModeBf16x9, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+        e = bn == 128 ? launch_kblock_t<kModeBf16x9, 128, 0>(mapA, mapB, mapC, p, clusters, stream, pdl)
+                      : launch_kblock_t<kModeBf16x9, 256, 0>(mapA, mapB, mapC, p, clusters, stream, pdl);
     } else if (mode == kModeBf16x3 && bn == 256) {
-        e = launch_kblock_t<kModeBf16x3, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+        e = launch_kblock_t<kModeBf16x3, 256, 0>(mapA, mapB, mapC, p, clusters, stream, pdl);
     } else if (mode == kModeTf32 && bn == 256) {
-        e = launch_kblock_t<kModeTf32, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+        e = launch_kblock_t<kModeTf32, 256, 0>(mapA, mapB, mapC, p, clusters, stream, pdl);
     } else if (mode == kModeTf32x3Oy && bn == 256) {
-        e = launch_kblock_t<kModeTf32x3Oy, 256, 0>(mapA, mapB, mapC, p, clusters, stream);
+        e = launch_kblock_t<kModeTf32x3Oy, 256, 0>(mapA, mapB, mapC, p, clusters, stream, pdl);
     } else {
         return cudaErrorInvalidValue;
     }

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) split3_rows_vec8(const float* __restrict_
                                                         uint16_t* __restrict__ P0,
                                                         uint16_t* __restrict__ P1,
                                                         uint16_t* __restrict__ P2, int64_t ldp) {
+    griddep_launch_dependents();
     const int64_t groups = cols / 8;
     const int64_t total = rows * groups;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
@@ -50,6 +51,7 @@ __global__ void __launch_bounds__(256) split3_rows_vec8(const float* __restrict_
         *reinterpret_cast<uint4*>(P1 + o) = o1;
         if (P2) *reinterpret_cast<uint4*>(P2 + o) = o2;
     }
+    griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
 
 // Any shape and alignment: one element per thread.
@@ -58,6 +60,7 @@ __global__ void __launch_bounds__(256) split3_rows_scalar(const float* __restric
                                                           uint16_t* __restrict__ P0,
                                                           uint16_t* __restrict__ P1,
                                                           uint16_t* __restrict__ P2, int64_t ldp) {
+    griddep_launch_dependents();
     const int64_t total = rows * cols;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
          t += (int64_t)gridDim.x * blockDim.x) {
@@ -69,12 +72,14 @@ __global__ void __launch_bounds__(256) split3_rows_scalar(const float* __restric
         P0[o] = h0; P1[o] = h1;
         if (P2) P2[o] = h2;
     }
+    griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
 
 __global__ void __launch_bounds__(256) split2_rows_vec4(const float* __restrict__ X, int64_t rows,
                                                         int64_t cols, int64_t ld,
                                                         float* __restrict__ HI,
                                                         float* __restrict__ LO, int64_t ldp, float lo_scale) {
+    griddep_launch_dependents();
     const int64_t groups = cols / 4;
     const int64_t total = rows * groups;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
@@ -90,12 +95,14 @@ __global__ void __launch_bounds__(256) split2_rows_vec4(const float* __restrict_
         *reinterpret_cast<float4*>(HI + r * ldp + c) = h;
         if (LO) *reinterpret_cast<float4*>(LO + r * ldp + c) = l;
     }
+    griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
 
 __global__ void __launch_bounds__(256) split2_rows_scalar(const float* __restrict__ X, int64_t rows,
                                                           int64_t cols, int64_t ld,
                                                           float* __restrict__ HI,
                                                           float* __restrict__ LO, int64_t ldp, float lo_scale) {
+    griddep_launch_dependents();
     const int64_t total = rows * cols;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
          t += (int64_t)gridDim.x * blockDim.x) {
@@ -106,6 +113,7 @@ __global__ void __launch_bounds__(256) split2_rows_scalar(const float* __restric
         HI[r * ldp + c] = h;
         if (LO) LO[r * ldp + c] = l;
     }
+    griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
 
 // ------------------------------------------------------------- transposed
@@ -120,6 +128,7 @@ __global__ void __launch_bounds__(256) split3_transposed(const float* __restrict
                                                          uint16_t* __restrict__ P0,
                                                          uint16_t* __restrict__ P1,
                                                          uint16_t* __restrict__ P2, int64_t ldp) {
+    griddep_launch_dependents();
     __shared__ float tile[kT][kT + 1];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
     const int64_t r0 = (int64_t)blockIdx.x * kT;              // op rows  = stored columns
@@ -152,6 +161,7 @@ __global__ void __launch_bounds__(256) split3_transposed(const float* __restrict
             if (c + 1 < cols) { P0[o + 1] = b0; P1[o + 1] = b1; if (P2) P2[o + 1] = b2; }
         }
     }
+    griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
 
 // Vectorised form for full 64 x 64 tiles with 16-byte aligned rows on both
@@ -163,6 +173,7 @@ __global__ void __launch_bounds__(256) split3_transposed_vec(const float* __rest
                                                              uint16_t* __restrict__ P0,
                                                              uint16_t* __restrict__ P1,
                                                              uint16_t* __restrict__ P2, int64_t ldp) {
+    griddep_launch_dependents();
     __shared__ float tile[kT][kT + 1];               // [op col (stored row)][op row]
     const int tid = threadIdx.x;
     const int64_t r0 = (int64_t)blockIdx.x * kT;     // op rows  = stored columns
@@ -196,12 +207,14 @@ __global__ void __launch_bounds__(256) split3_transposed_vec(const float* __rest
         if (P2) d2[q] = make_uint4(h2[b] | (uint32_t(h2[b + 1]) << 16), h2[b + 2] | (uint32_t(h2[b + 3]) << 16),
                            h2[b + 4] | (uint32_t(h2[b + 5]) << 16), h2[b + 6] | (uint32_t(h2[b + 7]) << 16));
     }
+    griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
 
 __global__ void __launch_bounds__(256) split2_transposed(const float* __restrict__ X, int64_t rows,
                                                          int64_t cols, int64_t ld,
                                                          float* __restrict__ HI,
                                                          float* __restrict__ LO, int64_t ldp, float lo_scale) {
+    griddep_launch_dependents();
     __shared__ float tile[kT][kT + 1];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     const int64_t r0 = (int64_t)blockIdx.x * kT;
@@ -229,6 +242,28 @@ __global__ void __launch_bounds__(256) split2_transposed(const float* __restrict
             }
         }
     }
+    griddep_wait();          // see launch_pdl: complete only after the kernel ahead
+}
+
+// Launch `kern` on `stream`; with pdl, as a programmatic dependent of the
+// kernel ahead of it: it may start while that kernel runs (this library only
+// asks for it where the two are independent), and because every split
+// kernel calls griddep_wait() before it exits, it completes only after the
+// kernel ahead -- so whatever waits for it (the GEMM's producer) also waits
+// for that one.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, cudaStream_t stream, bool pdl,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -246,57 +281,61 @@ int grid_for(int64_t work, int threads) {
 
 cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
                                 uint16_t* P0, uint16_t* P1, uint16_t* P2, int64_t ldp,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, bool pdl) {
     if (rows == 0 || cols == 0) return cudaSuccess;
+    cudaError_t e;
     if (trans) {
-        dim3 grid((unsigned)((rows + kT - 1) / kT), (unsigned)((cols + kT - 1) / kT));
+        const dim3 grid((unsigned)((rows + kT - 1) / kT), (unsigned)((cols + kT - 1) / kT));
         if (rows % kT == 0 && cols % kT == 0 && ld % 4 == 0 && ldp % 8 == 0 && aligned16(X) &&
             aligned16(P0) && aligned16(P1) && aligned16(P2))
-            split3_transposed_vec<<<grid, 256, 0, stream>>>(X, rows, cols, ld, P0, P1, P2, ldp);
+            e = launch_pdl(split3_transposed_vec, grid, stream, pdl, X, rows, cols, ld, P0, P1, P2,
+                           ldp);
         else
-            split3_transposed<<<grid, 256, 0, stream>>>(X, rows, cols, ld, P0, P1, P2, ldp);
+            e = launch_pdl(split3_transposed, grid, stream, pdl, X, rows, cols, ld, P0, P1, P2, ldp);
     } else if (cols % 8 == 0 && ld % 4 == 0 && ldp % 8 == 0 && aligned16(X) && aligned16(P0) &&
                aligned16(P1) && aligned16(P2)) {
-        split3_rows_vec8<<<grid_for(rows * (cols / 8), 256), 256, 0, stream>>>(X, rows, cols, ld,
-                                                                              P0, P1, P2, ldp);
+        e = launch_pdl(split3_rows_vec8, dim3(grid_for(rows * (cols / 8), 256)), stream, pdl, X,
+                       rows, cols, ld, P0, P1, P2, ldp);
     } else {
-        split3_rows_scalar<<<grid_for(rows * cols, 256), 256, 0, stream>>>(X, rows, cols, ld, P0,
-                                                                          P1, P2, ldp);
+        e = launch_pdl(split3_rows_scalar, dim3(grid_for(rows * cols, 256)), stream, pdl, X, rows,
+                       cols, ld, P0, P1, P2, ldp);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
                                 float* HI, float* LO, int64_t ldp, cudaStream_t stream,
-                                float lo_scale) {
+                                float lo_scale, bool pdl) {
     if (rows == 0 || cols == 0) return cudaSuccess;
+    cudaError_t e;
     if (trans) {
-        dim3 grid((unsigned)((rows + kT - 1) / kT), (unsigned)((cols + kT - 1) / kT));
-        split2_transposed<<<grid, 256, 0, stream>>>(X, rows, cols, ld, HI, LO, ldp, lo_scale);
+        const dim3 grid((unsigned)((rows + kT - 1) / kT), (unsigned)((cols + kT - 1) / kT));
+        e = launch_pdl(split2_transposed, grid, stream, pdl, X, rows, cols, ld, HI, LO, ldp,
+                       lo_scale);
     } else if (cols % 4 == 0 && ld % 4 == 0 && ldp % 4 == 0 && aligned16(X) && aligned16(HI) &&
                aligned16(LO)) {
-        split2_rows_vec4<<<grid_for(rows * (cols / 4), 256), 256, 0, stream>>>(X, rows, cols, ld,
-                                                                              HI, LO, ldp,
-                                                                              lo_scale);
+        e = launch_pdl(split2_rows_vec4, dim3(grid_for(rows * (cols / 4), 256)), stream, pdl, X,
+                       rows, cols, ld, HI, LO, ldp, lo_scale);
     } else {
-        split2_rows_scalar<<<grid_for(rows * cols, 256), 256, 0, stream>>>(X, rows, cols, ld, HI,
-                                                                          LO, ldp, lo_scale);
+        e = launch_pdl(split2_rows_scalar, dim3(grid_for(rows * cols, 256)), stream, pdl, X, rows,
+                       cols, ld, HI, LO, ldp, lo_scale);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_split_pieces(int mode, const float* X, int64_t rows, int64_t cols, int64_t ld,
-                                int trans, void* planes, int64_t ldp, cudaStream_t stream) {
+                                int trans, void* planes, int64_t ldp, cudaStream_t stream,
+                                bool pdl) {
     const int64_t n = rows * ldp;
     if (mode_is_tf32(mode)) {
         float* hi = static_cast<float*>(planes);
         return launch_split_tf32x2(X, rows, cols, ld, trans, hi,
                                    mode_pieces(mode) > 1 ? hi + n : nullptr, ldp, stream,
-                                   mode == kModeTf32x3Oy ? 2048.0f : 1.0f);
+                                   mode == kModeTf32x3Oy ? 2048.0f : 1.0f, pdl);
     }
     uint16_t* p0 = static_cast<uint16_t*>(planes);
     return launch_split_bf16x3(X, rows, cols, ld, trans, p0, p0 + n,
-                               mode_pieces(mode) > 2 ? p0 + 2 * n : nullptr, ldp, stream);
+                               mode_pieces(mode) > 2 ? p0 + 2 * n : nullptr, ldp, stream, pdl);
 }
 
 }  // namespace emu
