@@ -45,6 +45,16 @@ struct TcGemmParams {
     float* C;
     int64_t ldc;
     int tma_store;       // 1: the C tensor map is valid (bulk tensor stores of C)
+    // Tail split: the last tail_tiles tiles (one partial wave) run as
+    // tail_parts units each, over consecutive ranges of K blocks; units
+    // 0 .. tail_parts-2 leave their FP32 sums in part_ws and raise a flag
+    // (value epoch), the last unit adds them and writes C.  units = tiles +
+    // tail_tiles * (tail_parts - 1); tail_parts <= 1: no split.
+    int units;
+    int tail_tiles, tail_parts;
+    float* part_ws;
+    unsigned* flags;
+    unsigned epoch;
 };
 
 // Launchers (return the launch status; nothing is synchronised).
@@ -74,6 +84,9 @@ cudaError_t launch_gemm_kblock(int mode, int bn, int fused, const CUtensorMap& m
                                const CUtensorMap& mapB, const CUtensorMap& mapC,
                                const TcGemmParams& p, int sms, cudaStream_t stream,
                                bool pdl = false);
+// Clusters of the GEMM variant that can be resident at once on a GPU with
+// `sms` SMs (at most sms / 2); the persistent grid uses this many.
+int gemm_kblock_clusters(int mode, int bn, int fused, int sms);
 cudaError_t launch_gemm_simt(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                              const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
                              float* C, int64_t ldc, cudaStream_t stream);

@@ -37,6 +37,12 @@ struct DeviceState {
     // and per-chunk events (created on first use, kept until exit)
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t ev_in[kHostChunksMax] = {}, ev_done[kHostChunksMax] = {};
+    // the GEMM's tail split: partial sums (grown on demand), flags (zeroed
+    // once) and the epoch that marks this call's flags
+    void* part = nullptr;
+    size_t part_bytes = 0;
+    unsigned* flags = nullptr;
+    unsigned epoch = 0;
 };
 
 std::mutex g_mu;
@@ -221,6 +227,49 @@ bool make_c_map(CUtensorMap* map, float* C, int64_t M, int64_t N, int64_t ldc) {
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Split the last, partial wave of tiles along K so that it fills the GPU:
+// with C clusters and a remainder of r tiles, each of those r tiles runs as
+// min(C / r, 8, K blocks / 2) parts on as many clusters (C: the clusters
+// of this GEMM variant that can be resident at once).  Sets p.units,
+// p.tail_*, p.part_ws, p.flags and p.epoch.
+constexpr int kFlagsBytes = 64 << 10;
+
+emu_status_t plan_tail(TcGemmParams& p, int mode, int bm, int bn, int fused, DeviceState* d) {
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int clusters = gemm_kblock_clusters(mode, bn, fused, d->sms);
+    p.units = tiles;
+    p.tail_tiles = 0;
+    p.tail_parts = 1;
+    p.part_ws = nullptr;
+    p.flags = nullptr;
+    p.epoch = 0;
+    const int rem = clusters > 0 ? tiles % clusters : 0;
+    if (rem == 0) return EMU_OK;
+    int parts = clusters / rem;
+    if (parts > 8) parts = 8;
+    if (parts > p.num_kb / 2) parts = p.num_kb / 2;
+    if (parts < 2) return EMU_OK;
+    const size_t need = (size_t)rem * (parts - 1) * bm * bn * sizeof(float);
+    emu_status_t st = ensure_buffer(&d->part, &d->part_bytes, need);
+    if (st != EMU_OK) return st;
+    if (!d->flags) {
+        if (cudaMalloc(&d->flags, kFlagsBytes) != cudaSuccess) {
+            cudaGetLastError();
+            d->flags = nullptr;
+            return EMU_ERR_ALLOC;
+        }
+        if (cudaMemset(d->flags, 0, kFlagsBytes) != cudaSuccess) return from_cuda(cudaGetLastError());
+    }
+    if ((size_t)rem * (parts - 1) * 2 * 16 * sizeof(unsigned) > (size_t)kFlagsBytes) return EMU_OK;
+    p.tail_tiles = rem;
+    p.tail_parts = parts;
+    p.units = tiles + rem * (parts - 1);
+    p.part_ws = static_cast<float*>(d->part);
+    p.flags = d->flags;
+    p.epoch = ++d->epoch == 0 ? ++d->epoch : d->epoch;   // never 0 (the flags' initial value)
+    return EMU_OK;
+}
+
 emu_status_t check_gemm_args(int transA, int transB, int64_t M, int64_t N, int64_t K,
                              const float* A, int64_t lda, const float* B, int64_t ldb,
                              float beta, float* C, int64_t ldc, int mode) {
@@ -282,7 +331,7 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
     st = make_plane_map(&mapB, wb, tf32, N, K, ldp, planes, box_cols, bn / 2);
     if (st != EMU_OK) return st;
 
-    TcGemmParams p;
+    TcGemmParams p = {};
     p.err = d->err;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
     p.num_kb = (int)((K + box_cols - 1) / box_cols);
@@ -291,6 +340,8 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     CUtensorMap mapC = mapB;                 // placeholder when C is stored directly
     p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
+    st = plan_tail(p, mode, 256, bn, 0, d);
+    if (st != EMU_OK) return st;
     {
         ProfScope ps(1, stream);
         e = launch_gemm_kblock(mode, bn, 0, mapA, mapB, mapC, p, d->sms, stream, true);
@@ -328,7 +379,7 @@ emu_status_t run_fused(int transB, int64_t M, int64_t N, int64_t K, float alpha,
     if (st != EMU_OK) return st;
     st = make_plane_map(&mapB, pb, false, N, K, ldp, 3, 64, bn / 2);
     if (st != EMU_OK) return st;
-    TcGemmParams p;
+    TcGemmParams p = {};
     p.err = d->err;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
     p.num_kb = (int)((K + 63) / 64);
@@ -337,6 +388,8 @@ emu_status_t run_fused(int transB, int64_t M, int64_t N, int64_t K, float alpha,
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     CUtensorMap mapC = mapB;
     p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
+    st = plan_tail(p, kModeBf16x9, 256, bn, 1, d);
+    if (st != EMU_OK) return st;
     {
         ProfScope ps(2, stream);
         e = launch_gemm_kblock(0, bn, 1, mapA, mapB, mapC, p, d->sms, stream, true);
@@ -725,12 +778,17 @@ emu_status_t emu_shutdown(void) {
     cudaGetDevice(&cur);
     for (int i = 0; i < kMaxDevices; ++i) {
         DeviceState& d = g_dev[i];
-        if (!d.ws && !d.stage && !d.s_in) continue;
+        if (!d.ws && !d.stage && !d.s_in && !d.part && !d.flags) continue;
         cudaSetDevice(i);
         if (d.ws) cudaFree(d.ws);
         if (d.stage) cudaFree(d.stage);
         d.ws = d.stage = nullptr;
         d.ws_bytes = d.stage_bytes = 0;
+        if (d.part) cudaFree(d.part);
+        if (d.flags) cudaFree(d.flags);
+        d.part = nullptr;
+        d.part_bytes = 0;
+        d.flags = nullptr;
         if (d.s_in) {
             cudaStreamDestroy(d.s_in);
             cudaStreamDestroy(d.s_out);

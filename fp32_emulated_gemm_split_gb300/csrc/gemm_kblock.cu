@@ -116,6 +116,41 @@ struct KCfg {
     static_assert(!(FUSED && MODE != kModeBf16x9), "the fused path splits BF16x9 pieces only");
 };
 
+// Work unit u of the persistent schedule: a whole tile, or (tail split) one
+// part of a tail tile's K blocks.
+struct Unit {
+    int tile, kb0, kb1;
+    int part, parts;     // parts > 1: this is part `part` of tail tile `tail`
+    int tail;
+};
+
+__device__ __forceinline__ Unit unit_at(const TcGemmParams& p, int u) {
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int first = tiles - p.tail_tiles;
+    Unit w;
+    if (p.tail_parts <= 1 || u < first) {
+        w.tile = u; w.kb0 = 0; w.kb1 = p.num_kb; w.part = 0; w.parts = 1; w.tail = -1;
+        return w;
+    }
+    const int v = u - first;
+    w.tail = v / p.tail_parts;
+    w.part = v - w.tail * p.tail_parts;
+    w.parts = p.tail_parts;
+    w.tile = first + w.tail;
+    w.kb0 = w.part * p.num_kb / p.tail_parts;
+    w.kb1 = (w.part + 1) * p.num_kb / p.tail_parts;
+    return w;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned* a, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* a) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void tile_pos(int tile, int tiles_m, int tiles_n, int& tm, int& tn) {
     constexpr int G = 8;                  // tiles of M walked together: B tiles stay in L2
     const int per_group = G * tiles_n;
@@ -231,7 +266,6 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
     const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
-    const int total = p.tiles_m * p.tiles_n;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < nb_full; ++i) mbar_init(full0 + 8 * i, 1);
@@ -269,14 +303,15 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         // ---------------------------------------------------- TMA producer
         griddep_wait();                           // the split ahead has written the pieces
         const uint32_t full_leader0 = map_to_rank(full0, 0);
-        uint32_t kbg = 0;                         // K blocks staged so far (all tiles)
+        uint32_t kbg = 0;                         // K blocks staged so far (all units)
         bool ok = true;
-        for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
+        for (int u = cluster_id; u < p.units && ok; u += num_clusters) {
+            const Unit w = unit_at(p, u);
             int tm, tn;
-            tile_pos(tile, p.tiles_m, p.tiles_n, tm, tn);
+            tile_pos(w.tile, p.tiles_m, p.tiles_n, tm, tn);
             const int arow = tm * kBM + int(rank) * kHalfRows;
             const int brow = tn * BN + int(rank) * Cfg::b_rows;
-            for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++kbg) {
                 const uint32_t s = kbg % S, ph = (kbg / S) & 1;
                 if (FUSED) {
                     const uint32_t f = kbg % kA32Bufs, fph = (kbg / kA32Bufs) & 1;
@@ -314,12 +349,13 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         uint32_t kbg = 0, part = 0;              // K blocks and TMEM partials so far
         uint32_t prev_s = 0;                     // band-major: stage of the pair's first block
         bool ok = true;
-        for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
-            for (int kb = 0; kb < p.num_kb; ++kb, ++kbg) {
+        for (int u = cluster_id; u < p.units && ok; u += num_clusters) {
+            const Unit w = unit_at(p, u);
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++kbg) {
                 const uint32_t s = kbg % S, ph = (kbg / S) & 1;
                 const uint32_t buf = part % NB, cph = (part / NB) & 1;
-                const bool fresh = (kb % KBP) == 0;             // first block of a partial
-                const bool close = (kb % KBP) == KBP - 1 || kb == p.num_kb - 1;
+                const bool fresh = ((kb - w.kb0) % KBP) == 0;   // first block of a partial
+                const bool close = ((kb - w.kb0) % KBP) == KBP - 1 || kb == w.kb1 - 1;
                 if (fresh && !mbar_wait(cempty0 + 8 * buf, cph ^ 1, p.err, kDevErrTimeout)) {
                     ok = false;
                     break;
@@ -394,8 +430,11 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         // block has landed and its stage is free, ahead of the tensor core.
         const int w = warp - 2 - Cfg::acc_warps;
         const uint32_t aready_leader0 = map_to_rank(aready0, 0);
-        const int my_tiles = cluster_id < total ? (total - 1 - cluster_id) / num_clusters + 1 : 0;
-        const uint32_t my_blocks = uint32_t(my_tiles) * uint32_t(p.num_kb);
+        uint32_t my_blocks = 0;
+        for (int u = cluster_id; u < p.units; u += num_clusters) {
+            const Unit w = unit_at(p, u);
+            my_blocks += uint32_t(w.kb1 - w.kb0);
+        }
         for (uint32_t g = 0; g < my_blocks; ++g) {
             const uint32_t f = g % kA32Bufs, fph = (g / kA32Bufs) & 1;
             const uint32_t s = g % S, ph = (g / S) & 1;
@@ -426,9 +465,11 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
         bool ok = true;
         constexpr int KBP = Cfg::kb_per_partial;
-        const int nparts = (p.num_kb + KBP - 1) / KBP;   // TMEM partials per tile
         uint32_t part = 0;
-        for (int tile = cluster_id; tile < total && ok; tile += num_clusters) {
+        for (int u = cluster_id; u < p.units && ok; u += num_clusters) {
+            const Unit w = unit_at(p, u);
+            const int nparts = (w.kb1 - w.kb0 + KBP - 1) / KBP;   // TMEM partials of this unit
+            const int tile = w.tile;
             float acc[kAccCols];
 #pragma unroll
             for (int j = 0; j < kAccCols; ++j) acc[j] = 0.0f;
@@ -453,6 +494,42 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 if (lane == 0) mbar_arrive_remote(cempty_leader0 + 8 * buf);
             }
             if (!ok || *abort_flag) break;
+            if (w.parts > 1) {
+                // tail split: this thread's FP32 sums of the same elements,
+                // lane-contiguous per column (coalesced), one slot per
+                // (tail tile, part, CTA rank, accumulator warp)
+                const int aw = warp - 2;
+                auto slot = [&](int pt) {
+                    return ((w.tail * (w.parts - 1) + pt) * 2 + int(rank)) * Cfg::acc_warps + aw;
+                };
+                if (w.part < w.parts - 1) {
+                    float* dst = p.part_ws + (size_t)slot(w.part) * (kAccCols * 32);
+#pragma unroll
+                    for (int j = 0; j < kAccCols; ++j) dst[j * 32 + lane] = acc[j];
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) st_release_gpu(p.flags + slot(w.part), p.epoch);
+                    continue;                          // the last part writes C
+                }
+                // last part: add the other parts' sums (bounded waits)
+                for (int pt = 0; pt < w.parts - 1 && ok; ++pt) {
+                    const unsigned* f = p.flags + slot(pt);
+                    const uint64_t t0 = global_timer_ns();
+                    while (ld_acquire_gpu(f) != p.epoch) {
+                        __nanosleep(64);
+                        if (global_timer_ns() - t0 > EMU_WAIT_LIMIT_NS) {
+                            record_error(p.err, kDevErrTimeout);
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    const float* src = p.part_ws + (size_t)slot(pt) * (kAccCols * 32);
+#pragma unroll
+                    for (int j = 0; j < kAccCols; ++j) acc[j] += __ldcg(src + j * 32 + lane);
+                }
+                if (!ok) { *abort_flag = 1; break; }
+            }
             // ---- epilogue: C = alpha * acc + beta * C
             int tm, tn;
             tile_pos(tile, p.tiles_m, p.tiles_n, tm, tn);
@@ -552,9 +629,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
 }
 
 template <int MODE, int BN, int FUSED>
-cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
-                            const CUtensorMap& mapC, const TcGemmParams& p, int clusters,
-                            cudaStream_t stream, bool pdl) {
+cudaError_t set_smem_attr() {
     using Cfg = KCfg<MODE, BN, FUSED>;
     static bool attr = false;
     if (!attr) {
@@ -563,6 +638,50 @@ cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
         if (e != cudaSuccess) return e;
         attr = true;
     }
+    return cudaSuccess;
+}
+
+// Clusters of this kernel that can be resident at once (at most sms / 2).
+// The persistent grid never exceeds it, so every cluster runs concurrently:
+// the tail split's last part waits for the other parts, which must not be
+// queued behind it.
+template <int MODE, int BN, int FUSED>
+int max_clusters_t(int sms) {
+    using Cfg = KCfg<MODE, BN, FUSED>;
+    static int cached = -1;
+    if (cached < 0) {
+        int n = sms / 2;
+        if (set_smem_attr<MODE, BN, FUSED>() == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * (sms / 2));
+            cfg.blockDim = dim3(threads_k<FUSED>());
+            cfg.dynamicSmemBytes = Cfg::smem;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int m = 0;
+            if (cudaOccupancyMaxActiveClusters(&m, gemm_kblock_kernel<MODE, BN, FUSED>, &cfg) ==
+                    cudaSuccess && m > 0)
+                n = m;
+            else
+                cudaGetLastError();
+        }
+        cached = n;
+    }
+    return cached < sms / 2 ? cached : sms / 2;
+}
+
+template <int MODE, int BN, int FUSED>
+cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
+                            const CUtensorMap& mapC, const TcGemmParams& p, int clusters,
+                            cudaStream_t stream, bool pdl) {
+    using Cfg = KCfg<MODE, BN, FUSED>;
+    cudaError_t e = set_smem_attr<MODE, BN, FUSED>();
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(threads_k<FUSED>());
@@ -582,28 +701,58 @@ cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
 
 }  // namespace
 
+int gemm_kblock_clusters(int mode, int bn, int fused, int sms) {
+    if (fused) return max_clusters_t<kModeBf16x9, 128, 1>(sms);
+    switch (mode) {
+        case kModeTf32x3:
+            return bn == 128 ? max_clusters_t<kModeTf32x3, 128, 0>(sms)
+                             : max_clusters_t<kModeTf32x3, 256, 0>(sms);
+        case kModeBf16x9:
+            return bn == 128 ? max_clusters_t<kModeBf16x9, 128, 0>(sms)
+                             : max_clusters_t<kModeBf16x9, 256, 0>(sms);
+        case kModeBf16x3: return max_clusters_t<kModeBf16x3, 256, 0>(sms);
+        case kModeTf32: return max_clusters_t<kModeTf32, 256, 0>(sms);
+        case kModeTf32x3Oy: return max_clusters_t<kModeTf32x3Oy, 256, 0>(sms);
+        default: return sms / 2;
+    }
+}
+
 cudaError_t launch_gemm_kblock(int mode, int bn, int fused, const CUtensorMap& mapA,
                                const CUtensorMap& mapB, const CUtensorMap& mapC,
                                const TcGemmParams& p, int sms, cudaStream_t stream, bool pdl) {
     const int tiles = p.tiles_m * p.tiles_n;
     if (tiles == 0) return cudaSuccess;
-    const int clusters = tiles < sms / 2 ? tiles : sms / 2;
+    TcGemmParams q = p;
+    const int resident = gemm_kblock_clusters(mode, bn, fused, sms);
+    // a split plan is used only as made for this many clusters: all of a
+    // tail tile's parts then run at once, in the last round of the grid
+    const bool split_ok = q.tail_parts > 1 && q.tail_tiles > 0 && q.tail_tiles <= tiles &&
+                          q.part_ws && q.flags &&
+                          q.units == tiles + q.tail_tiles * (q.tail_parts - 1) &&
+                          q.num_kb >= q.tail_parts && (tiles - q.tail_tiles) % resident == 0 &&
+                          q.tail_tiles * q.tail_parts <= resident;
+    if (!split_ok) {                         // whole tiles only
+        q.units = tiles;
+        q.tail_tiles = 0;
+        q.tail_parts = 1;
+    }
+    const int clusters = q.units < resident ? q.units : resident;
     cudaError_t e;
     if (fused) {
         if (mode != kModeBf16x9 || bn != 128) return cudaErrorInvalidValue;
-        e = launch_kblock_t<kModeBf16x9, 128, 1>(mapA, mapB, mapC, p, clusters, stream, pdl);
+        e = launch_kblock_t<kModeBf16x9, 128, 1>(mapA, mapB, mapC, q, clusters, stream, pdl);
     } else if (mode == kModeTf32x3) {
-        e = bn == 128 ? launch_kblock_t<kModeTf32x3, 128, 0>(mapA, mapB, mapC, p, clusters, stream, pdl)
-                      : launch_kblock_t<kModeTf32x3, 256, 0>(mapA, mapB, mapC, p, clusters, stream, pdl);
+        e = bn == 128 ? launch_kblock_t<kModeTf32x3, 128, 0>(mapA, mapB, mapC, q, clusters, stream, pdl)
+                      : launch_kblock_t<kModeTf32x3, 256, 0>(mapA, mapB, mapC, q, clusters, stream, pdl);
     } else if (mode == kModeBf16x9) {
-        e = bn == 128 ? launch_kblock_t<kModeBf16x9, 128, 0>(mapA, mapB, mapC, p, clusters, stream, pdl)
-                      : launch_kblock_t<kModeBf16x9, 256, 0>(mapA, mapB, mapC, p, clusters, stream, pdl);
+        e = bn == 128 ? launch_kblock_t<kModeBf16x9, 128, 0>(mapA, mapB, mapC, q, clusters, stream, pdl)
+                      : launch_kblock_t<kModeBf16x9, 256, 0>(mapA, mapB, mapC, q, clusters, stream, pdl);
     } else if (mode == kModeBf16x3 && bn == 256) {
-        e = launch_kblock_t<kModeBf16x3, 256, 0>(mapA, mapB, mapC, p, clusters, stream, pdl);
+        e = launch_kblock_t<kModeBf16x3, 256, 0>(mapA, mapB, mapC, q, clusters, stream, pdl);
     } else if (mode == kModeTf32 && bn == 256) {
-        e = launch_kblock_t<kModeTf32, 256, 0>(mapA, mapB, mapC, p, clusters, stream, pdl);
+        e = launch_kblock_t<kModeTf32, 256, 0>(mapA, mapB, mapC, q, clusters, stream, pdl);
     } else if (mode == kModeTf32x3Oy && bn == 256) {
-        e = launch_kblock_t<kModeTf32x3Oy, 256, 0>(mapA, mapB, mapC, p, clusters, stream, pdl);
+        e = launch_kblock_t<kModeTf32x3Oy, 256, 0>(mapA, mapB, mapC, q, clusters, stream, pdl);
     } else {
         return cudaErrorInvalidValue;
     }

@@ -163,7 +163,7 @@ extern "C" emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int
     if (!piece_map(&mapA, wa, tf32, M, K, ldp, pieces, box_k, 128) ||
         !piece_map(&mapB, wb, tf32, N, K, ldp, pieces, box_k, 128))
         return EMU_ERR_CUDA;
-    TcGemmParams p;
+    TcGemmParams p = {};
     p.err = s->err;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
     p.num_kb = (int)((K + box_k - 1) / box_k);

@@ -153,9 +153,11 @@ emu_status_t emu_sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
  * move (and M >= 512), the copies are pipelined with the GEMM: B first, then
  * op(A) and C in row chunks of whole 256-row tiles on a library-owned copy
  * stream, each chunk's GEMM on `stream` as its rows land (B's pieces split
- * once), and C's chunks back on a second library-owned stream; the result is
- * element for element that of one emu_sgemm call.  Host buffers in pinned
- * memory let the copies overlap; pageable ones work too.
+ * once), and C's chunks back on a second library-owned stream.  The result
+ * meets the same accuracy bound as one emu_sgemm call; it is bit for bit the
+ * same unless the split of the GEMM's last wave along K (which depends on the
+ * tile count) differs between the call and its chunks.  Host buffers in
+ * pinned memory let the copies overlap; pageable ones work too.
  */
 emu_status_t emu_sgemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K,
                             float alpha, const float* A, int64_t lda,

@@ -239,8 +239,10 @@ def test_host_entry_point_matches_device_path(emu):
                           (1, 0, 0.0, "fp32_simt")])
 def test_host_entry_pipelined_rows_match_one_call(emu, transA, transB, beta, mode):
     """Large enough for the chunked copy/compute pipeline (row chunks of C on
-    three streams): every element equals the one-call device result, since
-    row chunks of C are computed independently by the same kernels."""
+    three streams): row chunks of C are computed independently by the same
+    kernels, so the result matches the one-call device result -- bit for bit
+    unless the GEMM's tail split (which depends on the tile count) differs
+    between the call and its chunks, and within the accuracy bound always."""
     M, N, K = 8300, 1024, 1024                       # ragged last chunk
     r = W.rng(18 + transA + 2 * transB)
     A = W.normal(r, (K, M) if transA else (M, K))
@@ -249,11 +251,13 @@ def test_host_entry_pipelined_rows_match_one_call(emu, transA, transB, beta, mod
     dev = _run(emu, A, B, transA, transB, alpha=0.75, beta=beta, C0=C0, mode=mode)
     host = emu.emu_sgemm_host(A, B, C0.copy(), transA=transA, transB=transB, alpha=0.75,
                               beta=beta, mode=mode)
-    assert np.array_equal(dev, host)
     mi, ni = W.sample_pairs(M, N, 1024, seed=3)
     Cref, Sabs = oracle.gemm_ref(A, B, transA, transB, 0.75, beta, C0, pairs=(mi, ni))
-    assert checks.error_ratio(host[mi, ni], Cref, Sabs, K, 0.75, beta, C0[mi, ni],
-                              mode=_bound_mode(mode)) <= 1.0
+    for C in (host, dev):
+        assert checks.error_ratio(C[mi, ni], Cref, Sabs, K, 0.75, beta, C0[mi, ni],
+                                  mode=_bound_mode(mode)) <= 1.0
+    # M = 8300 and both chunks (4352 and 3948 rows) leave no tail to split
+    assert np.array_equal(dev, host)
 
 
 def test_host_entry_pipelined_fused_shape(emu):
@@ -266,7 +270,13 @@ def test_host_entry_pipelined_fused_shape(emu):
     B = W.normal(r, (g.N, g.K), std=g.K ** -0.5)
     dev = _run(emu, A, B, transB=True)
     host = emu.emu_sgemm_host(A, B, transB=True)
-    assert np.array_equal(dev, host)
+    # the one call splits its last wave along K, the two chunks do not: the
+    # results agree within the accuracy bound, element by element
+    mi, ni = W.sample_pairs(M, g.N, 2048, seed=4)
+    Cref, Sabs = oracle.gemm_ref(A, B, transB=True, pairs=(mi, ni))
+    for C in (host, dev):
+        assert checks.error_ratio(C[mi, ni], Cref, Sabs, g.K, 1.0, 0.0) <= 1.0
+    assert np.allclose(host, dev, rtol=0, atol=4e-5 * float(np.abs(dev).max()))
 
 
 def test_bounded_wait_reports_timeout_and_context_survives(emu):
