@@ -378,3 +378,28 @@ def test_subnormal_operands_through_the_tensor_core(emu, mode):
         assert np.array_equal(C.view(np.uint32), emul(X, Y).view(np.uint32))
         if mode in ("bf16x9", "fp32_simt"):
             assert np.array_equal(C.view(np.uint32), u)
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 4096), (1024, 1024, 1024), (300, 513, 1000),
+                                   (4096, 4096, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3", "bf16x3"])
+def test_tail_split_shapes(emu, shape, mode):
+    """Shapes whose last round of tiles is split along K (1 tile in 8 parts,
+    16 tiles in 4, 6 tiles in 8, 28 of 256 tiles in 2): within the bound,
+    every element where the oracle is fast enough, and the same bits on a
+    second call (the reduction order is fixed)."""
+    M, N, K = shape
+    r = W.rng(M + 3 * N + 7 * K)
+    A, B = W.normal(r, (M, K)), W.normal(r, (K, N))
+    C1 = _run(emu, A, B, mode=mode)
+    C2 = _run(emu, A, B, mode=mode)
+    assert np.array_equal(C1, C2)
+    bm = mode if mode in ("tf32x3", "bf16x3") else "bf16x9"
+    if M * N * K <= (1 << 30):
+        Cref, Sabs = oracle.gemm_ref(A, B)
+        assert checks.error_ratio(C1, Cref, Sabs, K, 1.0, 0.0, mode=bm) <= 1.0
+    else:
+        mi, ni = W.sample_pairs(M, N, 2048, seed=8)
+        Cref, Sabs = oracle.gemm_ref(A, B, pairs=(mi, ni))
+        assert checks.error_ratio(C1[mi, ni], Cref, Sabs, K, 1.0, 0.0, mode=bm) <= 1.0
