@@ -268,6 +268,39 @@ __device__ __forceinline__ void split_bf16x3(float x, uint16_t& h0, uint16_t& h1
     h2 = bf16_rn_sat(s2);
 }
 
+// Two neighbouring elements at once: the same pieces as split_bf16x3, packed
+// as BF16 pairs (element a in the low half, b in the high half), with one
+// cvt.rn.satfinite.bf16x2.f32 per piece instead of two conversions and a
+// pack.  satfinite turns a finite value whose nearest BF16 is infinite into
+// the largest finite BF16, which is its truncation (the R2 rule); pairs
+// holding an infinity or a NaN take the scalar path.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float hi, float lo) {
+    uint32_t d;
+    asm("cvt.rn.satfinite.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ void split_bf16x3_pair(float a, float b, uint32_t& p0, uint32_t& p1,
+                                                  uint32_t& p2) {
+    const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+    if (((ua & 0x7F800000u) == 0x7F800000u) || ((ub & 0x7F800000u) == 0x7F800000u)) {
+        uint16_t a0, a1, a2, b0, b1, b2;
+        split_bf16x3(a, a0, a1, a2);
+        split_bf16x3(b, b0, b1, b2);
+        p0 = uint32_t(a0) | (uint32_t(b0) << 16);
+        p1 = uint32_t(a1) | (uint32_t(b1) << 16);
+        p2 = uint32_t(a2) | (uint32_t(b2) << 16);
+        return;
+    }
+    p0 = cvt_bf16x2(b, a);
+    const float sa1 = __fmul_rn(__fsub_rn(a, __uint_as_float(p0 << 16)), 256.0f);
+    const float sb1 = __fmul_rn(__fsub_rn(b, __uint_as_float(p0 & 0xFFFF0000u)), 256.0f);
+    p1 = cvt_bf16x2(sb1, sa1);
+    const float sa2 = __fmul_rn(__fsub_rn(sa1, __uint_as_float(p1 << 16)), 256.0f);
+    const float sb2 = __fmul_rn(__fsub_rn(sb1, __uint_as_float(p1 & 0xFFFF0000u)), 256.0f);
+    p2 = cvt_bf16x2(sb2, sa2);
+}
+
 // Nearest TF32 (10 explicit mantissa bits, ties to even) kept in an FP32
 // container with the low 13 bits zero; overflow to inf is replaced by the
 // truncated value.  Integer rounding on the bit pattern.

@@ -181,10 +181,6 @@ __device__ __forceinline__ void mma_pair(uint32_t d, uint32_t a_tile, uint32_t b
     }
 }
 
-__device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) {
-    return uint32_t(lo) | (uint32_t(hi) << 16);
-}
-
 // Split this thread's share of a 128 x 64 FP32 A block (two swizzled 128 x
 // 32 boxes at `a32`) into the three BF16 pieces at `pieces` (three 128 x 64
 // swizzled tiles, 16 KB apart).  Split warp w (0..15) takes rows 8w..8w+7;
@@ -202,18 +198,16 @@ __device__ __forceinline__ void split_block(const uint8_t* a32, uint8_t* pieces,
             const int c4 = (part & 1) * 4 + 2 * half;      // first float4 chunk of these 8
             const float4 x0 = *reinterpret_cast<const float4*>(box + ((c4 ^ sw) << 4));
             const float4 x1 = *reinterpret_cast<const float4*>(box + (((c4 + 1) ^ sw) << 4));
-            const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            uint16_t h0[8], h1[8], h2[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) split_bf16x3(v[i], h0[i], h1[i], h2[i]);
+            uint4 o0, o1, o2;
+            split_bf16x3_pair(x0.x, x0.y, o0.x, o1.x, o2.x);
+            split_bf16x3_pair(x0.z, x0.w, o0.y, o1.y, o2.y);
+            split_bf16x3_pair(x1.x, x1.y, o0.z, o1.z, o2.z);
+            split_bf16x3_pair(x1.z, x1.w, o0.w, o1.w, o2.w);
             const int c8 = part * 2 + half;                // 16-byte chunk of 8 BF16
             const int off = r * 128 + ((c8 ^ sw) << 4);
-            *reinterpret_cast<uint4*>(pieces + off) =
-                make_uint4(pack2(h0[0], h0[1]), pack2(h0[2], h0[3]), pack2(h0[4], h0[5]), pack2(h0[6], h0[7]));
-            *reinterpret_cast<uint4*>(pieces + kATile + off) =
-                make_uint4(pack2(h1[0], h1[1]), pack2(h1[2], h1[3]), pack2(h1[4], h1[5]), pack2(h1[6], h1[7]));
-            *reinterpret_cast<uint4*>(pieces + 2 * kATile + off) =
-                make_uint4(pack2(h2[0], h2[1]), pack2(h2[2], h2[3]), pack2(h2[4], h2[5]), pack2(h2[6], h2[7]));
+            *reinterpret_cast<uint4*>(pieces + off) = o0;
+            *reinterpret_cast<uint4*>(pieces + kATile + off) = o1;
+            *reinterpret_cast<uint4*>(pieces + 2 * kATile + off) = o2;
         }
     }
 }

@@ -35,17 +35,11 @@ __global__ void __launch_bounds__(256) split3_rows_vec8(const float* __restrict_
         const float4* src = reinterpret_cast<const float4*>(X + r * ld + c);
         const float4 a = __ldcs(src);
         const float4 b = __ldcs(src + 1);
-        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        uint16_t h0[8], h1[8], h2[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) split_bf16x3(v[i], h0[i], h1[i], h2[i]);
         uint4 o0, o1, o2;
-        o0.x = h0[0] | (uint32_t(h0[1]) << 16); o0.y = h0[2] | (uint32_t(h0[3]) << 16);
-        o0.z = h0[4] | (uint32_t(h0[5]) << 16); o0.w = h0[6] | (uint32_t(h0[7]) << 16);
-        o1.x = h1[0] | (uint32_t(h1[1]) << 16); o1.y = h1[2] | (uint32_t(h1[3]) << 16);
-        o1.z = h1[4] | (uint32_t(h1[5]) << 16); o1.w = h1[6] | (uint32_t(h1[7]) << 16);
-        o2.x = h2[0] | (uint32_t(h2[1]) << 16); o2.y = h2[2] | (uint32_t(h2[3]) << 16);
-        o2.z = h2[4] | (uint32_t(h2[5]) << 16); o2.w = h2[6] | (uint32_t(h2[7]) << 16);
+        split_bf16x3_pair(a.x, a.y, o0.x, o1.x, o2.x);
+        split_bf16x3_pair(a.z, a.w, o0.y, o1.y, o2.y);
+        split_bf16x3_pair(b.x, b.y, o0.z, o1.z, o2.z);
+        split_bf16x3_pair(b.z, b.w, o0.w, o1.w, o2.w);
         const int64_t o = r * ldp + c;
         *reinterpret_cast<uint4*>(P0 + o) = o0;
         *reinterpret_cast<uint4*>(P1 + o) = o1;
@@ -190,22 +184,19 @@ __global__ void __launch_bounds__(256) split3_transposed_vec(const float* __rest
     }
     __syncthreads();
     const int rr = tid >> 2, cp = tid & 3;           // op row in tile, 16-element part
-    uint16_t h0[16], h1[16], h2[16];
+    uint32_t w0[8], w1[8], w2[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) split_bf16x3(tile[16 * cp + i][rr], h0[i], h1[i], h2[i]);
+    for (int i = 0; i < 8; ++i)
+        split_bf16x3_pair(tile[16 * cp + 2 * i][rr], tile[16 * cp + 2 * i + 1][rr], w0[i], w1[i], w2[i]);
     const int64_t o = (r0 + rr) * ldp + c0 + 16 * cp;
     uint4* d0 = reinterpret_cast<uint4*>(P0 + o);
     uint4* d1 = reinterpret_cast<uint4*>(P1 + o);
     uint4* d2 = reinterpret_cast<uint4*>(P2 + o);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-        const int b = 8 * q;
-        d0[q] = make_uint4(h0[b] | (uint32_t(h0[b + 1]) << 16), h0[b + 2] | (uint32_t(h0[b + 3]) << 16),
-                           h0[b + 4] | (uint32_t(h0[b + 5]) << 16), h0[b + 6] | (uint32_t(h0[b + 7]) << 16));
-        d1[q] = make_uint4(h1[b] | (uint32_t(h1[b + 1]) << 16), h1[b + 2] | (uint32_t(h1[b + 3]) << 16),
-                           h1[b + 4] | (uint32_t(h1[b + 5]) << 16), h1[b + 6] | (uint32_t(h1[b + 7]) << 16));
-        if (P2) d2[q] = make_uint4(h2[b] | (uint32_t(h2[b + 1]) << 16), h2[b + 2] | (uint32_t(h2[b + 3]) << 16),
-                           h2[b + 4] | (uint32_t(h2[b + 5]) << 16), h2[b + 6] | (uint32_t(h2[b + 7]) << 16));
+        d0[q] = make_uint4(w0[4 * q], w0[4 * q + 1], w0[4 * q + 2], w0[4 * q + 3]);
+        d1[q] = make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
+        if (P2) d2[q] = make_uint4(w2[4 * q], w2[4 * q + 1], w2[4 * q + 2], w2[4 * q + 3]);
     }
     griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
