@@ -464,6 +464,21 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             const Unit w = unit_at(p, u);
             const int nparts = (w.kb1 - w.kb0 + KBP - 1) / KBP;   // TMEM partials of this unit
             const int tile = w.tile;
+            if (p.beta != 0.0f && w.part == w.parts - 1) {
+                // the epilogue will read this thread's row of C: start it on
+                // its way to L2 now, while the tensor core works
+                int tm_, tn_;
+                tile_pos(tile, p.tiles_m, p.tiles_n, tm_, tn_);
+                const int prow = tm_ * kBM + int(rank) * kHalfRows + q * 32 + lane;
+                const int pcol = tn_ * BN + h * kAccCols;
+                if (prow < p.M) {
+#pragma unroll
+                    for (int c = 0; c < kAccCols; c += 32)
+                        if (pcol + c < p.N)
+                            asm volatile("prefetch.global.L2 [%0];"
+                                         :: "l"(p.C + (int64_t)prow * p.ldc + pcol + c));
+                }
+            }
             float acc[kAccCols];
 #pragma unroll
             for (int j = 0; j < kAccCols; ++j) acc[j] = 0.0f;

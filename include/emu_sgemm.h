@@ -128,6 +128,11 @@ typedef enum {
  * FP32; C is not read when beta == 0, and A, B are not read when alpha == 0
  * or K == 0 (BLAS convention).  M == 0 or N == 0 is a no-op.
  *
+ * Non-finite inputs: the split keeps +-inf as (x, +0, +0) and NaN as NaN
+ * pieces, so an output that meets an infinity is usually NaN (products such
+ * as inf * 0 with a zero residual piece), where an IEEE FP32 dot product
+ * would give +-inf; outputs that meet no infinity or NaN are unaffected.
+ *
  * Accuracy: for BF16X9 every element satisfies
  *     |C - C_exact| <= (2K + 2) 2^-24 |alpha| sum_k |a_mk||b_kn| + 2^-23 |beta C|
  * (TF32X3 and TF32X3_OY add 2^-20 |alpha| sum_k |a_mk||b_kn|, BF16X3 2^-16 and TF32

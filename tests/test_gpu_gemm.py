@@ -403,3 +403,32 @@ def test_tail_split_shapes(emu, shape, mode):
         mi, ni = W.sample_pairs(M, N, 2048, seed=8)
         Cref, Sabs = oracle.gemm_ref(A, B, pairs=(mi, ni))
         assert checks.error_ratio(C1[mi, ni], Cref, Sabs, K, 1.0, 0.0, mode=bm) <= 1.0
+
+
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_non_finite_operands_follow_the_split(emu, mode):
+    """Infinities and NaNs: the split keeps +-inf as (x, +0, +0) and NaN as NaN
+    pieces, so an output that meets an infinity is formed from products such
+    as inf * 0 and inf * (opposite-signed residual): it comes out NaN or
+    +-inf exactly as the oracle's emulation of the same method says, which is
+    not always what a plain FP32 dot product gives (the emulation is not
+    IEEE-754 arithmetic).  The outputs that meet no special value stay
+    within the bound."""
+    r = W.rng(91)
+    A, B = W.normal(r, (70, 64)), W.normal(r, (64, 90))
+    A[3, 5], A[10, 7], A[11, 7] = np.inf, -np.inf, 1.0       # row 11 finite except a clean 1.0
+    A[20, 9] = np.nan
+    B[5, 20], B[30, 40], B[7, 60] = np.nan, np.inf, 0.0
+    C = _run(emu, A, B, mode=mode)
+    emul = {"bf16x9": oracle.gemm_bf16x9, "tf32x3": oracle.gemm_tf32x3}[mode](A, B)
+    assert np.array_equal(np.isnan(C), np.isnan(emul))
+    assert np.array_equal(np.isposinf(C), np.isposinf(emul))
+    assert np.array_equal(np.isneginf(C), np.isneginf(emul))
+    fin = np.isfinite(emul)
+    assert fin.sum() > 0.9 * fin.size
+    Af, Bf = np.nan_to_num(A, nan=0.0, posinf=0.0, neginf=0.0), np.nan_to_num(B, nan=0.0, posinf=0.0, neginf=0.0)
+    Cref, Sabs = oracle.gemm_ref(Af, Bf)
+    clean_rows = np.all(np.isfinite(A), axis=1)
+    clean_cols = np.all(np.isfinite(B), axis=0)
+    m = np.outer(clean_rows, clean_cols)
+    assert checks.error_ratio(C[m], Cref[m], Sabs[m], 64, 1.0, 0.0, mode=mode) <= 1.0
