@@ -60,10 +60,14 @@ double predict_tc_us(int64_t M, int64_t N, int64_t K, int mode, int sms) {
     const TcFit f = tc_fit(mode);
     const int pieces = mode_pieces(mode), esz = mode_piece_bytes(mode);
     const double split_mb = double(M + N) * double(K) * (4.0 + pieces * esz) * 1e-6;
-    const int64_t tiles = cdiv(M, 256) * cdiv(N, 256);
+    // N <= 128 runs 128-wide tiles (BF16x9, TF32x3): half the MMA work each
+    const bool narrow = N <= 128 && (mode == kModeBf16x9 || mode == kModeTf32x3);
+    const int64_t bn = narrow ? 128 : 256;
+    const int64_t tiles = cdiv(M, 256) * cdiv(N, bn);
     const int64_t waves = cdiv(tiles, sms / 2 > 0 ? sms / 2 : 1);
     const int64_t kb = cdiv(K, mode_is_tf32(mode) ? 32 : 64);
-    return f.fixed_us + split_mb * f.us_per_mb + double(waves) * (f.wave_us + double(kb) * f.block_us);
+    const double block = f.block_us * (narrow ? 0.5 : 1.0);
+    return f.fixed_us + split_mb * f.us_per_mb + double(waves) * (f.wave_us + double(kb) * block);
 }
 
 double predict_simt_us(int64_t M, int64_t N, int64_t K, int sms) {

@@ -103,15 +103,16 @@ emu_status_t from_cuda(cudaError_t e) {
     return EMU_ERR_CUDA;
 }
 
-// Tile width of the K-block kernel on the two-pass path: 256 (default) or
-// 128 (EMU_SGEMM_BN=128).
-int kblock_bn() {
-    static int v = 0;
-    if (v == 0) {
+// Tile width of the K-block kernel on the two-pass path: 128 when N <= 128
+// (a 256-wide tile would compute at least half zeros), else 256;
+// EMU_SGEMM_BN=128 or 256 fixes it.
+int kblock_bn(int64_t N) {
+    static int v = -1;
+    if (v < 0) {
         const char* s = std::getenv("EMU_SGEMM_BN");
-        v = (s && std::strcmp(s, "128") == 0) ? 128 : 256;
+        v = !s ? 0 : (std::strcmp(s, "128") == 0 ? 128 : (std::strcmp(s, "256") == 0 ? 256 : 0));
     }
-    return v;
+    return v ? v : (N <= 128 ? 128 : 256);
 }
 
 int read_strategy_env() {
@@ -324,7 +325,7 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
 
     const int box_cols = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
     // the two cheaper modes are built for 256-wide tiles only
-    const int bn = (mode == kModeBf16x9 || mode == kModeTf32x3) ? kblock_bn() : 256;
+    const int bn = (mode == kModeBf16x9 || mode == kModeTf32x3) ? kblock_bn(N) : 256;
     CUtensorMap mapA, mapB;
     st = make_plane_map(&mapA, wa, tf32, M, K, ldp, planes, box_cols, 128);
     if (st != EMU_OK) return st;
