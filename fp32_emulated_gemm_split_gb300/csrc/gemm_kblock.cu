@@ -536,6 +536,10 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     const float* src = p.part_ws + (size_t)slot(pt) * (kAccCols * 32);
 #pragma unroll
                     for (int j = 0; j < kAccCols; ++j) acc[j] += __ldcg(src + j * 32 + lane);
+                    // consumed: clear the flag, so that a replay of the same
+                    // launch (a CUDA graph bakes the epoch in) waits afresh
+                    __syncwarp();
+                    if (lane == 0) *const_cast<volatile unsigned*>(f) = 0u;
                 }
                 if (!ok) { *abort_flag = 1; break; }
             }

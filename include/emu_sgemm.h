@@ -139,6 +139,12 @@ typedef enum {
  * 2^-10 + 2^-21), where C_exact is the result in exact arithmetic.
  *
  * Returns EMU_OK once the kernels are enqueued on `stream`.
+ *
+ * CUDA graphs: a call can be captured on `stream` once a call of the same
+ * shape and mode (or one needing at least as much workspace) has run on the
+ * device outside capture -- the library sizes its buffers with cudaMalloc,
+ * which a capture does not allow.  Replays reuse the captured workspace and
+ * must not overlap one another or other calls on the GPU.
  */
 emu_status_t emu_sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
                        float alpha, const float* A, int64_t lda,

@@ -1,0 +1,51 @@
+"""emu_sgemm inside a CUDA graph: after one call outside capture (which
+sizes the library's buffers), a captured call replays with fresh operand
+values and gives, bit for bit, what a direct call gives -- including shapes
+whose last round of tiles is split along K, whose flags must not leak from
+one replay into the next."""
+import pytest
+
+from gpu_util import emu_module
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def emu():
+    m = emu_module()
+    yield m
+    m.emu_set_path("auto")
+
+
+@pytest.mark.parametrize("shape,path", [((4096, 4096, 512), "twopass"),
+                                        ((256, 256, 4096), "twopass"),
+                                        ((70000, 256, 256), "fused"),
+                                        ((1000, 700, 300), "auto")],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else v)
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_graph_replay_matches_direct_calls(emu, shape, path, mode):
+    import torch
+    if path == "fused" and mode != "bf16x9":
+        pytest.skip("the fused path is BF16x9 only")
+    M, N, K = shape
+    emu.emu_set_path(path)
+    g = torch.Generator(device="cuda").manual_seed(M + N + K)
+    A = torch.randn((M, K), device="cuda", generator=g)
+    B = torch.randn((K, N), device="cuda", generator=g)
+    C = torch.empty((M, N), device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        emu.emu_sgemm(A, B, C, mode=mode, stream=s)          # buffers sized outside capture
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            emu.emu_sgemm(A, B, C, mode=mode, stream=s)
+    for _ in range(3):
+        A.copy_(torch.randn((M, K), device="cuda", generator=g))
+        B.copy_(torch.randn((K, N), device="cuda", generator=g))
+        graph.replay()
+        torch.cuda.synchronize()
+        direct = emu.emu_sgemm(A, B, mode=mode)
+        torch.cuda.synchronize()
+        assert torch.equal(C, direct)
+    assert emu.emu_get_last_device_error() == 0
