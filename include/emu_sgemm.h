@@ -144,7 +144,10 @@ typedef enum {
  * shape and mode (or one needing at least as much workspace) has run on the
  * device outside capture -- the library sizes its buffers with cudaMalloc,
  * which a capture does not allow.  Replays reuse the captured workspace and
- * must not overlap one another or other calls on the GPU.
+ * must not overlap one another or other calls on the GPU.  A later call that
+ * needs more workspace than any before it reallocates it, which invalidates
+ * graphs captured earlier: capture after the largest call has run (or
+ * re-capture).
  */
 emu_status_t emu_sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
                        float alpha, const float* A, int64_t lda,
