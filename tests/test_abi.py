@@ -100,3 +100,32 @@ def test_profile_read_rejects_bad_kind(emu):
     n = ctypes.c_int64()
     ms = ctypes.c_double()
     assert emu.lib().emu_profile_read(9, ctypes.byref(n), ctypes.byref(ms)) == -1
+
+
+def _build_c_client(tmp_path):
+    import subprocess
+    from fp32_emulated_gemm_split_gb300 import _build
+    lib = _build.LIB_PATH
+    libdir = os.path.dirname(lib)
+    name = os.path.basename(lib)
+    exe = str(tmp_path / "c_client")
+    # link the library by its file name (it carries the machine in its name)
+    cmd = ["gcc", "-std=c11", "-O2", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c_client.c"), "-o", exe,
+           "-L" + libdir, "-l:" + name, "-Wl,-rpath," + libdir, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    return exe
+
+
+def test_c_client_compiles_and_links_against_the_header_and_library(emu, tmp_path):
+    """The header is plain C and every entry point the client uses links."""
+    assert os.path.exists(_build_c_client(tmp_path))
+
+
+@pytest.mark.gpu
+def test_c_client_runs(emu, tmp_path):
+    import subprocess
+    exe = _build_c_client(tmp_path)
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.startswith("ok ")
