@@ -226,6 +226,37 @@ __device__ __forceinline__ void mma_cta2_scaled(uint32_t d, uint64_t a, uint64_t
     }
 }
 
+// The same with the A operand in tensor memory: `a` is the TMEM address of
+// the first 32-bit column of this K step's A (rows = lanes, two 16-bit
+// elements per column).
+__device__ __forceinline__ void mma_cta2_ta(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+                 :: "r"(d), "r"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+template <int SHIFT>
+__device__ __forceinline__ void mma_cta2_ta_scaled(uint32_t d, uint32_t a, uint64_t b,
+                                                   uint32_t idesc) {
+    static_assert(SHIFT >= 1 && SHIFT <= 15, "scale-input-d takes 0..15");
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, 1, 0;\n"
+                 " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p, %4;\n}\n"
+                 :: "r"(d), "r"(a), "l"(b), "r"(idesc), "n"(SHIFT) : "memory");
+}
+
+// Store 8 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+           "r"(r[6]), "r"(r[7]) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Arrive on the barrier at this offset in both CTAs of the pair once the
 // MMAs issued so far have completed.
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {

@@ -81,7 +81,9 @@ struct KCfg {
     static constexpr int pieces = mode_pieces(MODE);
     static constexpr int b_rows = BN / 2;                        // B^T rows per CTA
     static constexpr int b_tile = b_rows * kTcBKBytes;
-    static constexpr int stage_bytes = pieces * (kATile + b_tile);
+    // fused: only B's pieces are staged in shared memory; A's go to tensor
+    // memory (a_tm_stages rings of 96 columns after the accumulators)
+    static constexpr int stage_bytes = pieces * ((FUSED ? 0 : kATile) + b_tile);
     static constexpr int a32_bytes = FUSED ? kA32Bufs * kA32Buf : 0;
     // epilogue staging for bulk tensor stores: 32 rows x 16 FP32 per
     // accumulator warp (2 KB)
@@ -105,7 +107,11 @@ struct KCfg {
         MODE == kModeTf32x3 || band_major ? 2 : MODE == kModeTf32 ? 8 : 1;
     // TMEM partial buffers of BN columns each (all 512 columns): 2 at BN = 256,
     // 4 at BN = 128, so the tensor core can run further ahead of the epilogue.
-    static constexpr int nbuf = 512 / BN;
+    static constexpr int nbuf = FUSED ? 2 : 512 / BN;
+    static constexpr int a_tm_stages = FUSED ? 2 : 0;
+    static constexpr int a_tm_cols = 3 * (kTcBKBytes / 4);            // 3 pieces x 32 columns
+    static constexpr int a_tm_base = nbuf * BN;
+    static_assert(a_tm_base + a_tm_stages * a_tm_cols <= 512, "tensor memory overflow");
     static constexpr int acc_warps = ::emu::acc_warps<FUSED>();
     static constexpr int acc_cols = BN / (acc_warps / 4);         // columns per accumulator thread
     static constexpr uint32_t tmem_cols = 512;
@@ -181,35 +187,42 @@ __device__ __forceinline__ void mma_pair(uint32_t d, uint32_t a_tile, uint32_t b
     }
 }
 
-// Split this thread's share of a 128 x 64 FP32 A block (two swizzled 128 x
-// 32 boxes at `a32`) into the three BF16 pieces at `pieces` (three 128 x 64
-// swizzled tiles, 16 KB apart).  Split warp w (0..15) takes rows 8w..8w+7;
-// lane l takes row 8w + l%8 and elements 16(l/8) .. +15.  The 8 lanes of a
-// quarter-warp read and write the same logical 16-byte chunk of 8
-// consecutive rows, which the 128-byte swizzle spreads over 8 distinct bank
-// groups, so the shared-memory accesses are conflict-free.
-__device__ __forceinline__ void split_block(const uint8_t* a32, uint8_t* pieces, int w, int lane) {
-    const int part = lane >> 3;                            // 16-element part of the 64
-    {
-        const int r = 8 * w + (lane & 7), sw = r & 7;
-        const uint8_t* box = a32 + (part >> 1) * kA32Box + r * 128;
+// The same with A in tensor memory (fused path): `a_tm` is the first column
+// of the piece's 64-element K block (32 columns, K=16 step = 8 columns).
+__device__ __forceinline__ void mma_pair_ta(uint32_t d, uint32_t a_tm, uint32_t b_tile,
+                                            uint32_t idesc, bool first, bool shift) {
+    const uint64_t bdesc = make_sw128_kmajor_desc(b_tile);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int c4 = (part & 1) * 4 + 2 * half;      // first float4 chunk of these 8
-            const float4 x0 = *reinterpret_cast<const float4*>(box + ((c4 ^ sw) << 4));
-            const float4 x1 = *reinterpret_cast<const float4*>(box + (((c4 + 1) ^ sw) << 4));
-            uint4 o0, o1, o2;
-            split_bf16x3_pair(x0.x, x0.y, o0.x, o1.x, o2.x);
-            split_bf16x3_pair(x0.z, x0.w, o0.y, o1.y, o2.y);
-            split_bf16x3_pair(x1.x, x1.y, o0.z, o1.z, o2.z);
-            split_bf16x3_pair(x1.z, x1.w, o0.w, o1.w, o2.w);
-            const int c8 = part * 2 + half;                // 16-byte chunk of 8 BF16
-            const int off = r * 128 + ((c8 ^ sw) << 4);
-            *reinterpret_cast<uint4*>(pieces + off) = o0;
-            *reinterpret_cast<uint4*>(pieces + kATile + off) = o1;
-            *reinterpret_cast<uint4*>(pieces + 2 * kATile + off) = o2;
-        }
+    for (int k = 0; k < 4; ++k) {
+        const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
+        if (k == 0 && shift)
+            mma_cta2_ta_scaled<8>(d, a_tm + 8 * k, bdesc + koff, idesc);
+        else
+            mma_cta2_ta(d, a_tm + 8 * k, bdesc + koff, idesc, (k == 0 && first) ? 0u : 1u);
     }
+}
+
+// Split this thread's share of a 128 x 64 FP32 A block (two swizzled 128 x
+// 32 boxes at `a32`) into the three BF16 pieces and store them to tensor
+// memory at column `col` (piece i at col + 32 i; BF16 pairs, two elements
+// per 32-bit column, rows = lanes).  A warp reaches only its own 32 lanes
+// (warp % 4), so row r = 32 (warp % 4) + lane, and the four split warps of a
+// lane quadrant take elements 16 kpart .. +15.  The 32 lanes read the same
+// logical 16-byte chunk of 32 consecutive rows, which the 128-byte swizzle
+// spreads over 8 distinct bank groups per 8 rows: conflict-free.
+__device__ __forceinline__ void split_block_tm(const uint8_t* a32, uint32_t col, int r, int kpart) {
+    const uint8_t* row = a32 + (kpart >> 1) * kA32Box + r * 128;
+    uint32_t w0[8], w1[8], w2[8];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int c4 = (kpart & 1) * 4 + c;
+        const float4 x = *reinterpret_cast<const float4*>(row + ((c4 ^ (r & 7)) << 4));
+        split_bf16x3_pair(x.x, x.y, w0[2 * c], w1[2 * c], w2[2 * c]);
+        split_bf16x3_pair(x.z, x.w, w0[2 * c + 1], w1[2 * c + 1], w2[2 * c + 1]);
+    }
+    tmem_st_32x32b_x8(col, w0);
+    tmem_st_32x32b_x8(col + 32, w1);
+    tmem_st_32x32b_x8(col + 64, w2);
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -253,7 +266,10 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     const uint32_t aready0 = cempty0 + 8 * NB;
     const uint32_t afull0 = aready0 + 8 * S;
     const uint32_t afree0 = afull0 + 8 * kA32Bufs;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nb_full + 2 * S + 2 * NB + 2 * kA32Bufs);
+    // fused: 2 tensor-memory A stages free (each CTA, arrived by the MMA commit)
+    const uint32_t atfree0 = afree0 + 8 * kA32Bufs;
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(bars + nb_full + 2 * S + 2 * NB + 2 * kA32Bufs + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -269,7 +285,9 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             mbar_init(cempty0 + 8 * b, 2 * Cfg::acc_warps);   // accumulator warps of both CTAs
         }
         if (FUSED) {
-            for (int s = 0; s < S; ++s) mbar_init(aready0 + 8 * s, 2);   // one per CTA
+            // A pieces of tensor-memory stage t written (leader; one per CTA)
+            for (int t = 0; t < Cfg::a_tm_stages; ++t) mbar_init(aready0 + 8 * t, 2);
+            for (int t = 0; t < Cfg::a_tm_stages; ++t) mbar_init(atfree0 + 8 * t, 1);
             for (int f = 0; f < kA32Bufs; ++f) {
                 mbar_init(afull0 + 8 * f, 1);
                 mbar_init(afree0 + 8 * f, 1);
@@ -330,7 +348,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     const uint32_t fbl = full_leader0 + 8 * (s * P + pc);
                     if (!FUSED)
                         tma_load_3d_pair(st + pc * kATile, &mapA, fbl, kb * Cfg::elems, arow, pc);
-                    tma_load_3d_pair(st + P * kATile + pc * Cfg::b_tile, &mapB, fbl,
+                    tma_load_3d_pair(st + P * (FUSED ? 0 : kATile) + pc * Cfg::b_tile, &mapB, fbl,
                                      kb * Cfg::elems, brow, pc);
                 }
             }
@@ -354,21 +372,46 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     ok = false;
                     break;
                 }
-                if (FUSED && !mbar_wait(aready0 + 8 * s, ph, p.err, kDevErrTimeout)) {
-                    ok = false;
-                    break;
+                // fused: A's pieces of this block in tensor-memory stage t
+                const uint32_t t = FUSED ? kbg % Cfg::a_tm_stages : 0;
+                const uint32_t tph = FUSED ? (kbg / Cfg::a_tm_stages) & 1 : 0;
+                if (FUSED) {
+                    if (!mbar_wait(aready0 + 8 * t, tph, p.err, kDevErrTimeout)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                 }
                 const uint32_t d = tmem + buf * BN;
                 const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
-                auto A = [&](int i) { return st + i * kATile; };
-                auto B = [&](int j) { return st + P * kATile + j * Cfg::b_tile; };
+                constexpr int a_smem = FUSED ? 0 : kATile;
+                auto A = [&](int i) { return st + i * a_smem; };
+                auto B = [&](int j) { return st + P * a_smem + j * Cfg::b_tile; };
+                const uint32_t a_tm0 = tmem + Cfg::a_tm_base + t * Cfg::a_tm_cols;
                 auto ready = [&](int pc) {
                     const bool r = mbar_wait(full0 + 8 * (s * P + pc), ph, p.err, kDevErrTimeout) &&
                                    !*abort_flag;
                     tc_fence_after();
                     return r;
                 };
-                if constexpr (MODE == kModeBf16x9) {
+                if constexpr (FUSED) {
+                    // A pieces from tensor memory, 32 columns apart
+                    auto pr = [&](int i, int j, bool first, bool shift) {
+                        mma_pair_ta(d, a_tm0 + 32 * i, B(j), idesc, first, shift);
+                    };
+                    if (!ready(2)) { ok = false; break; }
+                    pr(2, 2, true, false);                                    // band 4
+                    if (!ready(1)) { ok = false; break; }
+                    pr(1, 2, false, true);                                    // band 3
+                    pr(2, 1, false, false);
+                    if (!ready(0)) { ok = false; break; }
+                    pr(0, 2, false, true);                                    // band 2
+                    pr(1, 1, false, false);
+                    pr(2, 0, false, false);
+                    pr(0, 1, false, true);                                    // band 1
+                    pr(1, 0, false, false);
+                    pr(0, 0, false, true);                                    // band 0
+                } else if constexpr (MODE == kModeBf16x9) {
                     if (!ready(2)) { ok = false; break; }
                     mma_pair<0>(d, A(2), B(2), idesc, true, false);           // band 4
                     if (!ready(1)) { ok = false; break; }
@@ -411,6 +454,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     mma_pair<1>(d, A(0), B(0), idesc, fresh, false);          // hi*hi
                 }
                 tc_commit_pair(empty0 + 8 * s);
+                if (FUSED) tc_commit_pair(atfree0 + 8 * t);    // tensor-memory A stage free
                 if (close) {
                     tc_commit_pair(cfull0 + 8 * buf);
                     ++part;
@@ -423,6 +467,9 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         // Split every K block of this cluster's tiles, as soon as its FP32
         // block has landed and its stage is free, ahead of the tensor core.
         const int w = warp - 2 - Cfg::acc_warps;
+        const int kpart = w >> 2;                      // 16-element part of the 64
+        const int r = 32 * (warp & 3) + lane;          // row: this warp's TMEM lanes
+        const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const uint32_t aready_leader0 = map_to_rank(aready0, 0);
         uint32_t my_blocks = 0;
         for (int u = cluster_id; u < p.units; u += num_clusters) {
@@ -431,13 +478,17 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         for (uint32_t g = 0; g < my_blocks; ++g) {
             const uint32_t f = g % kA32Bufs, fph = (g / kA32Bufs) & 1;
-            const uint32_t s = g % S, ph = (g / S) & 1;
+            const uint32_t t = g % Cfg::a_tm_stages, tph = (g / Cfg::a_tm_stages) & 1;
             const bool ok = mbar_wait(afull0 + 8 * f, fph, p.err, kDevErrTimeout) &&
-                            mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) &&
+                            mbar_wait(atfree0 + 8 * t, tph ^ 1, p.err, kDevErrTimeout) &&
                             !*abort_flag;
             if (ok) {
-                split_block(a32 + f * kA32Buf, smem + s * Cfg::stage_bytes, w, lane);
-                fence_proxy_async_smem();    // generic-proxy writes -> tensor core
+                tc_fence_after();
+                split_block_tm(a32 + f * kA32Buf,
+                               (tmem + Cfg::a_tm_base + t * Cfg::a_tm_cols + 8 * kpart) | lane_off,
+                               r, kpart);
+                tmem_st_wait();
+                tc_fence_before();           // tensor-memory stores -> the MMA
             }
             // all 16 split warps done with this block; one thread signals, so
             // one cluster-scope release per block instead of sixteen
@@ -447,7 +498,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             }
             if (w == 0 && lane == 0) {
                 mbar_arrive(afree0 + 8 * f);
-                mbar_arrive_remote(aready_leader0 + 8 * s);
+                mbar_arrive_remote(aready_leader0 + 8 * t);
             }
         }
     } else if (warp >= 2) {
