@@ -87,7 +87,10 @@ struct KCfg {
     static constexpr int a32_bytes = FUSED ? kA32Bufs * kA32Buf : 0;
     // epilogue staging for bulk tensor stores: 32 rows x 16 FP32 per
     // accumulator warp (2 KB)
-    static constexpr int c_bytes = ::emu::acc_warps<FUSED>() * 2048;
+    // (two per warp on the fused path, which has the shared memory to spare:
+    // one is filled while the other's store is still reading it)
+    static constexpr int c_bufs = FUSED ? 2 : 1;
+    static constexpr int c_bytes = ::emu::acc_warps<FUSED>() * 2048 * c_bufs;
     static constexpr int avail = kSmemMax - 2048 - a32_bytes - c_bytes;
     static constexpr int max_stages = pieces == 1 ? 6 : 4;
     static constexpr int stages = avail / stage_bytes > max_stages ? max_stages : avail / stage_bytes;
@@ -606,12 +609,14 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 // bulk tensor store write them, coalesced and clipped at the
                 // matrix edge.  With beta != 0 each lane first reads its own
                 // row's 16 values of C (16-byte loads where they fit).
-                const uint32_t cst = smem_u32(cstage + (warp - 2) * 2048);
+                constexpr int CB = Cfg::c_bufs;
+                const uint32_t cst0 = smem_u32(cstage + (warp - 2) * 2048 * CB);
                 if (row0 < p.M) {
 #pragma unroll
                     for (int ch = 0; ch < kAccCols / 16; ++ch) {
                         if (col_base + 16 * ch >= p.N) break;          // warp-uniform
-                        if (lane == 0) bulk_wait_read();                // buffer free again
+                        const uint32_t cst = cst0 + (ch % CB) * 2048;
+                        if (lane == 0) bulk_wait_read_n<CB - 1>();      // this buffer free again
                         __syncwarp();
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
