@@ -432,3 +432,35 @@ def test_non_finite_operands_follow_the_split(emu, mode):
     clean_cols = np.all(np.isfinite(B), axis=0)
     m = np.outer(clean_rows, clean_cols)
     assert checks.error_ratio(C[m], Cref[m], Sabs[m], 64, 1.0, 0.0, mode=mode) <= 1.0
+
+
+@pytest.mark.parametrize("path", ["auto", "fused", "twopass"])
+def test_misaligned_operands_and_long_k(emu, path):
+    """Operands that start 4 bytes past a 16-byte boundary (the fused path and
+    the 16-byte split kernels must step aside), C likewise, and a one-tile
+    GEMM with K = 65536 split along K."""
+    import torch
+    emu.emu_set_path(path)
+    try:
+        r = W.rng(97)
+        M, N, K = 4100, 200, 300
+        A = W.normal(r, (M, K + 1))[:, 1:]
+        B = W.normal(r, (N, K + 1))[:, 1:]
+        dAbig, dBbig = to_dev(W.normal(W.rng(1), (M, K + 1))), to_dev(W.normal(W.rng(2), (N, K + 1)))
+        dAbig[:, 1:] = to_dev(np.ascontiguousarray(A))
+        dBbig[:, 1:] = to_dev(np.ascontiguousarray(B))
+        Cbig = torch.zeros((M, N + 1), device="cuda")
+        emu.emu_sgemm(dAbig[:, 1:], dBbig[:, 1:], Cbig[:, 1:], transB=True)
+        torch.cuda.synchronize()
+        mi, ni = W.sample_pairs(M, N, 2048, seed=9)
+        Cref, Sabs = oracle.gemm_ref(A, B, transB=True, pairs=(mi, ni))
+        got = Cbig[:, 1:].cpu().numpy()[mi, ni]
+        assert checks.error_ratio(got, Cref, Sabs, K, 1.0, 0.0) <= 1.0
+        assert torch.all(Cbig[:, 0] == 0)
+        # long K on one tile
+        A2, B2 = W.normal(r, (64, 65536)), W.normal(r, (65536, 48))
+        C2 = _run(emu, A2, B2)
+        Cref2, Sabs2 = oracle.gemm_ref(A2, B2)
+        assert checks.error_ratio(C2, Cref2, Sabs2, 65536, 1.0, 0.0) <= 1.0
+    finally:
+        emu.emu_set_path("auto")
