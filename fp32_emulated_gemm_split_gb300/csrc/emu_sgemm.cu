@@ -15,9 +15,9 @@ namespace emu {
 
 __device__ int g_emu_error = 0;
 
-static_assert(kModeBf16x9 == EMU_MODE_BF16X9 && kModeTf32x3 == EMU_MODE_TF32X3 &&
-                  kModeFp32Simt == EMU_MODE_FP32_SIMT && kModeBf16x3 == EMU_MODE_BF16X3 &&
-                  kModeTf32 == EMU_MODE_TF32 && kModeTf32x3Oy == EMU_MODE_TF32X3_OY,
+static_assert(kModeBf16x9 == int(EMU_MODE_BF16X9) && kModeTf32x3 == int(EMU_MODE_TF32X3) &&
+                  kModeFp32Simt == int(EMU_MODE_FP32_SIMT) && kModeBf16x3 == int(EMU_MODE_BF16X3) &&
+                  kModeTf32 == int(EMU_MODE_TF32) && kModeTf32x3Oy == int(EMU_MODE_TF32X3_OY),
               "kernel variants follow emu_mode_t");
 
 namespace {

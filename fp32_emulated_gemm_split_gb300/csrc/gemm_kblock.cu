@@ -112,6 +112,7 @@ struct KCfg {
     // 4 at BN = 128, so the tensor core can run further ahead of the epilogue.
     static constexpr int nbuf = FUSED ? 2 : 512 / BN;
     static constexpr int a_tm_stages = FUSED ? 2 : 0;
+    static constexpr int a_tm_ring = a_tm_stages > 0 ? a_tm_stages : 1;   // modulus (no zero)
     static constexpr int a_tm_cols = 3 * (kTcBKBytes / 4);            // 3 pieces x 32 columns
     static constexpr int a_tm_base = nbuf * BN;
     static_assert(a_tm_base + a_tm_stages * a_tm_cols <= 512, "tensor memory overflow");
@@ -376,8 +377,8 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     break;
                 }
                 // fused: A's pieces of this block in tensor-memory stage t
-                const uint32_t t = FUSED ? kbg % Cfg::a_tm_stages : 0;
-                const uint32_t tph = FUSED ? (kbg / Cfg::a_tm_stages) & 1 : 0;
+                const uint32_t t = FUSED ? kbg % Cfg::a_tm_ring : 0;
+                const uint32_t tph = FUSED ? (kbg / Cfg::a_tm_ring) & 1 : 0;
                 if (FUSED) {
                     if (!mbar_wait(aready0 + 8 * t, tph, p.err, kDevErrTimeout)) {
                         ok = false;
@@ -481,7 +482,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         for (uint32_t g = 0; g < my_blocks; ++g) {
             const uint32_t f = g % kA32Bufs, fph = (g / kA32Bufs) & 1;
-            const uint32_t t = g % Cfg::a_tm_stages, tph = (g / Cfg::a_tm_stages) & 1;
+            const uint32_t t = g % Cfg::a_tm_ring, tph = (g / Cfg::a_tm_ring) & 1;
             const bool ok = mbar_wait(afull0 + 8 * f, fph, p.err, kDevErrTimeout) &&
                             mbar_wait(atfree0 + 8 * t, tph ^ 1, p.err, kDevErrTimeout) &&
                             !*abort_flag;
