@@ -256,8 +256,13 @@ def test_host_entry_pipelined_rows_match_one_call(emu, transA, transB, beta, mod
     for C in (host, dev):
         assert checks.error_ratio(C[mi, ni], Cref, Sabs, K, 0.75, beta, C0[mi, ni],
                                   mode=_bound_mode(mode)) <= 1.0
-    # M = 8300 and both chunks (4352 and 3948 rows) leave no tail to split
-    assert np.array_equal(dev, host)
+    # with the default 256-wide tiles, M = 8300 and both chunks (4352 and
+    # 3948 rows) leave no tail to split: the same bits (other tile widths may
+    # split the call's tail and not the chunks', hence the bound first)
+    bound = checks.elementwise_bound(K, 0.75, beta, Sabs, C0[mi, ni], mode=_bound_mode(mode))
+    assert np.all(np.abs(host[mi, ni].astype(np.float64) - dev[mi, ni]) <= 2 * bound)
+    if os.environ.get("EMU_SGEMM_BN") is None:
+        assert np.array_equal(dev, host)
 
 
 def test_host_entry_pipelined_fused_shape(emu):
