@@ -1,8 +1,8 @@
 // gemm_kblock.cu -- the tensor-core GEMM: one K block at a time, all bands of
 // the block in the tensor core, the blocks summed in FP32 registers.  Used by
 // the two-pass path (pieces of A and B read from the workspace) and by the
-// fused path (A read as FP32 and split in shared memory; B's pieces from the
-// workspace).
+// fused path (A read as FP32 and split on chip into tensor memory; B's
+// pieces from the workspace).
 //
 // Method ("Unlocking Tensor Core Performance for Machine Learning Interatomic
 // Potentials", Figure 1 caption; discuss.pytorch.kr summary, section
@@ -37,14 +37,18 @@
 // when pieces 2 land.  Persistent: one cluster per SM pair walks the tiles;
 // tensor memory holds 512/BN partial buffers, so the tensor core fills the
 // next partials (of this tile or the next) while earlier ones are added to
-// the registers and the epilogue stores C.
+// the registers and the epilogue stores C.  The last, partial round of tiles
+// is split along K over the otherwise idle clusters (units of unit_at):
+// earlier parts leave FP32 sums and a flag in global memory, the last part
+// adds them and writes C.
 //
 // Fused A (BF16x9, BN = 128): the producer loads the FP32 A block (128 rows
 // x 64, two 128-byte-swizzled boxes) into one of two staging buffers;
-// sixteen split warps turn it (16 elements per thread) straight into the swizzled
-// piece layout the MMA reads, make the writes visible to the tensor core
-// (fence.proxy.async), meet at a named barrier, and one thread signals the
-// leader CTA, running ahead of the tensor core by up to two K blocks.
+// sixteen split warps turn it (16 elements per thread) into the three BF16
+// pieces and store them into tensor memory (tcgen05.st; two 96-column A
+// stages beside two 128-column accumulator buffers), fence, meet at a named
+// barrier, and one thread signals the leader CTA; the MMA reads A from tensor
+// memory and only B's pieces from shared memory.
 //
 // Warps (576 threads per CTA, 832 when fused):
 //   warp 0      TMA producer (both CTAs; completion counted on the leader's
