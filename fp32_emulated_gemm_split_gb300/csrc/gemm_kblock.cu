@@ -473,7 +473,8 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     } else if (FUSED && warp >= 2 + Cfg::acc_warps) {
         // ------------------------------------------------------ split warps
         // Split every K block of this cluster's tiles, as soon as its FP32
-        // block has landed and its stage is free, ahead of the tensor core.
+        // block has landed and its tensor-memory A stage is free, ahead of
+        // the tensor core.
         const int w = warp - 2 - Cfg::acc_warps;
         const int kpart = w >> 2;                      // 16-element part of the 64
         const int r = 32 * (warp & 3) + lane;          // row: this warp's TMEM lanes
