@@ -87,11 +87,11 @@ def cpu_oracle_time(g, A, B, C0, seconds):
     the whole GEMM's time is extrapolated linearly in rows."""
     import numpy as np
 
-    def rows(r):
+    def rows(r, fn=oracle.gemm_bf16x9):
         mi = np.repeat(np.arange(r, dtype=np.int64), g.N)
         ni = np.tile(np.arange(g.N, dtype=np.int64), r)
         t = time.perf_counter()
-        oracle.gemm_bf16x9(A, B, g.transA, g.transB, g.alpha, g.beta, C0, pairs=(mi, ni))
+        fn(A, B, g.transA, g.transB, g.alpha, g.beta, C0, pairs=(mi, ni))
         return time.perf_counter() - t
 
     r, t = 1, rows(1)
@@ -101,8 +101,10 @@ def cpu_oracle_time(g, A, B, C0, seconds):
         r = int(max(1, min(g.M, r * seconds / max(t, 1e-6))))
         t = rows(r)
     full = t * g.M / r
+    ref_full = rows(r, oracle.gemm_ref) * g.M / r      # the FP64 reference on the same rows
     return {"workload": g.name, "mode": "cpu_oracle_bf16x9", "rows_timed": r,
             "seconds_timed": round(t, 3), "seconds_full": round(full, 3),
+            "seconds_full_fp64_ref": round(ref_full, 3),
             "extrapolated": r < g.M, "threads": oracle.max_threads(),
             "tflops": round(g.flops / full / 1e12, 7)}
 
