@@ -21,7 +21,7 @@ LIB_NAME = f"libemusgemm.{platform.machine()}.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
 SOURCES = ["emu_sgemm.cu", "split.cu", "gemm_kblock.cu", "gemm_simt.cu", "noalloc.cu", "chooser.cu"]
-HEADERS = ["emu_device.cuh", "emu_internal.h"]
+HEADERS = ["emu_device.cuh", "emu_internal.h", "schedule.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]

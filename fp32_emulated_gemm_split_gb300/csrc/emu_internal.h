@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "schedule.h"
+
 namespace emu {
 
 // Device error codes recorded in the sticky error word (same values as the
@@ -45,13 +47,12 @@ struct TcGemmParams {
     float* C;
     int64_t ldc;
     int tma_store;       // 1: the C tensor map is valid (bulk tensor stores of C)
-    // Tail split: the last tail_tiles tiles (one partial wave) run as
-    // tail_parts units each, over consecutive ranges of K blocks; units
-    // 0 .. tail_parts-2 leave their FP32 sums in part_ws and raise a flag
-    // (value epoch), the last unit adds them and writes C.  units = tiles +
-    // tail_tiles * (tail_parts - 1); tail_parts <= 1: no split.
-    int units;
-    int tail_tiles, tail_parts;
+    // Stream-K tail (schedule.h): the K blocks of the last tail_tiles tiles
+    // are shared by tail_clusters clusters in consecutive ranges; a cluster
+    // whose range starts inside a tile leaves that part's FP32 sums in its
+    // slot of part_ws and raises its flag (value epoch); the tile's owner
+    // adds them and writes C.  tail_tiles = 0: whole tiles only.
+    int tail_tiles, tail_clusters;
     float* part_ws;
     unsigned* flags;
     unsigned epoch;

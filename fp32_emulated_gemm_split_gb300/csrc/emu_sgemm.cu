@@ -37,8 +37,8 @@ struct DeviceState {
     // and per-chunk events (created on first use, kept until exit)
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t ev_in[kHostChunksMax] = {}, ev_done[kHostChunksMax] = {};
-    // the GEMM's tail split: partial sums (grown on demand), flags (zeroed
-    // once) and the epoch that marks this call's flags
+    // the GEMM's stream-K tail: one slot of partial sums per cluster (grown on
+    // demand), flags (zeroed once) and the epoch that marks this call's flags
     void* part = nullptr;
     size_t part_bytes = 0;
     unsigned* flags = nullptr;
@@ -228,29 +228,41 @@ bool make_c_map(CUtensorMap* map, float* C, int64_t M, int64_t N, int64_t ldc) {
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Split the last, partial wave of tiles along K so that it fills the GPU:
-// with C clusters and a remainder of r tiles, each of those r tiles runs as
-// min(C / r, 8, K blocks / 2) parts on as many clusters (C: the clusters
-// of this GEMM variant that can be resident at once).  Sets p.units,
-// p.tail_*, p.part_ws, p.flags and p.epoch.
+// Plan the tail of the persistent GEMM (schedule.h) for the clusters of
+// this GEMM variant that can be resident at once, and give it its
+// workspace: one slot of bm x bn FP32 sums and 2 x 16 flags per cluster
+// sharing the tail.  Sets p.tail_*, p.part_ws, p.flags and p.epoch.
 constexpr int kFlagsBytes = 64 << 10;
+
+// What handing one part's sums to the tile's owner costs, in half K blocks
+// of the mode: writing and reading a slot takes about 4 us for 256-wide
+// tiles (2 us for 128-wide ones, whose K blocks also take half as long),
+// against measured K blocks of 2.7 us (BF16x9), 1.1 us (TF32x3, its
+// Ootomo-Yokota variant and BF16x3) and 0.53 us (single-pass TF32).
+int handover_half_blocks(int mode) {
+    switch (mode) {
+        case kModeBf16x9: return 3;
+        case kModeTf32x3:
+        case kModeTf32x3Oy: return 8;
+        case kModeBf16x3: return 7;
+        default: return 15;
+    }
+}
 
 emu_status_t plan_tail(TcGemmParams& p, int mode, int bm, int bn, int fused, DeviceState* d) {
     const int tiles = p.tiles_m * p.tiles_n;
     const int clusters = gemm_kblock_clusters(mode, bn, fused, d->sms);
-    p.units = tiles;
     p.tail_tiles = 0;
-    p.tail_parts = 1;
+    p.tail_clusters = 0;
     p.part_ws = nullptr;
     p.flags = nullptr;
     p.epoch = 0;
-    const int rem = clusters > 0 ? tiles % clusters : 0;
-    if (rem == 0) return EMU_OK;
-    int parts = clusters / rem;
-    if (parts > 8) parts = 8;
-    if (parts > p.num_kb / 2) parts = p.num_kb / 2;
-    if (parts < 2) return EMU_OK;
-    const size_t need = (size_t)rem * (parts - 1) * bm * bn * sizeof(float);
+    int tail_tiles = 0, tail_clusters = 0;
+    sched_plan_tail(tiles, p.num_kb, clusters, handover_half_blocks(mode), &tail_tiles,
+                    &tail_clusters);
+    if (tail_tiles == 0) return EMU_OK;
+    if ((size_t)tail_clusters * 2 * 16 * sizeof(unsigned) > (size_t)kFlagsBytes) return EMU_OK;
+    const size_t need = (size_t)tail_clusters * bm * bn * sizeof(float);
     emu_status_t st = ensure_buffer(&d->part, &d->part_bytes, need);
     if (st != EMU_OK) return st;
     if (!d->flags) {
@@ -261,10 +273,8 @@ emu_status_t plan_tail(TcGemmParams& p, int mode, int bm, int bn, int fused, Dev
         }
         if (cudaMemset(d->flags, 0, kFlagsBytes) != cudaSuccess) return from_cuda(cudaGetLastError());
     }
-    if ((size_t)rem * (parts - 1) * 2 * 16 * sizeof(unsigned) > (size_t)kFlagsBytes) return EMU_OK;
-    p.tail_tiles = rem;
-    p.tail_parts = parts;
-    p.units = tiles + rem * (parts - 1);
+    p.tail_tiles = tail_tiles;
+    p.tail_clusters = tail_clusters;
     p.part_ws = static_cast<float*>(d->part);
     p.flags = d->flags;
     p.epoch = ++d->epoch == 0 ? ++d->epoch : d->epoch;   // never 0 (the flags' initial value)

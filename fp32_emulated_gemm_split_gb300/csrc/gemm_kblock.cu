@@ -38,9 +38,10 @@
 // tensor memory holds 512/BN partial buffers, so the tensor core fills the
 // next partials (of this tile or the next) while earlier ones are added to
 // the registers and the epilogue stores C.  The last, partial round of tiles
-// is split along K over the otherwise idle clusters (units of unit_at):
-// earlier parts leave FP32 sums and a flag in global memory, the last part
-// adds them and writes C.
+// runs stream-K (schedule.h): its K blocks are shared evenly by all
+// clusters in consecutive ranges; a range that starts inside a tile leaves
+// that part's FP32 sums and a flag in global memory, and the part holding the
+// tile's first K block adds them in K order and writes C.
 //
 // Fused A (BF16x9, BN = 128): the producer loads the FP32 A block (128 rows
 // x 64, two 128-byte-swizzled boxes) into one of two staging buffers;
@@ -60,6 +61,7 @@
 //               C = alpha*acc + beta*C
 //   then        (fused) 16 split warps.
 #include "emu_device.cuh"
+#include "schedule.h"
 
 namespace emu {
 namespace {
@@ -130,34 +132,11 @@ struct KCfg {
     static_assert(!(FUSED && MODE != kModeBf16x9), "the fused path splits BF16x9 pieces only");
 };
 
-// Work unit u of the persistent schedule: a whole tile, or (tail split) one
-// part of a tail tile's K blocks.
-struct Unit {
-    int tile, kb0, kb1;
-    int part, parts;     // parts > 1: this is part `part` of tail tile `tail`
-    int tail;
-};
-
-__device__ __forceinline__ Unit unit_at(const TcGemmParams& p, int u) {
-    const int tiles = p.tiles_m * p.tiles_n;
-    const int first = tiles - p.tail_tiles;
-    Unit w;
-    if (p.tail_parts <= 1 || u < first) {
-        w.tile = u; w.kb0 = 0; w.kb1 = p.num_kb; w.part = 0; w.parts = 1; w.tail = -1;
-        return w;
-    }
-    const int v = u - first;
-    w.tail = v / p.tail_parts;
-    w.part = v - w.tail * p.tail_parts;
-    w.parts = p.tail_parts;
-    w.tile = first + w.tail;
-    w.kb0 = w.part * p.num_kb / p.tail_parts;
-    w.kb1 = (w.part + 1) * p.num_kb / p.tail_parts;
-    return w;
-}
-
 __device__ __forceinline__ void st_release_gpu(unsigned* a, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* a) {
     unsigned v;
@@ -284,6 +263,9 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
     const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
+    const TileSchedule sch = {p.tiles_m * p.tiles_n, p.num_kb, p.tail_tiles, p.tail_clusters,
+                              num_clusters};
+    const int nunits = sched_units(sch, cluster_id);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < nb_full; ++i) mbar_init(full0 + 8 * i, 1);
@@ -325,8 +307,8 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         const uint32_t full_leader0 = map_to_rank(full0, 0);
         uint32_t kbg = 0;                         // K blocks staged so far (all units)
         bool ok = true;
-        for (int u = cluster_id; u < p.units && ok; u += num_clusters) {
-            const Unit w = unit_at(p, u);
+        for (int i = 0; i < nunits && ok; ++i) {
+            const Unit w = sched_unit(sch, cluster_id, i);
             int tm, tn;
             tile_pos(w.tile, p.tiles_m, p.tiles_n, tm, tn);
             const int arow = tm * kBM + int(rank) * kHalfRows;
@@ -369,8 +351,8 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         uint32_t kbg = 0, part = 0;              // K blocks and TMEM partials so far
         uint32_t prev_s = 0;                     // band-major: stage of the pair's first block
         bool ok = true;
-        for (int u = cluster_id; u < p.units && ok; u += num_clusters) {
-            const Unit w = unit_at(p, u);
+        for (int i = 0; i < nunits && ok; ++i) {
+            const Unit w = sched_unit(sch, cluster_id, i);
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++kbg) {
                 const uint32_t s = kbg % S, ph = (kbg / S) & 1;
                 const uint32_t buf = part % NB, cph = (part / NB) & 1;
@@ -481,8 +463,8 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const uint32_t aready_leader0 = map_to_rank(aready0, 0);
         uint32_t my_blocks = 0;
-        for (int u = cluster_id; u < p.units; u += num_clusters) {
-            const Unit w = unit_at(p, u);
+        for (int i = 0; i < nunits; ++i) {
+            const Unit w = sched_unit(sch, cluster_id, i);
             my_blocks += uint32_t(w.kb1 - w.kb0);
         }
         for (uint32_t g = 0; g < my_blocks; ++g) {
@@ -520,11 +502,11 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         bool ok = true;
         constexpr int KBP = Cfg::kb_per_partial;
         uint32_t part = 0;
-        for (int u = cluster_id; u < p.units && ok; u += num_clusters) {
-            const Unit w = unit_at(p, u);
+        for (int i = 0; i < nunits && ok; ++i) {
+            const Unit w = sched_unit(sch, cluster_id, i);
             const int nparts = (w.kb1 - w.kb0 + KBP - 1) / KBP;   // TMEM partials of this unit
             const int tile = w.tile;
-            if (p.beta != 0.0f && w.part == w.parts - 1) {
+            if (p.beta != 0.0f && w.publish < 0) {
                 // the epilogue will read this thread's row of C: start it on
                 // its way to L2 now, while the tensor core works
                 int tm_, tn_;
@@ -563,46 +545,61 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 if (lane == 0) mbar_arrive_remote(cempty_leader0 + 8 * buf);
             }
             if (!ok || *abort_flag) break;
-            if (w.parts > 1) {
-                // tail split: this thread's FP32 sums of the same elements,
-                // lane-contiguous per column (coalesced), one slot per
-                // (tail tile, part, CTA rank, accumulator warp)
-                const int aw = warp - 2;
-                auto slot = [&](int pt) {
-                    return ((w.tail * (w.parts - 1) + pt) * 2 + int(rank)) * Cfg::acc_warps + aw;
-                };
-                if (w.part < w.parts - 1) {
-                    float* dst = p.part_ws + (size_t)slot(w.part) * (kAccCols * 32);
+            // stream-K tail: one FP32 slot per (cluster, CTA rank, accumulator
+            // warp); this thread's sums as 16-byte groups, lane-contiguous per
+            // group, so that a warp writes and reads 512 contiguous bytes at a
+            // time
+            const int aw = warp - 2;
+            auto slot = [&](int c) { return (c * 2 + int(rank)) * Cfg::acc_warps + aw; };
+            if (w.publish >= 0) {
+                // a later part of a split tile: leave the sums for the owner
+                float4* dst = reinterpret_cast<float4*>(p.part_ws) +
+                              (size_t)slot(w.publish) * (kAccCols / 4 * 32) + lane;
 #pragma unroll
-                    for (int j = 0; j < kAccCols; ++j) dst[j * 32 + lane] = acc[j];
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) st_release_gpu(p.flags + slot(w.part), p.epoch);
-                    continue;                          // the last part writes C
-                }
-                // last part: add the other parts' sums (bounded waits)
-                for (int pt = 0; pt < w.parts - 1 && ok; ++pt) {
-                    const unsigned* f = p.flags + slot(pt);
-                    const uint64_t t0 = global_timer_ns();
-                    while (ld_acquire_gpu(f) != p.epoch) {
-                        __nanosleep(64);
-                        if (global_timer_ns() - t0 > EMU_WAIT_LIMIT_NS) {
-                            record_error(p.err, kDevErrTimeout);
-                            ok = false;
-                            break;
-                        }
-                    }
-                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                    const float* src = p.part_ws + (size_t)slot(pt) * (kAccCols * 32);
-#pragma unroll
-                    for (int j = 0; j < kAccCols; ++j) acc[j] += __ldcg(src + j * 32 + lane);
-                    // consumed: clear the flag, so that a replay of the same
-                    // launch (a CUDA graph bakes the epoch in) waits afresh
-                    __syncwarp();
-                    if (lane == 0) *const_cast<volatile unsigned*>(f) = 0u;
-                }
-                if (!ok) { *abort_flag = 1; break; }
+                for (int j = 0; j < kAccCols / 4; ++j)
+                    __stcg(dst + j * 32, make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2],
+                                                     acc[4 * j + 3]));
+                fence_acq_rel_gpu();                   // each lane's stores before the flag
+                __syncwarp();
+                if (lane == 0) st_release_gpu(p.flags + slot(w.publish), p.epoch);
+                continue;                              // the owner writes C
             }
+            // owner of a split tile: add the later parts' sums in K order
+            // (bounded waits; those clusters publish before they wait on anything)
+            for (int o = 1; o <= w.others && ok; ++o) {
+                const unsigned* f = p.flags + slot(cluster_id + o);
+                const uint64_t t0 = global_timer_ns();
+                while (ld_acquire_gpu(f) != p.epoch) {
+                    __nanosleep(64);
+                    if (global_timer_ns() - t0 > EMU_WAIT_LIMIT_NS) {
+                        record_error(p.err, kDevErrTimeout);
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                const float4* src = reinterpret_cast<const float4*>(p.part_ws) +
+                                    (size_t)slot(cluster_id + o) * (kAccCols / 4 * 32) + lane;
+                constexpr int kBatch = kAccCols / 4 < 8 ? kAccCols / 4 : 8;   // loads in flight
+#pragma unroll
+                for (int j0 = 0; j0 < kAccCols / 4; j0 += kBatch) {
+                    float4 v[kBatch];
+#pragma unroll
+                    for (int b = 0; b < kBatch; ++b) v[b] = __ldcg(src + (j0 + b) * 32);
+#pragma unroll
+                    for (int b = 0; b < kBatch; ++b) {
+                        acc[4 * (j0 + b)] += v[b].x;
+                        acc[4 * (j0 + b) + 1] += v[b].y;
+                        acc[4 * (j0 + b) + 2] += v[b].z;
+                        acc[4 * (j0 + b) + 3] += v[b].w;
+                    }
+                }
+                // consumed: clear the flag, so that a replay of the same
+                // launch (a CUDA graph bakes the epoch in) waits afresh
+                __syncwarp();
+                if (lane == 0) *const_cast<volatile unsigned*>(f) = 0u;
+            }
+            if (!ok) { *abort_flag = 1; break; }
             // ---- epilogue: C = alpha * acc + beta * C
             int tm, tn;
             tile_pos(tile, p.tiles_m, p.tiles_n, tm, tn);
@@ -718,8 +715,8 @@ cudaError_t set_smem_attr() {
 
 // Clusters of this kernel that can be resident at once (at most sms / 2).
 // The persistent grid never exceeds it, so every cluster runs concurrently:
-// the tail split's last part waits for the other parts, which must not be
-// queued behind it.
+// the owner of a stream-K tail tile waits for the clusters that hold the
+// tile's later K ranges, which must not be queued behind it.
 template <int MODE, int BN, int FUSED>
 int max_clusters_t(int sms) {
     using Cfg = KCfg<MODE, BN, FUSED>;
@@ -799,19 +796,18 @@ cudaError_t launch_gemm_kblock(int mode, int bn, int fused, const CUtensorMap& m
     if (tiles == 0) return cudaSuccess;
     TcGemmParams q = p;
     const int resident = gemm_kblock_clusters(mode, bn, fused, sms);
-    // a split plan is used only as made for this many clusters: all of a
-    // tail tile's parts then run at once, in the last round of the grid
-    const bool split_ok = q.tail_parts > 1 && q.tail_tiles > 0 && q.tail_tiles <= tiles &&
-                          q.part_ws && q.flags &&
-                          q.units == tiles + q.tail_tiles * (q.tail_parts - 1) &&
-                          q.num_kb >= q.tail_parts && (tiles - q.tail_tiles) % resident == 0 &&
-                          q.tail_tiles * q.tail_parts <= resident;
+    // A stream-K tail is used only as planned for this many resident
+    // clusters: whole tiles fill complete rounds of all of them and every
+    // cluster sharing the tail runs at once (an owner waits for the others).
+    const int first = tiles - q.tail_tiles;
+    const bool split_ok = q.tail_tiles > 0 && q.tail_tiles <= tiles && q.part_ws && q.flags &&
+                          q.tail_clusters >= 1 && q.tail_clusters <= resident &&
+                          q.num_kb >= 2 && first % resident == 0;
     if (!split_ok) {                         // whole tiles only
-        q.units = tiles;
         q.tail_tiles = 0;
-        q.tail_parts = 1;
+        q.tail_clusters = 0;
     }
-    const int clusters = q.units < resident ? q.units : resident;
+    const int clusters = sched_grid_clusters(tiles, q.tail_tiles, q.tail_clusters, resident);
     cudaError_t e;
     if (fused) {
         if (mode != kModeBf16x9 || bn != 128) return cudaErrorInvalidValue;

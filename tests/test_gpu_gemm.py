@@ -240,9 +240,10 @@ def test_host_entry_point_matches_device_path(emu):
 def test_host_entry_pipelined_rows_match_one_call(emu, transA, transB, beta, mode):
     """Large enough for the chunked copy/compute pipeline (row chunks of C on
     three streams): row chunks of C are computed independently by the same
-    kernels, so the result matches the one-call device result -- bit for bit
-    unless the GEMM's tail split (which depends on the tile count) differs
-    between the call and its chunks, and within the accuracy bound always."""
+    kernels, so the result matches the one-call device result within the
+    accuracy bound -- and bit for bit where no K range is split (the SIMT
+    kernel); the GEMM's stream-K tail depends on the tile count, so a chunk
+    and the whole call may sum a tile's K blocks in different groupings."""
     M, N, K = 8300, 1024, 1024                       # ragged last chunk
     r = W.rng(18 + transA + 2 * transB)
     A = W.normal(r, (K, M) if transA else (M, K))
@@ -256,12 +257,9 @@ def test_host_entry_pipelined_rows_match_one_call(emu, transA, transB, beta, mod
     for C in (host, dev):
         assert checks.error_ratio(C[mi, ni], Cref, Sabs, K, 0.75, beta, C0[mi, ni],
                                   mode=_bound_mode(mode)) <= 1.0
-    # with the default 256-wide tiles, M = 8300 and both chunks (4352 and
-    # 3948 rows) leave no tail to split: the same bits (other tile widths may
-    # split the call's tail and not the chunks', hence the bound first)
     bound = checks.elementwise_bound(K, 0.75, beta, Sabs, C0[mi, ni], mode=_bound_mode(mode))
     assert np.all(np.abs(host[mi, ni].astype(np.float64) - dev[mi, ni]) <= 2 * bound)
-    if os.environ.get("EMU_SGEMM_BN") is None:
+    if mode == "fp32_simt":
         assert np.array_equal(dev, host)
 
 
@@ -390,10 +388,11 @@ def test_subnormal_operands_through_the_tensor_core(emu, mode):
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("mode", ["bf16x9", "tf32x3", "bf16x3"])
 def test_tail_split_shapes(emu, shape, mode):
-    """Shapes whose last round of tiles is split along K (1 tile in 8 parts,
-    16 tiles in 4, 6 tiles in 8, 28 of 256 tiles in 2): within the bound,
-    every element where the oracle is fast enough, and the same bits on a
-    second call (the reduction order is fixed)."""
+    """Shapes whose last round of tiles runs stream-K (its K blocks shared by
+    many clusters in consecutive ranges: 1 tile over 16 clusters, 16 tiles
+    over 76, 6 tiles over 48, the last 28 of 256 tiles over 76): within the
+    bound, every element where the oracle is fast enough, and the same bits
+    on a second call (the reduction order is fixed)."""
     M, N, K = shape
     r = W.rng(M + 3 * N + 7 * K)
     A, B = W.normal(r, (M, K)), W.normal(r, (K, N))
@@ -408,6 +407,46 @@ def test_tail_split_shapes(emu, shape, mode):
         mi, ni = W.sample_pairs(M, N, 2048, seed=8)
         Cref, Sabs = oracle.gemm_ref(A, B, pairs=(mi, ni))
         assert checks.error_ratio(C1[mi, ni], Cref, Sabs, K, 1.0, 0.0, mode=bm) <= 1.0
+
+
+@pytest.mark.parametrize("shape,transB,path", [
+    ((1536, 512, 700), True, "twopass"),      # BF16x9: 12 tiles of 11 blocks, 5 parts each
+    ((4864, 512, 700), False, "twopass"),     # 38 tiles of 11 blocks, 2 parts each
+    ((300, 384, 4100), True, "auto"),         # 4 tiles of 65 blocks (last one ragged), 8 parts
+    ((12288, 256, 1024), False, "twopass"),   # 48 tiles of 16 blocks, stream-K over 76
+    ((12288, 256, 4096), True, "twopass"),    # 48 tiles of 64 blocks, stream-K in every mode
+    ((12288, 256, 1024), False, "fused"),     # 96 tiles: 20 left over, 3 parts each
+], ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3", "bf16x3", "tf32", "tf32x3_oy"])
+def test_tail_parts_with_alpha_beta(emu, shape, transB, path, mode):
+    """Split tails -- equal parts inside a tile, and stream-K ranges that
+    start and end inside tiles so that a tile is summed by two or more
+    clusters -- with alpha, beta and C0 applied once by the tile's owner:
+    within each mode's bound on every element (sampled on the largest
+    shapes) and the same bits on a second call."""
+    if path == "fused" and mode != "bf16x9":
+        pytest.skip("the fused path is BF16x9 only")
+    M, N, K = shape
+    r = W.rng(M + 5 * N + 11 * K)
+    A = W.normal(r, (M, K))
+    B = W.normal(r, (N, K) if transB else (K, N), std=K ** -0.5)
+    C0 = W.uniform(r, (M, N))
+    emu.emu_set_path(path)
+    try:
+        C1 = _run(emu, A, B, False, transB, alpha=1.5, beta=0.5, C0=C0, mode=mode)
+        C2 = _run(emu, A, B, False, transB, alpha=1.5, beta=0.5, C0=C0, mode=mode)
+    finally:
+        emu.emu_set_path("auto")
+    assert np.array_equal(C1, C2)
+    assert emu.emu_get_last_device_error() == 0
+    if M * N * K <= (1 << 30):
+        Cref, Sabs = oracle.gemm_ref(A, B, False, transB, 1.5, 0.5, C0)
+        assert checks.error_ratio(C1, Cref, Sabs, K, 1.5, 0.5, C0, mode=mode) <= 1.0
+    else:
+        mi, ni = W.sample_pairs(M, N, 4096, seed=12)
+        Cref, Sabs = oracle.gemm_ref(A, B, False, transB, 1.5, 0.5, C0, pairs=(mi, ni))
+        assert checks.error_ratio(C1[mi, ni], Cref, Sabs, K, 1.5, 0.5, C0[mi, ni],
+                                  mode=mode) <= 1.0
 
 
 @pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
@@ -443,7 +482,7 @@ def test_non_finite_operands_follow_the_split(emu, mode):
 def test_misaligned_operands_and_long_k(emu, path):
     """Operands that start 4 bytes past a 16-byte boundary (the fused path and
     the 16-byte split kernels must step aside), C likewise, and a one-tile
-    GEMM with K = 65536 split along K."""
+    GEMM with K = 65536 whose K blocks are shared by 16 clusters."""
     import torch
     emu.emu_set_path(path)
     try:

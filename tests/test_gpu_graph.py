@@ -1,8 +1,9 @@
 """emu_sgemm inside a CUDA graph: after one call outside capture (which
 sizes the library's buffers), a captured call replays with fresh operand
 values and gives, bit for bit, what a direct call gives -- including shapes
-whose last round of tiles is split along K, whose flags must not leak from
-one replay into the next."""
+whose last round of tiles runs stream-K (K ranges of a tile summed by several
+clusters through flagged slots), whose flags must not leak from one replay
+into the next."""
 import pytest
 
 from gpu_util import emu_module
@@ -19,6 +20,7 @@ def emu():
 
 @pytest.mark.parametrize("shape,path", [((4096, 4096, 512), "twopass"),
                                         ((256, 256, 4096), "twopass"),
+                                        ((12288, 256, 1024), "twopass"),
                                         ((70000, 256, 256), "fused"),
                                         ((1000, 700, 300), "auto")],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else v)
