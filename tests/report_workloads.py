@@ -1,7 +1,11 @@
 """Accuracy and speed of every workload and mode on the GPU (a report, not a
 test): one JSON line per (workload, mode) with
 
-  tflops        effective 2MNK/t of emu_sgemm (CUDA events, median of runs)
+  tflops        effective 2MNK/t of emu_sgemm, one call at a time (CUDA events
+                around each call, median of runs: includes the launch latency)
+  tflops_stream the same for calls issued back to back (events around a run
+                of calls: the host's launch work overlaps the GPU's, as when
+                a model runs its layers one after another)
   pct_p9        that figure as a percentage of the measured BF16 peak / 9
   max_ratio     max |C - C_ref| / bound over the checked outputs (<= 1 passes)
   rel_frob      relative Frobenius error over the checked outputs
@@ -49,6 +53,23 @@ def time_call(fn, reps=10, warm=3):
     return float(np.median(times))
 
 
+def time_stream(fn, reps=20, rounds=3):
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(rounds):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e) / reps)
+    return float(np.median(times))
+
+
 def cublas_child(name, emulate):
     """Time torch.matmul FP32 on the workload in a child process."""
     code = f"""
@@ -68,7 +89,14 @@ ts = []
 for _ in range(10):
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(); f(); e.record(); torch.cuda.synchronize(); ts.append(s.elapsed_time(e))
-print(json.dumps({{"ms": float(np.median(ts))}}))
+reps = 20 if g.flops < 2e12 else 5
+tb = []
+for _ in range(3):
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps): f()
+    e.record(); torch.cuda.synchronize(); tb.append(s.elapsed_time(e) / reps)
+print(json.dumps({{"ms": float(np.median(ts)), "ms_stream": float(np.median(tb))}}))
 """
     env = dict(os.environ)
     if emulate:
@@ -77,8 +105,9 @@ print(json.dumps({{"ms": float(np.median(ts))}}))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
                        timeout=600)
     if r.returncode != 0:
-        return None
-    return json.loads(r.stdout.strip().splitlines()[-1])["ms"]
+        return None, None
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["ms"], d["ms_stream"]
 
 
 def cpu_oracle_time(g, A, B, C0, seconds):
@@ -166,11 +195,16 @@ def main():
             relf = checks.rel_frobenius(got, Cref)
             reps = 10 if g0.flops < 2e12 else 5
             ms = time_call(run, reps=reps)
+            ms_s = time_stream(run, reps=2 * reps)
             if dC0 is not None:   # subtract the restore copy of C
                 ms -= time_call(lambda: dC.copy_(dC0), reps=reps)
+                ms_s -= time_stream(lambda: dC.copy_(dC0), reps=2 * reps)
             tf = g0.flops / (ms * 1e-3) / 1e12
+            tfs = g0.flops / (ms_s * 1e-3) / 1e12
             rec = {"workload": name, "mode": mode_name, "M": g0.M, "N": g0.N, "K": g0.K,
                    "ms": round(ms, 4), "tflops": round(tf, 2), "pct_p9": round(100 * tf / p9, 1),
+                   "ms_stream": round(ms_s, 4), "tflops_stream": round(tfs, 2),
+                   "pct_p9_stream": round(100 * tfs / p9, 1),
                    "max_ratio": ratio, "rel_frob": relf,
                    "checked": "all" if full else int(mi.size)}
             print(json.dumps(rec), flush=True)
@@ -179,9 +213,11 @@ def main():
         emu.emu_set_path("auto")
         if not args.no_cublas and g0.mode == "bf16x9":
             for emulate in (False, True):
-                ms = cublas_child(name, emulate)
+                ms, ms_s = cublas_child(name, emulate)
                 rec = {"workload": name, "mode": "cublas_" + ("bf16x9_env" if emulate else "fp32"),
-                       "ms": ms, "tflops": None if ms is None else round(g0.flops / (ms * 1e-3) / 1e12, 2)}
+                       "ms": ms, "tflops": None if ms is None else round(g0.flops / (ms * 1e-3) / 1e12, 2),
+                       "ms_stream": ms_s,
+                       "tflops_stream": None if ms_s is None else round(g0.flops / (ms_s * 1e-3) / 1e12, 2)}
                 print(json.dumps(rec), flush=True)
                 if out:
                     out.write(json.dumps(rec) + "\n")
