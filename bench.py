@@ -439,7 +439,7 @@ def main(argv=None):
     ap.add_argument("--no-simt", action="store_true", help="skip the SIMT FP32 context number")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--shape", default=None, help="M,N,K override (same distribution)")
-    ap.add_argument("--path", default=None, choices=[None, "auto", "twopass", "fused"],
+    ap.add_argument("--path", default=None, choices=[None, "auto", "twopass", "fused", "fused_tmem"],
                     help="implementation of the tensor-core modes (default: the library's)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps

@@ -18,7 +18,7 @@ import os
 from . import _build
 
 MODE = {"bf16x9": 0, "tf32x3": 1, "fp32_simt": 2, "bf16x3": 3, "tf32": 4, "tf32x3_oy": 5}
-PATH = {"auto": 0, "twopass": 1, "fused": 2}
+PATH = {"auto": 0, "twopass": 1, "fused": 2, "fused_tmem": 3}
 PROFILE_KIND = {"split": 0, "gemm_tc": 1, "gemm_fused": 2, "gemm_simt": 3, "scale": 4}
 
 _lib = None
@@ -271,7 +271,7 @@ def emu_predict_us(M, N, K, mode="bf16x9", sms=152) -> float:
 
 def emu_get_path() -> str:
     v = lib().emu_get_path()
-    return {0: "auto", 1: "twopass", 2: "fused"}[v]
+    return {0: "auto", 1: "twopass", 2: "fused", 3: "fused_tmem"}[v]
 
 
 def emu_workspace_size(M, N, K, mode="bf16x9") -> int:

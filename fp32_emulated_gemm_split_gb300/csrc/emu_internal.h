@@ -53,6 +53,10 @@ struct TcGemmParams {
     // slot of part_ws and raises its flag (value epoch); the tile's owner
     // adds them and writes C.  tail_tiles = 0: whole tiles only.
     int tail_tiles, tail_clusters;
+    // shared-memory fused path only: FP32 A (row-major, 16-byte aligned,
+    // lda % 4 == 0), read by the kernel's split warps
+    const float* A32;
+    int64_t lda;
     float* part_ws;
     unsigned* flags;
     unsigned epoch;

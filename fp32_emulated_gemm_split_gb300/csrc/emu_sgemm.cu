@@ -126,6 +126,7 @@ int read_path_env() {
     if (!s) return EMU_PATH_AUTO;
     if (!std::strcmp(s, "twopass")) return EMU_PATH_TWOPASS;
     if (!std::strcmp(s, "fused")) return EMU_PATH_FUSED;
+    if (!std::strcmp(s, "fused_tmem")) return EMU_PATH_FUSED_TMEM;
     return EMU_PATH_AUTO;
 }
 
@@ -367,9 +368,11 @@ bool fused_ok(int mode, int transA, const float* A, int64_t lda) {
            (reinterpret_cast<uintptr_t>(A) & 15) == 0;
 }
 
-// Fused path: B's three pieces go to the workspace (one split kernel); A is
-// read as FP32 by the GEMM kernel and split in shared memory.
-emu_status_t run_fused(int transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+// Tensor-memory fused path: B's three pieces go to the workspace (one split
+// kernel); A is read as FP32 by the GEMM kernel (TMA into shared memory) and
+// split by its split warps into tensor memory, where the MMA reads it
+// (128-wide tiles).
+emu_status_t run_fused_tmem(int transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                        int64_t lda, const float* B, int64_t ldb, float beta, float* C,
                        int64_t ldc, DeviceState* d, cudaStream_t stream, bool b_ready = false) {
     const int64_t ldp = plane_ld(K);
@@ -408,11 +411,57 @@ emu_status_t run_fused(int transB, int64_t M, int64_t N, int64_t K, float alpha,
     return from_cuda(e);
 }
 
+// Shared-memory fused path (BF16x9): B's pieces go to the workspace (one
+// split kernel); the GEMM kernel's split warps read FP32 A and store its
+// pieces straight into the A half of each shared-memory stage, where the
+// two-pass path's TMA would have put them: 256-wide tiles, A read from HBM
+// once as FP32, its pieces never written out.
+emu_status_t run_fused_smem(int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                            const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                            float* C, int64_t ldc, DeviceState* d, cudaStream_t stream,
+                            bool b_ready = false) {
+    const int64_t ldp = plane_ld(K);
+    if (b_ready && d->ws_bytes < (size_t)3 * N * ldp * 2) return EMU_ERR_INVALID_VALUE;
+    emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, (size_t)3 * N * ldp * 2);
+    if (st != EMU_OK) return st;
+    uint16_t* pb = static_cast<uint16_t*>(d->ws);
+    cudaError_t e = cudaSuccess;
+    if (!b_ready) {
+        ProfScope ps(0, stream);
+        e = launch_split_bf16x3(B, N, K, ldb, !transB, pb, pb + N * ldp, pb + 2 * N * ldp, ldp,
+                                stream);
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    const int bn = kblock_bn(N);
+    CUtensorMap mapB;
+    st = make_plane_map(&mapB, pb, false, N, K, ldp, 3, 64, bn / 2);
+    if (st != EMU_OK) return st;
+    const CUtensorMap mapA = mapB;           // not read: the split warps fill A's stages
+    TcGemmParams p = {};
+    p.err = d->err;
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.num_kb = (int)((K + 63) / 64);
+    p.tiles_m = (int)((M + 255) / 256);
+    p.tiles_n = (int)((N + bn - 1) / bn);
+    p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
+    p.A32 = A; p.lda = lda;
+    CUtensorMap mapC = mapB;
+    p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
+    st = plan_tail(p, kModeBf16x9, 256, bn, 3, d);
+    if (st != EMU_OK) return st;
+    {
+        ProfScope ps(2, stream);
+        e = launch_gemm_kblock(0, bn, 3, mapA, mapB, mapC, p, d->sms, stream, true);
+    }
+    return from_cuda(e);
+}
+
 // What one call runs: the kernel mode after the strategy's choice, and
-// whether the fused path takes it.
+// which path takes it (0 two-pass, 1 tensor-memory fused, 3 shared-memory
+// fused).
 struct Plan {
     int mode;
-    bool fused;
+    int fused;
 };
 
 Plan plan_call(int transA, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, int mode,
@@ -422,12 +471,22 @@ Plan plan_call(int transA, int64_t M, int64_t N, int64_t K, const float* A, int6
     Plan pl;
     // PERFORMANT: the plain FP32 kernel where it is predicted faster
     pl.mode = choose_mode(M, N, K, mode, g_strategy == EMU_STRATEGY_PERFORMANT, d->sms);
-    // AUTO: the fused kernel splits A once per 128-column tile, so it pays off
-    // when N is small (measured on GB300: N = 256 MLIP layers 1.16x faster
-    // than two-pass; N = 1024 and square shapes slower).
-    const bool auto_fused = g_path == EMU_PATH_AUTO && N <= 256 && M >= 4096;
-    pl.fused = pl.mode != EMU_MODE_FP32_SIMT && (g_path == EMU_PATH_FUSED || auto_fused) &&
-               fused_ok(pl.mode, transA, A, lda);
+    // AUTO, for BF16x9 with M >= 4096 and N <= 256 (the MLIP layers), where
+    // splitting A in the GEMM kernel saves more than the split kernel's HBM
+    // round trip costs (measured on GB300, graph replays, shared-memory fused
+    // / tensor-memory fused / two-pass): for 128 < N <= 256 the shared-memory
+    // path (131072 x 256 x 1024 387 / 476 / 532 us; 131072 x 256 x 256 123 /
+    // 142 / 150 us; 12288 x 256 x 1024 55.2 / 60.6 / 63.3 us; 12288 x 256 x
+    // 256 24.3 / 26.8 / 26.8 us), for N <= 128 the tensor-memory path, whose
+    // 128-wide tiles then waste nothing (131072 x 128 x 256 95 / 79 / 114 us);
+    // two-pass elsewhere (N = 1024: 394 us two-pass against 447, as A's
+    // pieces are then reused by four column tiles).
+    const bool small_n = g_path == EMU_PATH_AUTO && N <= 256 && M >= 4096;
+    const bool on_chip = pl.mode != EMU_MODE_FP32_SIMT && fused_ok(pl.mode, transA, A, lda);
+    pl.fused = !on_chip ? 0
+             : g_path == EMU_PATH_FUSED_TMEM ? 1
+             : g_path == EMU_PATH_FUSED ? 3
+             : small_n ? (N > 128 ? 3 : 1) : 0;
     return pl;
 }
 
@@ -440,8 +499,12 @@ emu_status_t run_planned(const Plan& pl, int transA, int transB, int64_t M, int6
         return from_cuda(launch_gemm_simt(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
                                           ldc, stream));
     }
-    if (pl.fused)
-        return run_fused(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream, b_ready);
+    if (pl.fused == 3)
+        return run_fused_smem(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream,
+                              b_ready);
+    if (pl.fused == 1)
+        return run_fused_tmem(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream,
+                              b_ready);
     return run_two_pass(pl.mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d,
                         stream, b_ready);
 }
@@ -658,7 +721,8 @@ emu_status_t emu_split_tf32x2_scaled(const float* X, int64_t rows, int64_t cols,
 }
 
 emu_status_t emu_set_path(int path) {
-    if (path != EMU_PATH_AUTO && path != EMU_PATH_TWOPASS && path != EMU_PATH_FUSED)
+    if (path != EMU_PATH_AUTO && path != EMU_PATH_TWOPASS && path != EMU_PATH_FUSED &&
+        path != EMU_PATH_FUSED_TMEM)
         return EMU_ERR_INVALID_VALUE;
     std::lock_guard<std::mutex> lock(g_mu);
     g_path = path;

@@ -68,14 +68,23 @@ namespace {
 
 constexpr int kBM = 256, kHalfRows = 128;
 constexpr int kATile = kHalfRows * kTcBKBytes;       // 16 KB: 128 rows x 128 bytes
-// Accumulator warps: 16 (a column quarter each) on the two-pass path; 8 (a
-// column half each) on the fused path, which also runs 16 split warps and must
-// stay within 1024 threads.
+// FUSED selects how A's pieces reach the tensor core: 0 (two-pass) TMA
+// loads from the workspace the split kernel wrote; 1 (tensor-memory fused)
+// split warps store them into tensor memory; 3 (shared-memory fused) split
+// warps store them into the A half of each shared-memory stage, where the
+// two-pass path's TMA would have put them.
+// Accumulator warps: 16 (a column quarter each) on the two-pass and
+// shared-memory paths; 8 (a column half each) on the tensor-memory path,
+// which also runs 16 split warps and must stay within 1024 threads.
 template <int FUSED>
-constexpr int acc_warps() { return FUSED ? 8 : 16; }
-constexpr int kSplitWarps = 16;                       // fused path only
+constexpr int acc_warps() { return FUSED == 1 ? 8 : 16; }
+constexpr int kSplitWarps = 16;                       // tensor-memory path
+constexpr int kSmemSplitWarps = 8;                    // shared-memory path: 16 rows each
 template <int FUSED>
-constexpr int threads_k() { return (2 + acc_warps<FUSED>() + (FUSED ? kSplitWarps : 0)) * 32; }
+constexpr int threads_k() {
+    return (2 + acc_warps<FUSED>() + (FUSED == 1 ? kSplitWarps : FUSED == 3 ? kSmemSplitWarps : 0)) *
+           32;
+}
 constexpr int kSmemMax = 232448;                      // dynamic shared memory per CTA
 constexpr int kA32Box = 128 * 128;                    // FP32 box: 128 rows x 32 floats
 constexpr int kA32Buf = 2 * kA32Box;                  // one 64-wide K block of FP32 A
@@ -83,19 +92,20 @@ constexpr int kA32Bufs = 2;
 
 template <int MODE, int BN, int FUSED>
 struct KCfg {
+    static constexpr bool TM = FUSED == 1, SMS = FUSED == 3;
     static constexpr bool tf32 = mode_is_tf32(MODE);
     static constexpr int pieces = mode_pieces(MODE);
     static constexpr int b_rows = BN / 2;                        // B^T rows per CTA
     static constexpr int b_tile = b_rows * kTcBKBytes;
     // fused: only B's pieces are staged in shared memory; A's go to tensor
     // memory (a_tm_stages rings of 96 columns after the accumulators)
-    static constexpr int stage_bytes = pieces * ((FUSED ? 0 : kATile) + b_tile);
-    static constexpr int a32_bytes = FUSED ? kA32Bufs * kA32Buf : 0;
+    static constexpr int stage_bytes = pieces * ((TM ? 0 : kATile) + b_tile);
+    static constexpr int a32_bytes = TM ? kA32Bufs * kA32Buf : 0;
     // epilogue staging for bulk tensor stores: 32 rows x 16 FP32 per
     // accumulator warp (2 KB)
     // (two per warp on the fused path, which has the shared memory to spare:
     // one is filled while the other's store is still reading it)
-    static constexpr int c_bufs = FUSED ? 2 : 1;
+    static constexpr int c_bufs = TM ? 2 : 1;
     static constexpr int c_bytes = ::emu::acc_warps<FUSED>() * 2048 * c_bufs;
     static constexpr int avail = kSmemMax - 2048 - a32_bytes - c_bytes;
     static constexpr int max_stages = pieces == 1 ? 6 : 4;
@@ -116,8 +126,8 @@ struct KCfg {
         MODE == kModeTf32x3 || band_major ? 2 : MODE == kModeTf32 ? 8 : 1;
     // TMEM partial buffers of BN columns each (all 512 columns): 2 at BN = 256,
     // 4 at BN = 128, so the tensor core can run further ahead of the epilogue.
-    static constexpr int nbuf = FUSED ? 2 : 512 / BN;
-    static constexpr int a_tm_stages = FUSED ? 2 : 0;
+    static constexpr int nbuf = TM ? 2 : 512 / BN;
+    static constexpr int a_tm_stages = TM ? 2 : 0;
     static constexpr int a_tm_ring = a_tm_stages > 0 ? a_tm_stages : 1;   // modulus (no zero)
     static constexpr int a_tm_cols = 3 * (kTcBKBytes / 4);            // 3 pieces x 32 columns
     static constexpr int a_tm_base = nbuf * BN;
@@ -127,7 +137,7 @@ struct KCfg {
     static constexpr uint32_t tmem_cols = 512;
     static constexpr int smem = stages * stage_bytes + a32_bytes + c_bytes + 2048;
     // bytes a piece barrier waits for (both CTAs)
-    static constexpr uint32_t piece_tx = FUSED ? 2 * b_tile : 2 * (kATile + b_tile);
+    static constexpr uint32_t piece_tx = TM || SMS ? 2 * b_tile : 2 * (kATile + b_tile);
     static_assert(stages >= 2, "shared memory too small for two stages");
     static_assert(!(FUSED && MODE != kModeBf16x9), "the fused path splits BF16x9 pieces only");
 };
@@ -215,6 +225,10 @@ __device__ __forceinline__ void split_block_tm(const uint8_t* a32, uint32_t col,
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 
 // Named barrier `id` over `nthreads` threads that also ANDs a predicate: every
 // participating warp reaches it once per use, whatever its predicate, so a
@@ -274,7 +288,11 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             mbar_init(cfull0 + 8 * b, 1);
             mbar_init(cempty0 + 8 * b, 2 * Cfg::acc_warps);   // accumulator warps of both CTAs
         }
-        if (FUSED) {
+        if (Cfg::SMS) {
+            // A half of stage s written (leader; one arrive per CTA)
+            for (int s = 0; s < S; ++s) mbar_init(aready0 + 8 * s, 2);
+        }
+        if (Cfg::TM) {
             // A pieces of tensor-memory stage t written (leader; one per CTA)
             for (int t = 0; t < Cfg::a_tm_stages; ++t) mbar_init(aready0 + 8 * t, 2);
             for (int t = 0; t < Cfg::a_tm_stages; ++t) mbar_init(atfree0 + 8 * t, 1);
@@ -315,7 +333,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             const int brow = tn * BN + int(rank) * Cfg::b_rows;
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++kbg) {
                 const uint32_t s = kbg % S, ph = (kbg / S) & 1;
-                if (FUSED) {
+                if (Cfg::TM) {
                     const uint32_t f = kbg % kA32Bufs, fph = (kbg / kA32Bufs) & 1;
                     if (!mbar_wait(afree0 + 8 * f, fph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
                         ok = false;
@@ -336,9 +354,9 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 for (int pc = P - 1; pc >= 0; --pc) {
                     if (leader) mbar_arrive_expect_tx(full0 + 8 * (s * P + pc), Cfg::piece_tx);
                     const uint32_t fbl = full_leader0 + 8 * (s * P + pc);
-                    if (!FUSED)
+                    if (!Cfg::TM && !Cfg::SMS)
                         tma_load_3d_pair(st + pc * kATile, &mapA, fbl, kb * Cfg::elems, arow, pc);
-                    tma_load_3d_pair(st + P * (FUSED ? 0 : kATile) + pc * Cfg::b_tile, &mapB, fbl,
+                    tma_load_3d_pair(st + P * (Cfg::TM ? 0 : kATile) + pc * Cfg::b_tile, &mapB, fbl,
                                      kb * Cfg::elems, brow, pc);
                 }
             }
@@ -363,10 +381,18 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     break;
                 }
                 // fused: A's pieces of this block in tensor-memory stage t
-                const uint32_t t = FUSED ? kbg % Cfg::a_tm_ring : 0;
-                const uint32_t tph = FUSED ? (kbg / Cfg::a_tm_ring) & 1 : 0;
-                if (FUSED) {
+                const uint32_t t = Cfg::TM ? kbg % Cfg::a_tm_ring : 0;
+                const uint32_t tph = Cfg::TM ? (kbg / Cfg::a_tm_ring) & 1 : 0;
+                if (Cfg::TM) {
                     if (!mbar_wait(aready0 + 8 * t, tph, p.err, kDevErrTimeout)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                if (Cfg::SMS) {
+                    // both CTAs' split warps have written A's pieces into stage s
+                    if (!mbar_wait(aready0 + 8 * s, ph, p.err, kDevErrTimeout)) {
                         ok = false;
                         break;
                     }
@@ -374,7 +400,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 }
                 const uint32_t d = tmem + buf * BN;
                 const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
-                constexpr int a_smem = FUSED ? 0 : kATile;
+                constexpr int a_smem = Cfg::TM ? 0 : kATile;
                 auto A = [&](int i) { return st + i * a_smem; };
                 auto B = [&](int j) { return st + P * a_smem + j * Cfg::b_tile; };
                 const uint32_t a_tm0 = tmem + Cfg::a_tm_base + t * Cfg::a_tm_cols;
@@ -384,7 +410,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     tc_fence_after();
                     return r;
                 };
-                if constexpr (FUSED) {
+                if constexpr (Cfg::TM) {
                     // A pieces from tensor memory, 32 columns apart
                     auto pr = [&](int i, int j, bool first, bool shift) {
                         mma_pair_ta(d, a_tm0 + 32 * i, B(j), idesc, first, shift);
@@ -444,7 +470,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     mma_pair<1>(d, A(0), B(0), idesc, fresh, false);          // hi*hi
                 }
                 tc_commit_pair(empty0 + 8 * s);
-                if (FUSED) tc_commit_pair(atfree0 + 8 * t);    // tensor-memory A stage free
+                if (Cfg::TM) tc_commit_pair(atfree0 + 8 * t);    // tensor-memory A stage free
                 if (close) {
                     tc_commit_pair(cfull0 + 8 * buf);
                     ++part;
@@ -452,7 +478,85 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             }
         }
         if (!ok) *abort_flag = 1;
-    } else if (FUSED && warp >= 2 + Cfg::acc_warps) {
+    } else if (Cfg::SMS && warp >= 2 + Cfg::acc_warps) {
+        // ------------------------------------- split warps (shared memory)
+        // For every K block of this cluster's units, in the producer's order:
+        // prefetch this warp's rows of the block two ahead into L2; once the
+        // MMA has consumed the block that last used stage s, read this CTA's
+        // 128 rows x 64 K of FP32 A (warp w: rows 16 w .. +15, four rows per
+        // step, eight lanes per row, 8 floats per lane), split them and store
+        // the three pieces into the stage's A half in the 128-byte swizzled
+        // K-major layout the MMA reads (16-byte chunk j of row r at chunk
+        // j ^ (r % 8): the eight lanes of a row hit eight bank groups; zeros
+        // past M and K); fence for the tensor core, meet the other split
+        // warps, and one thread counts this CTA in on the leader's barrier.
+        const int sw = warp - 2 - Cfg::acc_warps;
+        const int rsub = lane >> 3, chunk = lane & 7, c8 = chunk * 8;
+        const uint32_t aready_leader0 = map_to_rank(aready0, 0);
+        uint32_t g = 0;
+        bool ok = true;
+        for (int i = 0; i < nunits && ok; ++i) {
+            const Unit w = sched_unit(sch, cluster_id, i);
+            int tm, tn;
+            tile_pos(w.tile, p.tiles_m, p.tiles_n, tm, tn);
+            const int arow = tm * kBM + int(rank) * kHalfRows;
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+                const uint32_t s = g % S, ph = (g / S) & 1;
+                if (kb + 2 < w.kb1) {
+                    const int prow = arow + 16 * sw + (lane & 15);
+                    const int pk = (kb + 2) * 64 + 32 * (lane >> 4);
+                    if (prow < p.M && pk < p.K)
+                        asm volatile("prefetch.global.L2 [%0];"
+                                     :: "l"(p.A32 + (int64_t)prow * p.lda + pk));
+                }
+                // this block's FP32 rows first: their latency overlaps the wait
+                const int k = kb * 64 + c8;
+                float4 x[4][2];
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int row = arow + 16 * sw + 4 * it + rsub;
+                    x[it][0] = x[it][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (row < p.M && k < p.K) {
+                        const float* src = p.A32 + (int64_t)row * p.lda + k;
+                        if (k + 7 < p.K) {
+                            x[it][0] = __ldg(reinterpret_cast<const float4*>(src));
+                            x[it][1] = __ldg(reinterpret_cast<const float4*>(src + 4));
+                        } else {
+                            float t[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            for (int j = 0; j < 8 && k + j < p.K; ++j) t[j] = src[j];
+                            x[it][0] = make_float4(t[0], t[1], t[2], t[3]);
+                            x[it][1] = make_float4(t[4], t[5], t[6], t[7]);
+                        }
+                    }
+                }
+                bool good = mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) &&
+                            !*abort_flag;
+                if (good) {
+                    const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        uint4 q0, q1, q2;
+                        split_bf16x3_pair(x[it][0].x, x[it][0].y, q0.x, q1.x, q2.x);
+                        split_bf16x3_pair(x[it][0].z, x[it][0].w, q0.y, q1.y, q2.y);
+                        split_bf16x3_pair(x[it][1].x, x[it][1].y, q0.z, q1.z, q2.z);
+                        split_bf16x3_pair(x[it][1].z, x[it][1].w, q0.w, q1.w, q2.w);
+                        const int r = 16 * sw + 4 * it + rsub;
+                        const uint32_t off = r * 128 + ((chunk ^ (r & 7)) << 4);
+                        st_shared_v4(st + off, q0);
+                        st_shared_v4(st + kATile + off, q1);
+                        st_shared_v4(st + 2 * kATile + off, q2);
+                    }
+                    fence_proxy_async_smem();        // generic writes -> the tensor core
+                }
+                if (!bar_and(kSplitBarrier, kSmemSplitWarps * 32, good)) {
+                    ok = false;
+                    break;
+                }
+                if (sw == 0 && lane == 0) mbar_arrive_remote(aready_leader0 + 8 * s);
+            }
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (Cfg::TM && warp >= 2 + Cfg::acc_warps) {
         // ------------------------------------------------------ split warps
         // Split every K block of this cluster's tiles, as soon as its FP32
         // block has landed and its tensor-memory A stage is free, ahead of
@@ -774,6 +878,9 @@ cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
 }  // namespace
 
 int gemm_kblock_clusters(int mode, int bn, int fused, int sms) {
+    if (fused == 3)
+        return bn == 128 ? max_clusters_t<kModeBf16x9, 128, 3>(sms)
+                         : max_clusters_t<kModeBf16x9, 256, 3>(sms);
     if (fused) return max_clusters_t<kModeBf16x9, 128, 1>(sms);
     switch (mode) {
         case kModeTf32x3:
@@ -809,7 +916,11 @@ cudaError_t launch_gemm_kblock(int mode, int bn, int fused, const CUtensorMap& m
     }
     const int clusters = sched_grid_clusters(tiles, q.tail_tiles, q.tail_clusters, resident);
     cudaError_t e;
-    if (fused) {
+    if (fused == 3) {
+        if (mode != kModeBf16x9 || !q.A32) return cudaErrorInvalidValue;
+        e = bn == 128 ? launch_kblock_t<kModeBf16x9, 128, 3>(mapA, mapB, mapC, q, clusters, stream, pdl)
+                      : launch_kblock_t<kModeBf16x9, 256, 3>(mapA, mapB, mapC, q, clusters, stream, pdl);
+    } else if (fused) {
         if (mode != kModeBf16x9 || bn != 128) return cudaErrorInvalidValue;
         e = launch_kblock_t<kModeBf16x9, 128, 1>(mapA, mapB, mapC, q, clusters, stream, pdl);
     } else if (mode == kModeTf32x3) {

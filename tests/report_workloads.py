@@ -169,10 +169,11 @@ def main():
             mi, ni = W.sample_pairs(g0.M, g0.N, args.samples)
             Cref, Sabs = oracle.gemm_ref(A, B, g0.transA, g0.transB, g0.alpha, g0.beta, C0,
                                          pairs=(mi, ni))
-        modes = ["bf16x9", "bf16x9_fused", "tf32x3", "tf32x3_oy", "bf16x3", "tf32", "fp32_simt"]
+        modes = ["bf16x9", "bf16x9_fused", "bf16x9_fused_tmem", "tf32x3", "tf32x3_oy", "bf16x3",
+                 "tf32", "fp32_simt"]
         for mode_name in modes:
-            mode = mode_name.replace("_fused", "")
-            emu.emu_set_path("fused" if mode_name.endswith("_fused") else "twopass")
+            mode, _, path = mode_name.partition("_") if mode_name.startswith("bf16x9_") else (mode_name, "", "")
+            emu.emu_set_path(path or "twopass")
             dC = torch.from_numpy(C0).cuda() if C0 is not None else torch.empty((g0.M, g0.N), device="cuda")
             dC0 = dC.clone() if C0 is not None else None
 

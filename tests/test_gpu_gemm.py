@@ -263,16 +263,22 @@ def test_host_entry_pipelined_rows_match_one_call(emu, transA, transB, beta, mod
         assert np.array_equal(dev, host)
 
 
-def test_host_entry_pipelined_fused_shape(emu):
-    """N = 256 rows of an MLIP layer: the fused path in every chunk, B's
-    pieces split once and reused."""
+@pytest.mark.parametrize("path", ["auto", "fused_tmem"])
+def test_host_entry_pipelined_fused_shape(emu, path):
+    """N = 256 rows of an MLIP layer: an on-chip path in every chunk (AUTO
+    takes the shared-memory one), B's pieces split once and reused."""
     g = W.WORKLOADS["mlip192_k256_n256"]
     M = 70000
     r = W.rng(19)
     A = W.normal(r, (M, g.K))
     B = W.normal(r, (g.N, g.K), std=g.K ** -0.5)
-    dev = _run(emu, A, B, transB=True)
-    host = emu.emu_sgemm_host(A, B, transB=True)
+    old = emu.emu_get_path()
+    emu.emu_set_path(path)
+    try:
+        dev = _run(emu, A, B, transB=True)
+        host = emu.emu_sgemm_host(A, B, transB=True)
+    finally:
+        emu.emu_set_path(old)
     # the one call splits its last wave along K, the two chunks do not: the
     # results agree within the accuracy bound, element by element
     mi, ni = W.sample_pairs(M, g.N, 2048, seed=4)
@@ -295,18 +301,24 @@ def test_no_device_error_recorded(emu):
     assert emu.emu_get_last_device_error() == 0
 
 
-# --------------------------------------------------------- the fused path --
-# EMU_PATH_FUSED: A is read as FP32 and split in shared memory by the GEMM
-# kernel (BF16x9, K-major A with 16-byte-aligned rows); otherwise the call
+# ------------------------------------------------------ the on-chip paths --
+# EMU_PATH_FUSED: the GEMM kernel's split warps read FP32 A and store its
+# pieces into the shared-memory stages (256-wide tiles); EMU_PATH_FUSED_TMEM:
+# A is loaded as FP32 and split into tensor memory (128-wide tiles).  Both
+# take BF16x9 with K-major A with 16-byte-aligned rows; otherwise the call
 # falls back to the two-pass path.
 
+ON_CHIP = ["fused", "fused_tmem"]
+
+
 class _fused_path:
-    def __init__(self, emu):
+    def __init__(self, emu, path="fused"):
         self.emu = emu
+        self.path = path
 
     def __enter__(self):
         self.old = self.emu.emu_get_path()
-        self.emu.emu_set_path("fused")
+        self.emu.emu_set_path(self.path)
 
     def __exit__(self, *exc):
         self.emu.emu_set_path(self.old)
@@ -315,13 +327,14 @@ class _fused_path:
 @pytest.mark.parametrize("shape", SHAPES + [(1000, 700, 300), (257, 129, 4096)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("transB", [0, 1])
-def test_fused_path_every_element(emu, shape, transB):
+@pytest.mark.parametrize("path", ON_CHIP)
+def test_fused_path_every_element(emu, shape, transB, path):
     M, N, K = shape
     r = W.rng(M * 11 + N * 5 + K + transB)
     A = W.normal(r, (M, K))
     B = W.normal(r, (N, K) if transB else (K, N))
     C0 = W.uniform(r, (M, N))
-    with _fused_path(emu):
+    with _fused_path(emu, path):
         C = _run(emu, A, B, False, transB, 1.5, -0.75, C0, "bf16x9")
     Cref, Sabs = oracle.gemm_ref(A, B, False, transB, 1.5, -0.75, C0)
     assert checks.error_ratio(C, Cref, Sabs, K, 1.5, -0.75, C0) <= 1.0
@@ -330,10 +343,11 @@ def test_fused_path_every_element(emu, shape, transB):
     assert np.all(np.abs(C.astype(np.float64) - C2) <= bound)
 
 
-def test_fused_path_identity_is_exact_and_falls_back_when_needed(emu):
+@pytest.mark.parametrize("path", ON_CHIP)
+def test_fused_path_identity_is_exact_and_falls_back_when_needed(emu, path):
     X = W.normal(W.rng(31), (256, 256))
     I = np.eye(256, dtype=np.float32)
-    with _fused_path(emu):
+    with _fused_path(emu, path):
         assert np.array_equal(_run(emu, I, X), X)
         assert np.array_equal(_run(emu, X, I), X)
         # transposed A and a misaligned row stride take the two-pass path
@@ -345,14 +359,16 @@ def test_fused_path_identity_is_exact_and_falls_back_when_needed(emu):
 
 @pytest.mark.parametrize("name", ["mlip17280_k256_n256", "mlip17280_k1024_n256",
                                   "mlip17280_k256_n1024"])
-def test_fused_path_mlip17280_sampled(emu, name):
-    with _fused_path(emu):
+@pytest.mark.parametrize("path", ON_CHIP)
+def test_fused_path_mlip17280_sampled(emu, name, path):
+    with _fused_path(emu, path):
         ratio, relf, _, _ = _sampled_check(emu, W.WORKLOADS[name], "bf16x9")
     assert ratio <= 1.0 and relf <= checks.FROBENIUS_TOL, (ratio, relf)
 
 
-def test_fused_path_square8192_sampled(emu):
-    with _fused_path(emu):
+@pytest.mark.parametrize("path", ON_CHIP)
+def test_fused_path_square8192_sampled(emu, path):
+    with _fused_path(emu, path):
         ratio, relf, _, _ = _sampled_check(emu, W.WORKLOADS["square8192_normal"], "bf16x9")
     assert ratio <= 1.0 and relf <= checks.FROBENIUS_TOL, (ratio, relf)
 
@@ -415,7 +431,9 @@ def test_tail_split_shapes(emu, shape, mode):
     ((300, 384, 4100), True, "auto"),         # 4 tiles of 65 blocks (last one ragged), 8 parts
     ((12288, 256, 1024), False, "twopass"),   # 48 tiles of 16 blocks, stream-K over 76
     ((12288, 256, 4096), True, "twopass"),    # 48 tiles of 64 blocks, stream-K in every mode
-    ((12288, 256, 1024), False, "fused"),     # 96 tiles: 20 left over, 3 parts each
+    ((12288, 256, 1024), False, "fused_tmem"),  # 96 tiles: 20 left over, 3 parts each
+    ((12288, 256, 1024), False, "fused"),     # 48 tiles of 16 blocks, stream-K over 76
+    ((1536, 512, 700), True, "fused"),        # 12 tiles of 11 blocks, 5 parts each
 ], ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 @pytest.mark.parametrize("mode", ["bf16x9", "tf32x3", "bf16x3", "tf32", "tf32x3_oy"])
 def test_tail_parts_with_alpha_beta(emu, shape, transB, path, mode):
@@ -424,8 +442,8 @@ def test_tail_parts_with_alpha_beta(emu, shape, transB, path, mode):
     clusters -- with alpha, beta and C0 applied once by the tile's owner:
     within each mode's bound on every element (sampled on the largest
     shapes) and the same bits on a second call."""
-    if path == "fused" and mode != "bf16x9":
-        pytest.skip("the fused path is BF16x9 only")
+    if path in ON_CHIP and mode != "bf16x9":
+        pytest.skip("the on-chip paths are BF16x9 only")
     M, N, K = shape
     r = W.rng(M + 5 * N + 11 * K)
     A = W.normal(r, (M, K))
@@ -478,7 +496,7 @@ def test_non_finite_operands_follow_the_split(emu, mode):
     assert checks.error_ratio(C[m], Cref[m], Sabs[m], 64, 1.0, 0.0, mode=mode) <= 1.0
 
 
-@pytest.mark.parametrize("path", ["auto", "fused", "twopass"])
+@pytest.mark.parametrize("path", ["auto", "fused", "fused_tmem", "twopass"])
 def test_misaligned_operands_and_long_k(emu, path):
     """Operands that start 4 bytes past a 16-byte boundary (the fused path and
     the 16-byte split kernels must step aside), C likewise, and a one-tile

@@ -22,13 +22,15 @@ def emu():
                                         ((256, 256, 4096), "twopass"),
                                         ((12288, 256, 1024), "twopass"),
                                         ((70000, 256, 256), "fused"),
+                                        ((70000, 256, 256), "fused_tmem"),
+                                        ((4096, 4096, 512), "fused"),
                                         ((1000, 700, 300), "auto")],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else v)
 @pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
 def test_graph_replay_matches_direct_calls(emu, shape, path, mode):
     import torch
-    if path == "fused" and mode != "bf16x9":
-        pytest.skip("the fused path is BF16x9 only")
+    if path in ("fused", "fused_tmem") and mode != "bf16x9":
+        pytest.skip("the on-chip paths are BF16x9 only")
     M, N, K = shape
     emu.emu_set_path(path)
     g = torch.Generator(device="cuda").manual_seed(M + N + K)
