@@ -43,23 +43,33 @@
 // that part's FP32 sums and a flag in global memory, and the part holding the
 // tile's first K block adds them in K order and writes C.
 //
-// Fused A (BF16x9, BN = 128): the producer loads the FP32 A block (128 rows
-// x 64, two 128-byte-swizzled boxes) into one of two staging buffers;
-// sixteen split warps turn it (16 elements per thread) into the three BF16
-// pieces and store them into tensor memory (tcgen05.st; two 96-column A
-// stages beside two 128-column accumulator buffers), fence, meet at a named
-// barrier, and one thread signals the leader CTA; the MMA reads A from tensor
-// memory and only B's pieces from shared memory.
+// Fused A in shared memory (BF16x9, FUSED = 3, BN = 256 or 128): the
+// two-pass layout, but the producer loads only B's pieces; eight split warps
+// read each K block of FP32 A from global memory (prefetched into L2 two
+// blocks ahead, loaded before the stage-free wait), split it and store the
+// three pieces into the stage's A half in the same 128-byte swizzled layout
+// the TMA would have written, fence, meet at a named barrier, and one
+// thread signals the leader CTA, whose MMA waits for both CTAs' halves.
 //
-// Warps (576 threads per CTA, 832 when fused):
+// Fused A in tensor memory (BF16x9, FUSED = 1, BN = 128): the producer
+// loads the FP32 A block (128 rows x 64, two 128-byte-swizzled boxes) into
+// one of two staging buffers; sixteen split warps turn it (16 elements per
+// thread) into the three BF16 pieces and store them into tensor memory
+// (tcgen05.st; two 96-column A stages beside two 128-column accumulator
+// buffers), fence, meet at a named barrier, and one thread signals the
+// leader CTA; the MMA reads A from tensor memory and only B's pieces from
+// shared memory.
+//
+// Warps (576 threads per CTA; 832 on either fused path):
 //   warp 0      TMA producer (both CTAs; completion counted on the leader's
 //               barriers) and tensor-memory allocation
 //   warp 1      MMA issuer (leader CTA only)
-//   warps 2..   accumulators (16, or 8 when fused): warp w owns TMEM lanes
-//               32(w%4)..+31 and column group (w-2)/4 of the tile (BN/4, or
-//               BN/2 when fused, FP32 registers per thread) and writes
-//               C = alpha*acc + beta*C
-//   then        (fused) 16 split warps.
+//   warps 2..   accumulators (16, or 8 in tensor-memory fused): warp w owns
+//               TMEM lanes 32(w%4)..+31 and column group (w-2)/4 of the tile
+//               (BN/4, or BN/2 in tensor-memory fused, FP32 registers per
+//               thread) and writes C = alpha*acc + beta*C
+//   then        split warps: 8 (shared-memory fused) or 16 (tensor-memory
+//               fused).
 #include "emu_device.cuh"
 #include "schedule.h"
 
