@@ -248,6 +248,12 @@ def bench_gpu(args):
     out["clocks"] = clocks.summary()
 
     if rank == 0:
+        if not args.no_configs:
+            del dA, dB, dC
+            torch.cuda.empty_cache()
+            out["configs"] = bench_configs(emu, stream, peaks, peak_src)
+            dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+            dC = torch.from_numpy(C0).cuda() if C0 is not None else torch.empty((g.M, g.N), device="cuda")
         if not args.no_e2e:
             out["e2e"] = bench_e2e(emu, g, A, B, C0, stream, args)
         if not args.no_simt and g.mode != "fp32_simt":
@@ -259,6 +265,142 @@ def bench_gpu(args):
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------ every config --
+
+# The benchmark's configurations besides the headline one: the 256^3 GEMM,
+# the three linear layers of a transformer interatomic potential on the
+# edge tokens of a 192-atom and of a 17,280-atom system (M = atoms x 64),
+# the dynamic-range stress GEMM with alpha and beta, and the 8192^3 GEMM in
+# TF32x3 mode.
+CONFIG_WORKLOADS = ["square256_uniform",
+                    "mlip192_k256_n256", "mlip192_k256_n1024", "mlip192_k1024_n256",
+                    "mlip17280_k256_n256", "mlip17280_k256_n1024", "mlip17280_k1024_n256",
+                    "stress4096", "square8192_normal_tf32x3"]
+
+
+def device_operands(g):
+    """A, B (and C0) of workload g drawn on the GPU with a seeded torch
+    generator: the distributions of the workload (workloads.py), not its
+    exact values (drawing 4.5 GB on the host would take minutes)."""
+    import torch
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1000 + g.seed)
+    a_shape = (g.K, g.M) if g.transA else (g.M, g.K)
+    b_shape = (g.N, g.K) if g.transB else (g.K, g.N)
+
+    def normal(shape, std=1.0):
+        x = torch.randn(shape, generator=gen, device="cuda")
+        return x.mul_(std) if std != 1.0 else x
+
+    def uniform(shape):
+        return torch.rand(shape, generator=gen, device="cuda").mul_(2.0).sub_(1.0)
+
+    def stress(shape):
+        # sign * m * 2^e, m ~ U[1, 2), e ~ U{-30..30}; 1% zeros, 0.1% subnormals
+        n = 1
+        for d in shape:
+            n *= d
+        sign = torch.where(torch.rand(n, generator=gen, device="cuda") < 0.5, -1.0, 1.0)
+        m = torch.rand(n, generator=gen, device="cuda").add_(1.0)
+        e = torch.randint(-30, 31, (n,), generator=gen, device="cuda", dtype=torch.int32)
+        x = torch.ldexp(sign * m, e.float())
+        u = torch.rand(n, generator=gen, device="cuda")
+        x[u < 0.01] = 0.0
+        bits = torch.randint(1, 1 << 23, (n,), generator=gen, device="cuda", dtype=torch.int32)
+        bits = bits | torch.where(sign < 0, torch.tensor(-(1 << 31), dtype=torch.int32, device="cuda"),
+                                  torch.tensor(0, dtype=torch.int32, device="cuda"))
+        sub = (u >= 0.01) & (u < 0.011)
+        x[sub] = bits.view(torch.float32)[sub]
+        return x.view(shape)
+
+    if g.dist == "mlip":
+        return normal(a_shape), normal(b_shape, g.K ** -0.5), None
+    draw = {"normal": normal, "uniform": uniform, "stress": stress}[g.dist]
+    A, B = draw(a_shape), draw(b_shape)
+    C0 = uniform((g.M, g.N)) if g.beta != 0.0 else None
+    return A, B, C0
+
+
+def bench_configs(emu, stream, peaks, peak_src, reps=10):
+    """Each configuration timed two ways: single calls on a cold L2 (a 256 MB
+    buffer is written between calls, outside the timed region; the median of
+    `reps` calls, CUDA events around each call on the launching stream), and
+    `reps` calls back to back (the steady state of consecutive layers, events
+    around the run).  Single calls are compared with the burst BF16 peak,
+    back-to-back runs with the sustained one (MEASURED_PEAKS.json).  The
+    dominant kernel's time per launch comes from the library's own events."""
+    import torch
+    from fp32_emulated_gemm_split_gb300 import workloads as W
+    p_bf16 = float(peaks["bf16_tflops"])
+    p_sus = float(peaks.get("bf16_tflops_sustained", p_bf16))
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")     # 256 MB > L2
+    res = {}
+    for name in CONFIG_WORKLOADS:
+        g = W.WORKLOADS[name]
+        A, B, C0 = device_operands(g)
+        C = C0.clone() if C0 is not None else torch.empty((g.M, g.N), device="cuda")
+
+        def call():
+            emu.emu_sgemm(A, B, C, transA=g.transA, transB=g.transB, alpha=g.alpha, beta=g.beta,
+                          mode=g.mode, stream=stream)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        emu.emu_profile_enable(True)
+        evs = []
+        for _ in range(reps):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            call()
+            e.record(stream)
+            evs.append((s, e))
+        torch.cuda.synchronize()
+        prof = {k: emu.emu_profile_read(k) for k in ("split", "gemm_tc", "gemm_fused", "gemm_simt")}
+        emu.emu_profile_enable(False)
+        single = statistics.median(s.elapsed_time(e) for s, e in evs)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(reps):
+            call()
+        e.record(stream)
+        torch.cuda.synchronize()
+        b2b = s.elapsed_time(e) / reps
+        dom = "gemm_fused" if prof["gemm_fused"][0] > 0 else "gemm_tc"
+        n_dom, ms_dom = prof[dom]
+        k_ms = ms_dom / max(n_dom, 1)
+        products = {"bf16x9": 9, "tf32x3": 3}[g.mode]
+        tf32 = g.mode == "tf32x3"
+        peak = p_bf16 / 2.0 if tf32 else p_bf16
+        entry = {
+            "M": g.M, "N": g.N, "K": g.K, "mode": g.mode, "transB": g.transB,
+            "alpha": g.alpha, "beta": g.beta,
+            "path": "on-chip split of A" if dom == "gemm_fused" else "two-pass",
+            "value": round(g.flops / (single * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms": round(single, 4),
+            "pct_bf16_peak_over_9": round(100.0 * g.flops / (single * 1e-3) / 1e12 / (p_bf16 / 9), 1),
+            "b2b_value": round(g.flops / (b2b * 1e-3) / 1e12, 2), "b2b_ms": round(b2b, 4),
+            "b2b_pct_sustained_peak_over_9": round(
+                100.0 * g.flops / (b2b * 1e-3) / 1e12 / (p_sus / 9), 1),
+            "kernel": dom, "kernel_ms": round(k_ms, 4),
+            "kernel_frac": round(products * g.flops / (k_ms * 1e-3) / 1e12 / peak, 4),
+            "split_ms": round(prof["split"][1] / max(reps, 1), 4),
+        }
+        if tf32:
+            entry["pct_bf16_peak_over_6"] = round(
+                100.0 * g.flops / (single * 1e-3) / 1e12 / (p_bf16 / 6), 1)
+        res[name] = entry
+        del A, B, C, C0
+        torch.cuda.empty_cache()
+    res["_how"] = ("operands drawn on the GPU (seeded torch generator, the workloads' "
+                   "distributions); value: median of single calls with L2 flushed before each "
+                   f"(% of burst P/9, {peak_src}); b2b: calls back to back (% of sustained P/9); "
+                   "kernel_frac: tensor FLOPs per launch / kernel time / peak "
+                   "(TF32: half the BF16 peak)")
+    return res
 
 
 def pick_workload(W, args):
@@ -438,6 +580,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-simt", action="store_true", help="skip the SIMT FP32 context number")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the timing of the other configurations")
     ap.add_argument("--shape", default=None, help="M,N,K override (same distribution)")
     ap.add_argument("--path", default=None, choices=[None, "auto", "twopass", "fused", "fused_tmem"],
                     help="implementation of the tensor-core modes (default: the library's)")

@@ -104,16 +104,8 @@ emu_status_t from_cuda(cudaError_t e) {
 }
 
 // Tile width of the K-block kernel on the two-pass path: 128 when N <= 128
-// (a 256-wide tile would compute at least half zeros), else 256;
-// EMU_SGEMM_BN=128 or 256 fixes it.
-int kblock_bn(int64_t N) {
-    static int v = -1;
-    if (v < 0) {
-        const char* s = std::getenv("EMU_SGEMM_BN");
-        v = !s ? 0 : (std::strcmp(s, "128") == 0 ? 128 : (std::strcmp(s, "256") == 0 ? 256 : 0));
-    }
-    return v ? v : (N <= 128 ? 128 : 256);
-}
+// (a 256-wide tile would compute at least half zeros), else 256.
+int kblock_bn(int64_t N) { return N <= 128 ? 128 : 256; }
 
 int read_strategy_env() {
     const char* s = std::getenv("EMU_SGEMM_STRATEGY");
@@ -280,6 +272,26 @@ emu_status_t plan_tail(TcGemmParams& p, int mode, int bm, int bn, int fused, Dev
     p.flags = d->flags;
     p.epoch = ++d->epoch == 0 ? ++d->epoch : d->epoch;   // never 0 (the flags' initial value)
     return EMU_OK;
+}
+
+// a * b + c, or false when it does not fit in 62 bits (no allocation that
+// large can succeed; the check keeps every later size product from wrapping).
+bool fits_mul_add(uint64_t a, uint64_t b, uint64_t c, size_t* out) {
+    uint64_t p = 0;
+    if (__builtin_mul_overflow(a, b, &p) || __builtin_add_overflow(p, c, &p) ||
+        p > (uint64_t(1) << 62))
+        return false;
+    *out = (size_t)p;
+    return true;
+}
+
+// The largest workspace any mode needs for this shape: 3 pieces x 4 bytes x
+// ldp per row of op(A) and op(B)^T, plus the 1 KB alignment of A's region.
+// Beyond 2^62 bytes the call returns EMU_ERR_ALLOC before any size product
+// is formed (M, N, K up to INT32_MAX would otherwise wrap a 64-bit size).
+bool workspace_fits(int64_t M, int64_t N, int64_t K) {
+    size_t bytes = 0;
+    return fits_mul_add((uint64_t)M + (uint64_t)N, 12 * (uint64_t)plane_ld(K), 2048, &bytes);
 }
 
 emu_status_t check_gemm_args(int transA, int transB, int64_t M, int64_t N, int64_t K,
@@ -515,6 +527,7 @@ emu_status_t sgemm_device(int transA, int transB, int64_t M, int64_t N, int64_t 
     emu_status_t st = check_gemm_args(transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, mode);
     if (st != EMU_OK) return st;
     if (M == 0 || N == 0) return EMU_OK;
+    if (!workspace_fits(M, N, K)) return EMU_ERR_ALLOC;
     DeviceState* d = nullptr;
     st = current_device(&d);
     if (st != EMU_OK) return st;
@@ -655,11 +668,18 @@ emu_status_t emu_sgemm_host(int transA, int transB, int64_t M, int64_t N, int64_
     DeviceState* d = nullptr;
     st = current_device(&d);
     if (st != EMU_OK) return st;
-    // stored extents: A is (transA ? K : M) rows of lda, B is (transB ? N : K) rows of ldb
+    if (!workspace_fits(M, N, K)) return EMU_ERR_ALLOC;
+    // stored extents: A is (transA ? K : M) rows of lda, B is (transB ? N : K)
+    // rows of ldb; sizes that do not fit in 62 bits cannot be staged
     const int64_t a_rows = transA ? K : M, b_rows = transB ? N : K;
-    const size_t a_bytes = K > 0 ? (size_t)((a_rows - 1) * lda + (transA ? M : K)) * 4 : 0;
-    const size_t b_bytes = K > 0 ? (size_t)((b_rows - 1) * ldb + (transB ? K : N)) * 4 : 0;
-    const size_t c_bytes = (size_t)((M - 1) * ldc + N) * 4;
+    size_t a_el = 0, b_el = 0, c_el = 0;
+    if (K > 0 && (!fits_mul_add((uint64_t)(a_rows - 1), (uint64_t)lda, (uint64_t)(transA ? M : K), &a_el) ||
+                  !fits_mul_add((uint64_t)(b_rows - 1), (uint64_t)ldb, (uint64_t)(transB ? K : N), &b_el)))
+        return EMU_ERR_ALLOC;
+    if (!fits_mul_add((uint64_t)(M - 1), (uint64_t)ldc, (uint64_t)N, &c_el) ||
+        (a_el + b_el + c_el) > (size_t(1) << 60))
+        return EMU_ERR_ALLOC;
+    const size_t a_bytes = a_el * 4, b_bytes = b_el * 4, c_bytes = c_el * 4;
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     st = ensure_buffer(&d->stage, &d->stage_bytes, up(a_bytes) + up(b_bytes) + up(c_bytes));
     if (st != EMU_OK) return st;
@@ -691,7 +711,10 @@ emu_status_t emu_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_
     emu_status_t st = check_split_args(X, rows, cols, ld, trans, P0, P1, P2, ldp);
     if (st != EMU_OK || rows == 0 || cols == 0) return st;
     DeviceState* d = nullptr;
-    st = current_device(&d);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        st = current_device(&d);
+    }
     if (st != EMU_OK) return st;
     return from_cuda(launch_split_bf16x3(X, rows, cols, ld, trans, P0, P1, P2, ldp,
                                          reinterpret_cast<cudaStream_t>(stream)));
@@ -702,7 +725,10 @@ emu_status_t emu_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_
     emu_status_t st = check_split_args(X, rows, cols, ld, trans, HI, LO, LO, ldp);
     if (st != EMU_OK || rows == 0 || cols == 0) return st;
     DeviceState* d = nullptr;
-    st = current_device(&d);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        st = current_device(&d);
+    }
     if (st != EMU_OK) return st;
     return from_cuda(launch_split_tf32x2(X, rows, cols, ld, trans, HI, LO, ldp,
                                          reinterpret_cast<cudaStream_t>(stream)));
@@ -714,7 +740,10 @@ emu_status_t emu_split_tf32x2_scaled(const float* X, int64_t rows, int64_t cols,
     emu_status_t st = check_split_args(X, rows, cols, ld, trans, HI, LO, LO, ldp);
     if (st != EMU_OK || rows == 0 || cols == 0) return st;
     DeviceState* d = nullptr;
-    st = current_device(&d);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        st = current_device(&d);
+    }
     if (st != EMU_OK) return st;
     return from_cuda(launch_split_tf32x2(X, rows, cols, ld, trans, HI, LO, ldp,
                                          reinterpret_cast<cudaStream_t>(stream), 2048.0f));
@@ -755,6 +784,7 @@ int emu_choose_mode(int64_t M, int64_t N, int64_t K, int mode, int strategy, int
     if (strategy != EMU_STRATEGY_EAGER && strategy != EMU_STRATEGY_PERFORMANT) return -1;
     if (sms <= 0) {
         DeviceState* d = nullptr;
+        std::lock_guard<std::mutex> lock(g_mu);
         if (current_device(&d) != EMU_OK) return -1;
         sms = d->sms;
     }
@@ -769,7 +799,8 @@ double emu_predict_us(int64_t M, int64_t N, int64_t K, int mode, int sms) {
 
 size_t emu_workspace_size(int64_t M, int64_t N, int64_t K, int mode) {
     if (M <= 0 || N <= 0 || K <= 0 || mode == EMU_MODE_FP32_SIMT) return 0;
-    if (!valid_mode(mode)) return 0;
+    if (!valid_mode(mode) || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return 0;
+    if (!workspace_fits(M, N, K)) return SIZE_MAX;
     const size_t per = (size_t)mode_pieces(mode) * plane_ld(K) * mode_piece_bytes(mode);
     return (per * M + 1023) / 1024 * 1024 + per * N;
 }
@@ -793,7 +824,11 @@ emu_status_t emu_clear_device_error(void) {
 emu_status_t emu_selftest_timeout(int limit_us, emu_stream_t stream) {
     if (limit_us < 1 || limit_us > 1000000) return EMU_ERR_INVALID_VALUE;
     DeviceState* d = nullptr;
-    emu_status_t st = current_device(&d);
+    emu_status_t st;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        st = current_device(&d);
+    }
     if (st != EMU_OK) return st;
     cudaError_t e = launch_timeout_probe(d->err, (uint64_t)limit_us * 1000ull,
                                          reinterpret_cast<cudaStream_t>(stream));

@@ -70,6 +70,8 @@
 //               thread) and writes C = alpha*acc + beta*C
 //   then        split warps: 8 (shared-memory fused) or 16 (tensor-memory
 //               fused).
+#include <mutex>
+
 #include "emu_device.cuh"
 #include "schedule.h"
 
@@ -814,17 +816,45 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     }
 }
 
+// Host-side state of one kernel variant, per device: whether its dynamic
+// shared-memory limit has been raised there, and how many of its clusters
+// can be resident.  emu_sgemm and emu_sgemm_noalloc take different locks, so
+// this state has a lock of its own: their first calls may come from two
+// host threads at once.
+constexpr int kMaxDevices = 64;
+struct VariantState {
+    std::mutex mu;
+    bool attr[kMaxDevices] = {};
+    int clusters[kMaxDevices] = {};
+};
+
+template <int MODE, int BN, int FUSED>
+VariantState& variant_state() {
+    static VariantState st;
+    return st;
+}
+
+int current_device_index() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+template <int MODE, int BN, int FUSED>
+cudaError_t set_smem_attr_locked(VariantState& st, int dev) {
+    using Cfg = KCfg<MODE, BN, FUSED>;
+    if (dev >= 0 && st.attr[dev]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(gemm_kblock_kernel<MODE, BN, FUSED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::smem);
+    if (e == cudaSuccess && dev >= 0) st.attr[dev] = true;
+    return e;
+}
+
 template <int MODE, int BN, int FUSED>
 cudaError_t set_smem_attr() {
-    using Cfg = KCfg<MODE, BN, FUSED>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kblock_kernel<MODE, BN, FUSED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    return cudaSuccess;
+    VariantState& st = variant_state<MODE, BN, FUSED>();
+    std::lock_guard<std::mutex> lock(st.mu);
+    return set_smem_attr_locked<MODE, BN, FUSED>(st, current_device_index());
 }
 
 // Clusters of this kernel that can be resident at once (at most sms / 2).
@@ -834,10 +864,13 @@ cudaError_t set_smem_attr() {
 template <int MODE, int BN, int FUSED>
 int max_clusters_t(int sms) {
     using Cfg = KCfg<MODE, BN, FUSED>;
-    static int cached = -1;
-    if (cached < 0) {
-        int n = sms / 2;
-        if (set_smem_attr<MODE, BN, FUSED>() == cudaSuccess) {
+    VariantState& st = variant_state<MODE, BN, FUSED>();
+    std::lock_guard<std::mutex> lock(st.mu);
+    const int dev = current_device_index();
+    int n = dev >= 0 ? st.clusters[dev] : 0;
+    if (n <= 0) {
+        n = sms / 2;
+        if (set_smem_attr_locked<MODE, BN, FUSED>(st, dev) == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * (sms / 2));
             cfg.blockDim = dim3(threads_k<FUSED>());
@@ -856,9 +889,9 @@ int max_clusters_t(int sms) {
             else
                 cudaGetLastError();
         }
-        cached = n;
+        if (dev >= 0) st.clusters[dev] = n;
     }
-    return cached < sms / 2 ? cached : sms / 2;
+    return n < sms / 2 ? n : sms / 2;
 }
 
 template <int MODE, int BN, int FUSED>

@@ -138,10 +138,17 @@ extern "C" emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int
     const bool tf32 = mode_is_tf32(mode);
     const int pieces = mode_pieces(mode), es = mode_piece_bytes(mode);
     const int64_t ldp = plane_ld(K);
-    const size_t a_region = ((size_t)pieces * M * ldp * es + 1023) / 1024 * 1024;
-    const size_t need = a_region + (size_t)pieces * N * ldp * es;
     const bool uses_scratch = mode != EMU_MODE_FP32_SIMT && K > 0 && alpha != 0.0f;
-    if (uses_scratch && need > kNoAllocBytes) return EMU_ERR_INVALID_VALUE;   // too large
+    // Bytes of one row of pieces (at most 3 * 4 * (2^31 + 7), no overflow).
+    // M + N rows must fit before any product of sizes is formed: with M, N
+    // and K near INT32_MAX, (M + N) * row_bytes would wrap past 2^64.
+    const size_t row_bytes = (size_t)pieces * es * (size_t)ldp;
+    size_t a_region = 0;
+    if (uses_scratch) {
+        if ((size_t)M + (size_t)N > kNoAllocBytes / row_bytes) return EMU_ERR_INVALID_VALUE;
+        a_region = ((size_t)M * row_bytes + 1023) / 1024 * 1024;
+        if (a_region + (size_t)N * row_bytes > kNoAllocBytes) return EMU_ERR_INVALID_VALUE;
+    }
 
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     Slot* s = nullptr;

@@ -230,15 +230,23 @@ emu_status_t emu_split_tf32x2_scaled(const float* X, int64_t rows, int64_t cols,
  * in one fixed 64 MiB array in device memory, which every GPU that loads
  * the library holds until the process exits.
  *
- * Same arguments, layout, modes, results and error codes as emu_sgemm, and
- * the same kernels, with one limit: the pieces must fit in the array,
+ * Same arguments, layout, modes and error codes as emu_sgemm, and its
+ * results meet the same accuracy bound.  It always runs the two-pass split
+ * and GEMM kernels with 256-wide tiles, whole tiles only (no split of the
+ * last wave along K) and C stored by the epilogue warps, so its results are
+ * bit for bit emu_sgemm's only where emu_sgemm takes that same path (N > 128,
+ * no split tail, the two-pass path).  One limit: the pieces must fit in the
+ * array,
  *     BF16X9:  3 * 2 * (M + N) * ldp  bytes  (plus < 1 KB of alignment),
  *     TF32X3:  2 * 4 * (M + N) * ldp  bytes,   ldp = K rounded up to 8,
  *     BF16X3:  2 * 2 * (M + N) * ldp  bytes,   TF32: 1 * 4 * (M + N) * ldp,
  *     TF32X3_OY: as TF32X3,
  * at most 64 MiB; a larger request returns EMU_ERR_INVALID_VALUE and
- * launches nothing (FP32_SIMT and the K == 0 / alpha == 0 cases use no
- * scratch and have no limit).  The first call on a device, with that device
+ * launches nothing (the check is made before any size product is formed, so
+ * no M, N, K can wrap it; FP32_SIMT and the K == 0 / alpha == 0 cases use no
+ * scratch and have no limit).  Once the first call on a device has
+ * returned, later calls change neither the device's free memory nor any
+ * allocator's state.  The first call on a device, with that device
  * current, resolves the array's device address (cudaGetSymbolAddress) once;
  * make that first call before any stream capture.  All calls on a device
  * share the array: calls whose work overlaps on the GPU (other streams,
