@@ -335,7 +335,11 @@ def bench_configs(emu, stream, peaks, peak_src, reps=10):
     from fp32_emulated_gemm_split_gb300 import workloads as W
     p_bf16 = float(peaks["bf16_tflops"])
     p_sus = float(peaks.get("bf16_tflops_sustained", p_bf16))
-    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")     # 256 MB > L2
+    # L2 flush between single calls: write a 256 MB buffer (> L2), then read
+    # another, so that the flush's dirty lines are written back before the
+    # timed call rather than during it
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+    flush_r = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
     res = {}
     for name in CONFIG_WORKLOADS:
         g = W.WORKLOADS[name]
@@ -353,6 +357,7 @@ def bench_configs(emu, stream, peaks, peak_src, reps=10):
         evs = []
         for _ in range(reps):
             flush.zero_()
+            flush_r.sum()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             call()
@@ -392,14 +397,55 @@ def bench_configs(emu, stream, peaks, peak_src, reps=10):
         if tf32:
             entry["pct_bf16_peak_over_6"] = round(
                 100.0 * g.flops / (single * 1e-3) / 1e12 / (p_bf16 / 6), 1)
+        if g.dist == "mlip":
+            # the layer's weight split once and reused (emu_sgemm_bsplit):
+            # what a linear layer applied batch after batch runs
+            P = emu.emu_split_b(B, transB=g.transB, mode=g.mode)
+
+            def call_ws():
+                emu.emu_sgemm_bsplit(A, P, C, transA=g.transA, alpha=g.alpha, beta=g.beta,
+                                     mode=g.mode, stream=stream)
+
+            for _ in range(3):
+                call_ws()
+            torch.cuda.synchronize()
+            evs = []
+            for _ in range(reps):
+                flush.zero_()
+                flush_r.sum()
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                call_ws()
+                e.record(stream)
+                evs.append((s, e))
+            torch.cuda.synchronize()
+            ws_single = statistics.median(s.elapsed_time(e) for s, e in evs)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            for _ in range(reps):
+                call_ws()
+            e.record(stream)
+            torch.cuda.synchronize()
+            ws_b2b = s.elapsed_time(e) / reps
+            entry["weight_split_once"] = {
+                "value": round(g.flops / (ws_single * 1e-3) / 1e12, 2), "ms": round(ws_single, 4),
+                "pct_bf16_peak_over_9": round(
+                    100.0 * g.flops / (ws_single * 1e-3) / 1e12 / (p_bf16 / 9), 1),
+                "b2b_value": round(g.flops / (ws_b2b * 1e-3) / 1e12, 2), "b2b_ms": round(ws_b2b, 4),
+                "b2b_pct_sustained_peak_over_9": round(
+                    100.0 * g.flops / (ws_b2b * 1e-3) / 1e12 / (p_sus / 9), 1),
+                "api": "emu_sgemm_bsplit"}
+            del P
         res[name] = entry
         del A, B, C, C0
         torch.cuda.empty_cache()
     res["_how"] = ("operands drawn on the GPU (seeded torch generator, the workloads' "
                    "distributions); value: median of single calls with L2 flushed before each "
+                   "(a 256 MB buffer written, another read) "
                    f"(% of burst P/9, {peak_src}); b2b: calls back to back (% of sustained P/9); "
                    "kernel_frac: tensor FLOPs per launch / kernel time / peak "
-                   "(TF32: half the BF16 peak)")
+                   "(TF32: half the BF16 peak); weight_split_once: the layer's weight split "
+                   "once (emu_split_b) and every call through emu_sgemm_bsplit")
     return res
 
 

@@ -55,6 +55,9 @@ def _declare(L):
         getattr(L, name).restype = _int
     L.emu_sgemm_noalloc.argtypes = gemm
     L.emu_sgemm_noalloc.restype = _int
+    L.emu_sgemm_bsplit.argtypes = [_int, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp,
+                                   _i64, _int, _vp]
+    L.emu_sgemm_bsplit.restype = _int
     L.emu_split_bf16x3.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _vp, _i64, _vp]
     L.emu_split_bf16x3.restype = _int
     L.emu_split_tf32x2.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp, _i64, _vp]
@@ -173,6 +176,61 @@ def emu_sgemm_noalloc(A, B, C, *, transA=False, transB=False, alpha=1.0, beta=0.
                                  Bs.data_ptr(), ldb, float(beta), C.data_ptr(), max(ldc, N, 1),
                                  _mode(mode), _stream_handle(stream))
     _check(st, "emu_sgemm_noalloc")
+    return C
+
+
+PIECES = {"bf16x9": 3, "bf16x3": 2, "tf32x3": 2, "tf32x3_oy": 2, "tf32": 1}
+
+
+def emu_split_b(B, transB=False, mode="bf16x9", stream=None):
+    """The pieces of op(B)^T that emu_sgemm_bsplit takes, as one CUDA tensor
+    of shape (pieces, N, ldp) (int16 BF16 bits for the BF16 modes, float32
+    for the TF32 ones; ldp = K rounded up to 8), split by the library's own
+    split kernels."""
+    import torch
+    m = mode if isinstance(mode, str) else {v: k for k, v in MODE.items()}[int(mode)]
+    Bs, tB, ldb = _stored(B, transB)
+    K, N = (Bs.size(1), Bs.size(0)) if tB else (Bs.size(0), Bs.size(1))
+    ldp = max((K + 7) // 8 * 8, 8)
+    tf32 = m.startswith("tf32")
+    P = torch.zeros((3 if not tf32 else 2, N, ldp),
+                    dtype=torch.float32 if tf32 else torch.int16, device=B.device)
+    h = _stream_handle(stream)
+    if N > 0 and K > 0:
+        if tf32:
+            name = "emu_split_tf32x2_scaled" if m == "tf32x3_oy" else "emu_split_tf32x2"
+            st = getattr(lib(), name)(Bs.data_ptr(), N, K, ldb, int(not tB), P[0].data_ptr(),
+                                      P[1].data_ptr(), ldp, h)
+        else:
+            st = lib().emu_split_bf16x3(Bs.data_ptr(), N, K, ldb, int(not tB), P[0].data_ptr(),
+                                        P[1].data_ptr(), P[2].data_ptr(), ldp, h)
+        _check(st, "emu_split_b")
+    return P[:PIECES[m]]
+
+
+def emu_sgemm_bsplit(A, Bp, C=None, *, transA=False, alpha=1.0, beta=0.0, mode="bf16x9",
+                     stream=None):
+    """C = alpha * op(A) @ op(B) + beta * C with op(B) given by its pieces
+    (``emu_split_b``): a (pieces, N, ldp) CUDA tensor."""
+    import torch
+    As, tA, lda = _stored(A, transA)
+    M, K = (As.size(1), As.size(0)) if tA else (As.size(0), As.size(1))
+    if Bp.dim() != 3 or not Bp.is_contiguous():
+        raise ValueError("Bp must be a contiguous (pieces, N, ldp) tensor")
+    N, ldp = Bp.size(1), Bp.size(2)
+    if ldp < K:
+        raise ValueError("Bp's rows are shorter than K")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if C.dim() != 2 or C.shape != (M, N) or C.dtype != torch.float32 or (C.stride(1) != 1 and N > 1):
+        raise ValueError("C must be an M x N float32 tensor with unit row stride")
+    ldc = C.stride(0) if M > 1 else max(N, 1)
+    st = lib().emu_sgemm_bsplit(int(tA), M, N, K, float(alpha), As.data_ptr(), lda,
+                                Bp.data_ptr(), ldp, float(beta), C.data_ptr(), max(ldc, N, 1),
+                                _mode(mode), _stream_handle(stream))
+    _check(st, "emu_sgemm_bsplit")
     return C
 
 

@@ -315,16 +315,23 @@ emu_status_t check_gemm_args(int transA, int transB, int64_t M, int64_t N, int64
 // where they are for any M), then op(A)'s at a 1 KB boundary.  b_ready: B's
 // pieces for this B, mode and K are already there (an earlier row chunk of
 // the same emu_sgemm_host call put them) and are not split again.
+// B's pieces supplied by the caller (emu_sgemm_bsplit): the pieces of
+// op(B)^T as consecutive planes of N rows x ldbp elements.
+struct BPieces {
+    const void* p = nullptr;
+    int64_t ld = 0;
+};
+
 emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
                           float alpha, const float* A, int64_t lda, const float* B, int64_t ldb,
                           float beta, float* C, int64_t ldc, DeviceState* d, cudaStream_t stream,
-                          bool b_ready = false) {
+                          bool b_ready = false, BPieces bext = {}) {
     const int64_t ldp = plane_ld(K);
     const int tf32 = mode_is_tf32(mode);
     const int planes = mode_pieces(mode);
     const int esize = mode_piece_bytes(mode);
     const size_t a_bytes = (size_t)planes * M * ldp * esize;
-    const size_t b_bytes = (size_t)planes * N * ldp * esize;
+    const size_t b_bytes = bext.p ? 0 : (size_t)planes * N * ldp * esize;
     const size_t b_region = (b_bytes + 1023) / 1024 * 1024;
     if (b_ready && d->ws_bytes < b_region + a_bytes) return EMU_ERR_INVALID_VALUE;  // caller's bug
     emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, b_region + a_bytes);
@@ -338,7 +345,7 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
         e = launch_split_pieces(mode, A, M, K, lda, transA, wa, ldp, stream);
     }
     if (e != cudaSuccess) return from_cuda(e);
-    if (!b_ready) {
+    if (!b_ready && !bext.p) {
         // op(B)^T is N x K: B itself when transB == 1, B^T otherwise
         ProfScope ps(0, stream);
         // independent of A's split: may run beside it (programmatic launch)
@@ -352,7 +359,10 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
     CUtensorMap mapA, mapB;
     st = make_plane_map(&mapA, wa, tf32, M, K, ldp, planes, box_cols, 128);
     if (st != EMU_OK) return st;
-    st = make_plane_map(&mapB, wb, tf32, N, K, ldp, planes, box_cols, bn / 2);
+    if (bext.p)
+        st = make_plane_map(&mapB, bext.p, tf32, N, K, bext.ld, planes, box_cols, bn / 2);
+    else
+        st = make_plane_map(&mapB, wb, tf32, N, K, ldp, planes, box_cols, bn / 2);
     if (st != EMU_OK) return st;
 
     TcGemmParams p = {};
@@ -386,14 +396,22 @@ bool fused_ok(int mode, int transA, const float* A, int64_t lda) {
 // (128-wide tiles).
 emu_status_t run_fused_tmem(int transB, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                        int64_t lda, const float* B, int64_t ldb, float beta, float* C,
-                       int64_t ldc, DeviceState* d, cudaStream_t stream, bool b_ready = false) {
-    const int64_t ldp = plane_ld(K);
-    if (b_ready && d->ws_bytes < (size_t)3 * N * ldp * 2) return EMU_ERR_INVALID_VALUE;
-    emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, (size_t)3 * N * ldp * 2);
-    if (st != EMU_OK) return st;
-    uint16_t* pb = static_cast<uint16_t*>(d->ws);
+                       int64_t ldc, DeviceState* d, cudaStream_t stream, bool b_ready = false,
+                       BPieces bext = {}) {
+    int64_t ldp = plane_ld(K);
+    uint16_t* pb = nullptr;
+    emu_status_t st;
+    if (bext.p) {
+        pb = const_cast<uint16_t*>(static_cast<const uint16_t*>(bext.p));
+        ldp = bext.ld;
+    } else {
+        if (b_ready && d->ws_bytes < (size_t)3 * N * ldp * 2) return EMU_ERR_INVALID_VALUE;
+        st = ensure_buffer(&d->ws, &d->ws_bytes, (size_t)3 * N * ldp * 2);
+        if (st != EMU_OK) return st;
+        pb = static_cast<uint16_t*>(d->ws);
+    }
     cudaError_t e = cudaSuccess;
-    if (!b_ready) {
+    if (!b_ready && !bext.p) {
         ProfScope ps(0, stream);
         e = launch_split_bf16x3(B, N, K, ldb, !transB, pb, pb + N * ldp, pb + 2 * N * ldp, ldp,
                                 stream);
@@ -431,14 +449,21 @@ emu_status_t run_fused_tmem(int transB, int64_t M, int64_t N, int64_t K, float a
 emu_status_t run_fused_smem(int transB, int64_t M, int64_t N, int64_t K, float alpha,
                             const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
                             float* C, int64_t ldc, DeviceState* d, cudaStream_t stream,
-                            bool b_ready = false) {
-    const int64_t ldp = plane_ld(K);
-    if (b_ready && d->ws_bytes < (size_t)3 * N * ldp * 2) return EMU_ERR_INVALID_VALUE;
-    emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, (size_t)3 * N * ldp * 2);
-    if (st != EMU_OK) return st;
-    uint16_t* pb = static_cast<uint16_t*>(d->ws);
+                            bool b_ready = false, BPieces bext = {}) {
+    int64_t ldp = plane_ld(K);
+    uint16_t* pb = nullptr;
+    emu_status_t st;
+    if (bext.p) {
+        pb = const_cast<uint16_t*>(static_cast<const uint16_t*>(bext.p));
+        ldp = bext.ld;
+    } else {
+        if (b_ready && d->ws_bytes < (size_t)3 * N * ldp * 2) return EMU_ERR_INVALID_VALUE;
+        st = ensure_buffer(&d->ws, &d->ws_bytes, (size_t)3 * N * ldp * 2);
+        if (st != EMU_OK) return st;
+        pb = static_cast<uint16_t*>(d->ws);
+    }
     cudaError_t e = cudaSuccess;
-    if (!b_ready) {
+    if (!b_ready && !bext.p) {
         ProfScope ps(0, stream);
         e = launch_split_bf16x3(B, N, K, ldb, !transB, pb, pb + N * ldp, pb + 2 * N * ldp, ldp,
                                 stream);
@@ -477,12 +502,14 @@ struct Plan {
 };
 
 Plan plan_call(int transA, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, int mode,
-               const DeviceState* d) {
+               const DeviceState* d, bool keep_mode = false) {
     if (g_strategy < 0) g_strategy = read_strategy_env();
     if (g_path < 0) g_path = read_path_env();
     Plan pl;
-    // PERFORMANT: the plain FP32 kernel where it is predicted faster
-    pl.mode = choose_mode(M, N, K, mode, g_strategy == EMU_STRATEGY_PERFORMANT, d->sms);
+    // PERFORMANT: the plain FP32 kernel where it is predicted faster (not
+    // when B comes already split: the pieces are what the caller gives)
+    pl.mode = keep_mode ? mode
+                        : choose_mode(M, N, K, mode, g_strategy == EMU_STRATEGY_PERFORMANT, d->sms);
     // AUTO, for BF16x9 with M >= 4096 and N <= 256 (the MLIP layers), where
     // splitting A in the GEMM kernel saves more than the split kernel's HBM
     // round trip costs (measured on GB300, graph replays, shared-memory fused
@@ -505,7 +532,7 @@ Plan plan_call(int transA, int64_t M, int64_t N, int64_t K, const float* A, int6
 emu_status_t run_planned(const Plan& pl, int transA, int transB, int64_t M, int64_t N, int64_t K,
                          float alpha, const float* A, int64_t lda, const float* B, int64_t ldb,
                          float beta, float* C, int64_t ldc, DeviceState* d, cudaStream_t stream,
-                         bool b_ready) {
+                         bool b_ready, BPieces bext = {}) {
     if (pl.mode == EMU_MODE_FP32_SIMT) {
         ProfScope ps(3, stream);
         return from_cuda(launch_gemm_simt(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
@@ -513,12 +540,12 @@ emu_status_t run_planned(const Plan& pl, int transA, int transB, int64_t M, int6
     }
     if (pl.fused == 3)
         return run_fused_smem(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream,
-                              b_ready);
+                              b_ready, bext);
     if (pl.fused == 1)
         return run_fused_tmem(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream,
-                              b_ready);
+                              b_ready, bext);
     return run_two_pass(pl.mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d,
-                        stream, b_ready);
+                        stream, b_ready, bext);
 }
 
 emu_status_t sgemm_device(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
@@ -703,6 +730,40 @@ emu_status_t emu_sgemm_host(int transA, int transB, int64_t M, int64_t N, int64_
     e = cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     return from_cuda(e);
+}
+
+emu_status_t emu_sgemm_bsplit(int transA, int64_t M, int64_t N, int64_t K, float alpha,
+                              const float* A, int64_t lda, const void* Bp, int64_t ldbp,
+                              float beta, float* C, int64_t ldc, int mode,
+                              emu_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (transA != 0 && transA != 1) return EMU_ERR_INVALID_VALUE;
+    if (!valid_mode(mode) || mode == EMU_MODE_FP32_SIMT) return EMU_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return EMU_ERR_INVALID_VALUE;
+    if (lda < 1 || lda < (transA ? M : K) || ldc < 1 || ldc < N) return EMU_ERR_INVALID_VALUE;
+    // the pieces are read by TMA: 16-byte aligned base and rows
+    if (ldbp < K || ldbp < 1 || (ldbp % 8) != 0 || ldbp > INT32_MAX) return EMU_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return EMU_OK;
+    if (C == nullptr) return EMU_ERR_INVALID_VALUE;
+    if (K > 0 && (A == nullptr || Bp == nullptr || (reinterpret_cast<uintptr_t>(Bp) & 15) != 0))
+        return EMU_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!workspace_fits(M, N, K)) return EMU_ERR_ALLOC;
+    DeviceState* d = nullptr;
+    emu_status_t st = current_device(&d);
+    if (st != EMU_OK) return st;
+    if (K == 0 || alpha == 0.0f) {
+        ProfScope ps(4, stream);
+        return from_cuda(launch_scale(M, N, beta, C, ldc, stream));
+    }
+    const Plan pl = plan_call(transA, M, N, K, A, lda, mode, d, true);
+    BPieces bext;
+    bext.p = Bp;
+    bext.ld = ldbp;
+    // transB and B are not used: op(B)^T's pieces are given
+    return run_planned(pl, transA, 0, M, N, K, alpha, A, lda, nullptr, 0, beta, C, ldc, d, stream,
+                       false, bext);
 }
 
 emu_status_t emu_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,

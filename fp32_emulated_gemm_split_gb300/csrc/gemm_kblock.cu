@@ -46,7 +46,8 @@
 // Fused A in shared memory (BF16x9, FUSED = 3, BN = 256 or 128): the
 // two-pass layout, but the producer loads only B's pieces; eight split warps
 // read each K block of FP32 A from global memory (prefetched into L2 two
-// blocks ahead, loaded before the stage-free wait), split it and store the
+// blocks ahead, across tile boundaries, and loaded before the stage-free
+// wait), split it and store the
 // three pieces into the stage's A half in the same 128-byte swizzled layout
 // the TMA would have written, fence, meet at a named barrier, and one
 // thread signals the leader CTA, whose MMA waits for both CTAs' halves.
@@ -85,18 +86,26 @@ constexpr int kATile = kHalfRows * kTcBKBytes;       // 16 KB: 128 rows x 128 by
 // split warps store them into tensor memory; 3 (shared-memory fused) split
 // warps store them into the A half of each shared-memory stage, where the
 // two-pass path's TMA would have put them.
-// Accumulator warps: 16 (a column quarter each) on the two-pass and
-// shared-memory paths; 8 (a column half each) on the tensor-memory path,
-// which also runs 16 split warps and must stay within 1024 threads.
+// Warp roles: warp 0 is the TMA producer (and allocates tensor memory),
+// warp 1 the MMA issuer, then come the accumulator warps -- 16 (a column
+// quarter each), or 8 (a column half each) on the tensor-memory path, which
+// also runs 16 split warps and must stay within 1024 threads -- and the split
+// warps: 8 of 16 rows each on the shared-memory path (their loads in flight
+// must cover the latency of reading A: fewer warps starve them).
 template <int FUSED>
-constexpr int acc_warps() { return FUSED == 1 ? 8 : 16; }
+struct Roles {
+    static constexpr int acc = FUSED == 1 ? 8 : 16;
+    static constexpr int split = FUSED == 1 ? 16 : FUSED == 3 ? 8 : 0;
+    static constexpr int producer = 0, mma = 1, acc0 = 2, split0 = 2 + acc;
+    static constexpr int warps = 2 + acc + split;
+};
+template <int FUSED>
+constexpr int acc_warps() { return Roles<FUSED>::acc; }
 constexpr int kSplitWarps = 16;                       // tensor-memory path
-constexpr int kSmemSplitWarps = 8;                    // shared-memory path: 16 rows each
+constexpr int kSmemSplitWarps = 8;                    // shared-memory path
+constexpr int kSmemSplitRows = 128 / kSmemSplitWarps;
 template <int FUSED>
-constexpr int threads_k() {
-    return (2 + acc_warps<FUSED>() + (FUSED == 1 ? kSplitWarps : FUSED == 3 ? kSmemSplitWarps : 0)) *
-           32;
-}
+constexpr int threads_k() { return Roles<FUSED>::warps * 32; }
 constexpr int kSmemMax = 232448;                      // dynamic shared memory per CTA
 constexpr int kA32Box = 128 * 128;                    // FP32 box: 128 rows x 32 floats
 constexpr int kA32Buf = 2 * kA32Box;                  // one 64-wide K block of FP32 A
@@ -260,6 +269,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapC, const TcGemmParams p) {
     using Cfg = KCfg<MODE, BN, FUSED>;
+    using R = Roles<FUSED>;
     constexpr int S = Cfg::stages, P = Cfg::pieces, kAccCols = Cfg::acc_cols;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -293,6 +303,27 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                               num_clusters};
     const int nunits = sched_units(sch, cluster_id);
 
+    if constexpr (Cfg::SMS) {
+        // split warps: start the first two K blocks of their rows of A on
+        // their way to L2 while the prologue runs (a hint; see griddep_wait
+        // below for the reads)
+        if (warp >= R::split0 && warp < R::split0 + R::split && nunits > 0) {
+            const Unit u0 = sched_unit(sch, cluster_id, 0);
+            int tm0, tn0;
+            tile_pos(u0.tile, p.tiles_m, p.tiles_n, tm0, tn0);
+            const int row0 = tm0 * kBM + int(rank) * kHalfRows +
+                             kSmemSplitRows * (warp - R::split0);
+            for (int d = 0; d < 2 && u0.kb0 + d < u0.kb1; ++d) {
+                for (int t = lane; t < 2 * kSmemSplitRows; t += 32) {
+                    const int prow = row0 + (t >> 1);
+                    const int pk = (u0.kb0 + d) * 64 + 32 * (t & 1);
+                    if (prow < p.M && pk < p.K)
+                        asm volatile("prefetch.global.L2 [%0];"
+                                     :: "l"(p.A32 + (int64_t)prow * p.lda + pk));
+                }
+            }
+        }
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < nb_full; ++i) mbar_init(full0 + 8 * i, 1);
         for (int s = 0; s < S; ++s) mbar_init(empty0 + 8 * s, 1);
@@ -316,7 +347,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == R::producer) {
         if (lane == 0) {
             tma_prefetch_desc(&mapA);
             tma_prefetch_desc(&mapB);
@@ -330,203 +361,244 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    if (warp == 0 && lane == 0) {
-        // ---------------------------------------------------- TMA producer
-        griddep_wait();                           // the split ahead has written the pieces
-        const uint32_t full_leader0 = map_to_rank(full0, 0);
-        uint32_t kbg = 0;                         // K blocks staged so far (all units)
-        bool ok = true;
-        for (int i = 0; i < nunits && ok; ++i) {
-            const Unit w = sched_unit(sch, cluster_id, i);
-            int tm, tn;
-            tile_pos(w.tile, p.tiles_m, p.tiles_n, tm, tn);
-            const int arow = tm * kBM + int(rank) * kHalfRows;
-            const int brow = tn * BN + int(rank) * Cfg::b_rows;
-            for (int kb = w.kb0; kb < w.kb1; ++kb, ++kbg) {
-                const uint32_t s = kbg % S, ph = (kbg / S) & 1;
-                if (Cfg::TM) {
-                    const uint32_t f = kbg % kA32Bufs, fph = (kbg / kA32Bufs) & 1;
-                    if (!mbar_wait(afree0 + 8 * f, fph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
+    // A kernel launched behind this one as a programmatic dependent (the next
+    // GEMM of a run of calls on already-split weights) may start now on SMs
+    // this grid leaves free: every one of its reads and writes of global
+    // memory waits for this grid's completion (griddep_wait), and its CTAs
+    // cannot share an SM with this grid's (each takes most of the shared
+    // memory), so the overlap covers only its launch and prologue.
+    griddep_launch_dependents();
+    if (warp == R::producer) {
+        if (lane == 0) {
+            // ---------------------------------------------------- TMA producer
+            griddep_wait();                           // the split ahead has written the pieces
+            const uint32_t full_leader0 = map_to_rank(full0, 0);
+            uint32_t kbg = 0;                         // K blocks staged so far (all units)
+            bool ok = true;
+            for (int i = 0; i < nunits && ok; ++i) {
+                const Unit w = sched_unit(sch, cluster_id, i);
+                int tm, tn;
+                tile_pos(w.tile, p.tiles_m, p.tiles_n, tm, tn);
+                const int arow = tm * kBM + int(rank) * kHalfRows;
+                const int brow = tn * BN + int(rank) * Cfg::b_rows;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++kbg) {
+                    const uint32_t s = kbg % S, ph = (kbg / S) & 1;
+                    if (Cfg::TM) {
+                        const uint32_t f = kbg % kA32Bufs, fph = (kbg / kA32Bufs) & 1;
+                        if (!mbar_wait(afree0 + 8 * f, fph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(afull0 + 8 * f, kA32Buf);
+                        const uint32_t dst = smem_u32(a32 + f * kA32Buf);
+                        // FP32 A map is (K, M, 1): the two 32-wide boxes of this K block
+                        tma_load_3d(dst, &mapA, afull0 + 8 * f, kb * 64, arow, 0);
+                        tma_load_3d(dst + kA32Box, &mapA, afull0 + 8 * f, kb * 64 + 32, arow, 0);
+                    }
+                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(afull0 + 8 * f, kA32Buf);
-                    const uint32_t dst = smem_u32(a32 + f * kA32Buf);
-                    // FP32 A map is (K, M, 1): the two 32-wide boxes of this K block
-                    tma_load_3d(dst, &mapA, afull0 + 8 * f, kb * 64, arow, 0);
-                    tma_load_3d(dst + kA32Box, &mapA, afull0 + 8 * f, kb * 64 + 32, arow, 0);
-                }
-                if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) || *abort_flag) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
-                // largest piece index first: the first band needs it first
-                for (int pc = P - 1; pc >= 0; --pc) {
-                    if (leader) mbar_arrive_expect_tx(full0 + 8 * (s * P + pc), Cfg::piece_tx);
-                    const uint32_t fbl = full_leader0 + 8 * (s * P + pc);
-                    if (!Cfg::TM && !Cfg::SMS)
-                        tma_load_3d_pair(st + pc * kATile, &mapA, fbl, kb * Cfg::elems, arow, pc);
-                    tma_load_3d_pair(st + P * (Cfg::TM ? 0 : kATile) + pc * Cfg::b_tile, &mapB, fbl,
-                                     kb * Cfg::elems, brow, pc);
+                    const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
+                    // largest piece index first: the first band needs it first
+                    for (int pc = P - 1; pc >= 0; --pc) {
+                        if (leader) mbar_arrive_expect_tx(full0 + 8 * (s * P + pc), Cfg::piece_tx);
+                        const uint32_t fbl = full_leader0 + 8 * (s * P + pc);
+                        if (!Cfg::TM && !Cfg::SMS)
+                            tma_load_3d_pair(st + pc * kATile, &mapA, fbl, kb * Cfg::elems, arow, pc);
+                        tma_load_3d_pair(st + P * (Cfg::TM ? 0 : kATile) + pc * Cfg::b_tile, &mapB, fbl,
+                                         kb * Cfg::elems, brow, pc);
+                    }
                 }
             }
+            if (!ok) *abort_flag = 1;
         }
-        if (!ok) *abort_flag = 1;
-    } else if (warp == 1 && lane == 0 && leader) {
-        // ------------------------------------------------------ MMA issuer
-        const uint32_t idesc = make_idesc(Cfg::tf32 ? 2u : 1u, kBM, BN);
-        constexpr int KBP = Cfg::kb_per_partial;
-        uint32_t kbg = 0, part = 0;              // K blocks and TMEM partials so far
-        uint32_t prev_s = 0;                     // band-major: stage of the pair's first block
-        bool ok = true;
-        for (int i = 0; i < nunits && ok; ++i) {
-            const Unit w = sched_unit(sch, cluster_id, i);
-            for (int kb = w.kb0; kb < w.kb1; ++kb, ++kbg) {
-                const uint32_t s = kbg % S, ph = (kbg / S) & 1;
-                const uint32_t buf = part % NB, cph = (part / NB) & 1;
-                const bool fresh = ((kb - w.kb0) % KBP) == 0;   // first block of a partial
-                const bool close = ((kb - w.kb0) % KBP) == KBP - 1 || kb == w.kb1 - 1;
-                if (fresh && !mbar_wait(cempty0 + 8 * buf, cph ^ 1, p.err, kDevErrTimeout)) {
-                    ok = false;
-                    break;
-                }
-                // fused: A's pieces of this block in tensor-memory stage t
-                const uint32_t t = Cfg::TM ? kbg % Cfg::a_tm_ring : 0;
-                const uint32_t tph = Cfg::TM ? (kbg / Cfg::a_tm_ring) & 1 : 0;
-                if (Cfg::TM) {
-                    if (!mbar_wait(aready0 + 8 * t, tph, p.err, kDevErrTimeout)) {
+    } else if (warp == R::mma) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------------ MMA issuer
+            const uint32_t idesc = make_idesc(Cfg::tf32 ? 2u : 1u, kBM, BN);
+            constexpr int KBP = Cfg::kb_per_partial;
+            uint32_t kbg = 0, part = 0;              // K blocks and TMEM partials so far
+            uint32_t prev_s = 0;                     // band-major: stage of the pair's first block
+            bool ok = true;
+            for (int i = 0; i < nunits && ok; ++i) {
+                const Unit w = sched_unit(sch, cluster_id, i);
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++kbg) {
+                    const uint32_t s = kbg % S, ph = (kbg / S) & 1;
+                    const uint32_t buf = part % NB, cph = (part / NB) & 1;
+                    const bool fresh = ((kb - w.kb0) % KBP) == 0;   // first block of a partial
+                    const bool close = ((kb - w.kb0) % KBP) == KBP - 1 || kb == w.kb1 - 1;
+                    if (fresh && !mbar_wait(cempty0 + 8 * buf, cph ^ 1, p.err, kDevErrTimeout)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                }
-                if (Cfg::SMS) {
-                    // both CTAs' split warps have written A's pieces into stage s
-                    if (!mbar_wait(aready0 + 8 * s, ph, p.err, kDevErrTimeout)) {
-                        ok = false;
-                        break;
+                    // fused: A's pieces of this block in tensor-memory stage t
+                    const uint32_t t = Cfg::TM ? kbg % Cfg::a_tm_ring : 0;
+                    const uint32_t tph = Cfg::TM ? (kbg / Cfg::a_tm_ring) & 1 : 0;
+                    if (Cfg::TM) {
+                        if (!mbar_wait(aready0 + 8 * t, tph, p.err, kDevErrTimeout)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
                     }
-                    tc_fence_after();
-                }
-                const uint32_t d = tmem + buf * BN;
-                const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
-                constexpr int a_smem = Cfg::TM ? 0 : kATile;
-                auto A = [&](int i) { return st + i * a_smem; };
-                auto B = [&](int j) { return st + P * a_smem + j * Cfg::b_tile; };
-                const uint32_t a_tm0 = tmem + Cfg::a_tm_base + t * Cfg::a_tm_cols;
-                auto ready = [&](int pc) {
-                    const bool r = mbar_wait(full0 + 8 * (s * P + pc), ph, p.err, kDevErrTimeout) &&
-                                   !*abort_flag;
-                    tc_fence_after();
-                    return r;
-                };
-                if constexpr (Cfg::TM) {
-                    // A pieces from tensor memory, 32 columns apart
-                    auto pr = [&](int i, int j, bool first, bool shift) {
-                        mma_pair_ta(d, a_tm0 + 32 * i, B(j), idesc, first, shift);
+                    if (Cfg::SMS) {
+                        // both CTAs' split warps have written A's pieces into stage s
+                        if (!mbar_wait(aready0 + 8 * s, ph, p.err, kDevErrTimeout)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    const uint32_t d = tmem + buf * BN;
+                    const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
+                    constexpr int a_smem = Cfg::TM ? 0 : kATile;
+                    auto A = [&](int i) { return st + i * a_smem; };
+                    auto B = [&](int j) { return st + P * a_smem + j * Cfg::b_tile; };
+                    const uint32_t a_tm0 = tmem + Cfg::a_tm_base + t * Cfg::a_tm_cols;
+                    auto ready = [&](int pc) {
+                        const bool r = mbar_wait(full0 + 8 * (s * P + pc), ph, p.err, kDevErrTimeout) &&
+                                       !*abort_flag;
+                        tc_fence_after();
+                        return r;
                     };
-                    if (!ready(2)) { ok = false; break; }
-                    pr(2, 2, true, false);                                    // band 4
-                    if (!ready(1)) { ok = false; break; }
-                    pr(1, 2, false, true);                                    // band 3
-                    pr(2, 1, false, false);
-                    if (!ready(0)) { ok = false; break; }
-                    pr(0, 2, false, true);                                    // band 2
-                    pr(1, 1, false, false);
-                    pr(2, 0, false, false);
-                    pr(0, 1, false, true);                                    // band 1
-                    pr(1, 0, false, false);
-                    pr(0, 0, false, true);                                    // band 0
-                } else if constexpr (MODE == kModeBf16x9) {
-                    if (!ready(2)) { ok = false; break; }
-                    mma_pair<0>(d, A(2), B(2), idesc, true, false);           // band 4
-                    if (!ready(1)) { ok = false; break; }
-                    mma_pair<0>(d, A(1), B(2), idesc, false, true);           // band 3
-                    mma_pair<0>(d, A(2), B(1), idesc, false, false);
-                    if (!ready(0)) { ok = false; break; }
-                    mma_pair<0>(d, A(0), B(2), idesc, false, true);           // band 2
-                    mma_pair<0>(d, A(1), B(1), idesc, false, false);
-                    mma_pair<0>(d, A(2), B(0), idesc, false, false);
-                    mma_pair<0>(d, A(0), B(1), idesc, false, true);           // band 1
-                    mma_pair<0>(d, A(1), B(0), idesc, false, false);
-                    mma_pair<0>(d, A(0), B(0), idesc, false, true);           // band 0
-                } else if constexpr (MODE == kModeTf32x3) {
-                    if (!ready(1) || !ready(0)) { ok = false; break; }
-                    mma_pair<1>(d, A(0), B(1), idesc, fresh, false);          // hi*lo
-                    mma_pair<1>(d, A(1), B(0), idesc, false, false);          // lo*hi
-                    mma_pair<1>(d, A(0), B(0), idesc, false, false);          // hi*hi
-                } else if constexpr (Cfg::band_major) {
-                    // BF16x3: band 1 = a0 b1 + a1 b0, band 0 = a0 b0, shift 2^-8.
-                    // Ootomo-Yokota: hi lo' + lo' hi, then hi hi, shift 2^-11.
-                    constexpr int T = Cfg::tf32 ? 1 : 0, SH = Cfg::band_shift;
-                    if (!ready(1) || !ready(0)) { ok = false; break; }
-                    mma_pair<T>(d, A(0), B(1), idesc, fresh, false);          // band 1
-                    mma_pair<T>(d, A(1), B(0), idesc, false, false);
-                    if (!close) {
-                        prev_s = s;                  // band 0 after the next block's band 1
-                        continue;                    // stage held: no empty commit yet
-                    }
-                    if (!fresh) {
-                        // band 0 of the pair's first block (shift), free its stage
-                        const uint32_t pst = smem_u32(smem + prev_s * Cfg::stage_bytes);
-                        mma_pair<T, SH>(d, pst, pst + P * kATile, idesc, false, true);
-                        tc_commit_pair(empty0 + 8 * prev_s);
-                        mma_pair<T>(d, A(0), B(0), idesc, false, false);
+                    if constexpr (Cfg::TM) {
+                        // A pieces from tensor memory, 32 columns apart
+                        auto pr = [&](int i, int j, bool first, bool shift) {
+                            mma_pair_ta(d, a_tm0 + 32 * i, B(j), idesc, first, shift);
+                        };
+                        if (!ready(2)) { ok = false; break; }
+                        pr(2, 2, true, false);                                    // band 4
+                        if (!ready(1)) { ok = false; break; }
+                        pr(1, 2, false, true);                                    // band 3
+                        pr(2, 1, false, false);
+                        if (!ready(0)) { ok = false; break; }
+                        pr(0, 2, false, true);                                    // band 2
+                        pr(1, 1, false, false);
+                        pr(2, 0, false, false);
+                        pr(0, 1, false, true);                                    // band 1
+                        pr(1, 0, false, false);
+                        pr(0, 0, false, true);                                    // band 0
+                    } else if constexpr (MODE == kModeBf16x9) {
+                        if (!ready(2)) { ok = false; break; }
+                        mma_pair<0>(d, A(2), B(2), idesc, true, false);           // band 4
+                        if (!ready(1)) { ok = false; break; }
+                        mma_pair<0>(d, A(1), B(2), idesc, false, true);           // band 3
+                        mma_pair<0>(d, A(2), B(1), idesc, false, false);
+                        if (!ready(0)) { ok = false; break; }
+                        mma_pair<0>(d, A(0), B(2), idesc, false, true);           // band 2
+                        mma_pair<0>(d, A(1), B(1), idesc, false, false);
+                        mma_pair<0>(d, A(2), B(0), idesc, false, false);
+                        mma_pair<0>(d, A(0), B(1), idesc, false, true);           // band 1
+                        mma_pair<0>(d, A(1), B(0), idesc, false, false);
+                        mma_pair<0>(d, A(0), B(0), idesc, false, true);           // band 0
+                    } else if constexpr (MODE == kModeTf32x3) {
+                        if (!ready(1) || !ready(0)) { ok = false; break; }
+                        mma_pair<1>(d, A(0), B(1), idesc, fresh, false);          // hi*lo
+                        mma_pair<1>(d, A(1), B(0), idesc, false, false);          // lo*hi
+                        mma_pair<1>(d, A(0), B(0), idesc, false, false);          // hi*hi
+                    } else if constexpr (Cfg::band_major) {
+                        // BF16x3: band 1 = a0 b1 + a1 b0, band 0 = a0 b0, shift 2^-8.
+                        // Ootomo-Yokota: hi lo' + lo' hi, then hi hi, shift 2^-11.
+                        constexpr int T = Cfg::tf32 ? 1 : 0, SH = Cfg::band_shift;
+                        if (!ready(1) || !ready(0)) { ok = false; break; }
+                        mma_pair<T>(d, A(0), B(1), idesc, fresh, false);          // band 1
+                        mma_pair<T>(d, A(1), B(0), idesc, false, false);
+                        if (!close) {
+                            prev_s = s;                  // band 0 after the next block's band 1
+                            continue;                    // stage held: no empty commit yet
+                        }
+                        if (!fresh) {
+                            // band 0 of the pair's first block (shift), free its stage
+                            const uint32_t pst = smem_u32(smem + prev_s * Cfg::stage_bytes);
+                            mma_pair<T, SH>(d, pst, pst + P * kATile, idesc, false, true);
+                            tc_commit_pair(empty0 + 8 * prev_s);
+                            mma_pair<T>(d, A(0), B(0), idesc, false, false);
+                        } else {
+                            mma_pair<T, SH>(d, A(0), B(0), idesc, false, true);
+                        }
                     } else {
-                        mma_pair<T, SH>(d, A(0), B(0), idesc, false, true);
+                        if (!ready(0)) { ok = false; break; }
+                        mma_pair<1>(d, A(0), B(0), idesc, fresh, false);          // hi*hi
                     }
-                } else {
-                    if (!ready(0)) { ok = false; break; }
-                    mma_pair<1>(d, A(0), B(0), idesc, fresh, false);          // hi*hi
-                }
-                tc_commit_pair(empty0 + 8 * s);
-                if (Cfg::TM) tc_commit_pair(atfree0 + 8 * t);    // tensor-memory A stage free
-                if (close) {
-                    tc_commit_pair(cfull0 + 8 * buf);
-                    ++part;
+                    tc_commit_pair(empty0 + 8 * s);
+                    if (Cfg::TM) tc_commit_pair(atfree0 + 8 * t);    // tensor-memory A stage free
+                    if (close) {
+                        tc_commit_pair(cfull0 + 8 * buf);
+                        ++part;
+                    }
                 }
             }
+            if (!ok) *abort_flag = 1;
         }
-        if (!ok) *abort_flag = 1;
-    } else if (Cfg::SMS && warp >= 2 + Cfg::acc_warps) {
+    } else if (Cfg::SMS && warp >= R::split0 && warp < R::split0 + R::split) {
         // ------------------------------------- split warps (shared memory)
         // For every K block of this cluster's units, in the producer's order:
-        // prefetch this warp's rows of the block two ahead into L2; once the
-        // MMA has consumed the block that last used stage s, read this CTA's
-        // 128 rows x 64 K of FP32 A (warp w: rows 16 w .. +15, four rows per
-        // step, eight lanes per row, 8 floats per lane), split them and store
-        // the three pieces into the stage's A half in the 128-byte swizzled
-        // K-major layout the MMA reads (16-byte chunk j of row r at chunk
-        // j ^ (r % 8): the eight lanes of a row hit eight bank groups; zeros
-        // past M and K); fence for the tensor core, meet the other split
-        // warps, and one thread counts this CTA in on the leader's barrier.
-        const int sw = warp - 2 - Cfg::acc_warps;
+        // prefetch this warp's rows of the block two ahead into L2 (across
+        // tile boundaries); load this block's rows, then, once the MMA has
+        // consumed the block that last used stage s, split this CTA's 128
+        // rows x 64 K of FP32 A (warp w: rows 16 w .. +15, four rows per
+        // step, eight lanes per row, 8 floats per lane) and store the three
+        // pieces into the stage's A half in the 128-byte swizzled K-major
+        // layout the MMA reads (16-byte chunk j of row r at chunk j ^ (r % 8):
+        // the eight lanes of a row hit eight bank groups; zeros past M and
+        // K); fence for the tensor core, meet the other split warps, and one
+        // thread counts this CTA in on the leader's barrier.
+        const int sw = warp - R::split0;
         const int rsub = lane >> 3, chunk = lane & 7, c8 = chunk * 8;
         const uint32_t aready_leader0 = map_to_rank(aready0, 0);
+        constexpr int RW = kSmemSplitRows, IT = RW / 4;   // rows per warp, 4-row steps
+        // L2 prefetch of this warp's rows x 64 K of one block (two 128-byte
+        // lines per row); a hint only, so it may run ahead of the grid
+        // dependency below
+        auto prefetch_block = [&](int arow_, int kb_) {
+#pragma unroll
+            for (int t = lane; t < 2 * RW; t += 32) {
+                const int prow = arow_ + RW * sw + (t >> 1);
+                const int pk = kb_ * 64 + 32 * (t & 1);
+                if (prow < p.M && pk < p.K)
+                    asm volatile("prefetch.global.L2 [%0];"
+                                 :: "l"(p.A32 + (int64_t)prow * p.lda + pk));
+            }
+        };
+        auto unit_arow = [&](const Unit& u) {
+            int tm_, tn_;
+            tile_pos(u.tile, p.tiles_m, p.tiles_n, tm_, tn_);
+            return tm_ * kBM + int(rank) * kHalfRows;
+        };
+        constexpr int kAhead = 2;                 // blocks prefetched ahead
+        Unit wnext = {};
+        int arow_next = 0;
+        if (nunits > 0) {                         // (its first blocks: prefetched at entry)
+            wnext = sched_unit(sch, cluster_id, 0);
+            arow_next = unit_arow(wnext);
+        }
+        // A may be the output of the kernel ahead in the stream (a
+        // programmatic dependent launch starts before it ends)
+        griddep_wait();
         uint32_t g = 0;
         bool ok = true;
         for (int i = 0; i < nunits && ok; ++i) {
-            const Unit w = sched_unit(sch, cluster_id, i);
-            int tm, tn;
-            tile_pos(w.tile, p.tiles_m, p.tiles_n, tm, tn);
-            const int arow = tm * kBM + int(rank) * kHalfRows;
+            const Unit w = wnext;
+            const int arow = arow_next;
+            if (i + 1 < nunits) {
+                wnext = sched_unit(sch, cluster_id, i + 1);
+                arow_next = unit_arow(wnext);
+            }
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
                 const uint32_t s = g % S, ph = (g / S) & 1;
-                if (kb + 2 < w.kb1) {
-                    const int prow = arow + 16 * sw + (lane & 15);
-                    const int pk = (kb + 2) * 64 + 32 * (lane >> 4);
-                    if (prow < p.M && pk < p.K)
-                        asm volatile("prefetch.global.L2 [%0];"
-                                     :: "l"(p.A32 + (int64_t)prow * p.lda + pk));
-                }
+                // the block kAhead ahead in this cluster's sequence, which
+                // may lie in the next unit (the next tile's rows)
+                if (kb + kAhead < w.kb1)
+                    prefetch_block(arow, kb + kAhead);
+                else if (i + 1 < nunits && wnext.kb0 + (kb + kAhead - w.kb1) < wnext.kb1)
+                    prefetch_block(arow_next, wnext.kb0 + (kb + kAhead - w.kb1));
                 // this block's FP32 rows first: their latency overlaps the wait
                 const int k = kb * 64 + c8;
-                float4 x[4][2];
+                float4 x[IT][2];
 #pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int row = arow + 16 * sw + 4 * it + rsub;
+                for (int it = 0; it < IT; ++it) {
+                    const int row = arow + RW * sw + 4 * it + rsub;
                     x[it][0] = x[it][1] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (row < p.M && k < p.K) {
                         const float* src = p.A32 + (int64_t)row * p.lda + k;
@@ -541,18 +613,18 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                         }
                     }
                 }
-                bool good = mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) &&
-                            !*abort_flag;
+                const bool good = mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, kDevErrTimeout) &&
+                                  !*abort_flag;
                 if (good) {
                     const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
 #pragma unroll
-                    for (int it = 0; it < 4; ++it) {
+                    for (int it = 0; it < IT; ++it) {
                         uint4 q0, q1, q2;
                         split_bf16x3_pair(x[it][0].x, x[it][0].y, q0.x, q1.x, q2.x);
                         split_bf16x3_pair(x[it][0].z, x[it][0].w, q0.y, q1.y, q2.y);
                         split_bf16x3_pair(x[it][1].x, x[it][1].y, q0.z, q1.z, q2.z);
                         split_bf16x3_pair(x[it][1].z, x[it][1].w, q0.w, q1.w, q2.w);
-                        const int r = 16 * sw + 4 * it + rsub;
+                        const int r = RW * sw + 4 * it + rsub;
                         const uint32_t off = r * 128 + ((chunk ^ (r & 7)) << 4);
                         st_shared_v4(st + off, q0);
                         st_shared_v4(st + kATile + off, q1);
@@ -568,12 +640,12 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             }
         }
         if (!ok) *abort_flag = 1;
-    } else if (Cfg::TM && warp >= 2 + Cfg::acc_warps) {
+    } else if (Cfg::TM && warp >= R::split0 && warp < R::split0 + R::split) {
         // ------------------------------------------------------ split warps
         // Split every K block of this cluster's tiles, as soon as its FP32
         // block has landed and its tensor-memory A stage is free, ahead of
         // the tensor core.
-        const int w = warp - 2 - Cfg::acc_warps;
+        const int w = warp - R::split0;
         const int kpart = w >> 2;                      // 16-element part of the 64
         const int r = 32 * (warp & 3) + lane;          // row: this warp's TMEM lanes
         const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
@@ -608,10 +680,10 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 mbar_arrive_remote(aready_leader0 + 8 * t);
             }
         }
-    } else if (warp >= 2) {
+    } else if (warp >= R::acc0 && warp < R::acc0 + R::acc) {
         // ------------------------------------------------ accumulator warps
         const int q = warp & 3;                        // TMEM lane quadrant
-        const int h = (warp - 2) >> 2;                 // column group of the tile
+        const int h = (warp - R::acc0) >> 2;           // column group of the tile
         const uint32_t cempty_leader0 = map_to_rank(cempty0, 0);
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
@@ -648,13 +720,26 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 }
                 tc_fence_after();
                 const uint32_t col0 = tmem + buf * BN + h * kAccCols + lane_off;
+                if constexpr (FUSED == 0) {
+                    // 16 columns per load and wait (the fused kernels, at 72
+                    // registers a thread, load 8)
 #pragma unroll
-                for (int g = 0; g < kAccCols / 8; ++g) {
-                    uint32_t r[8];
-                    tmem_ld_32x32b_x8(col0 + 8 * g, r);
-                    tmem_ld_wait();
+                    for (int g = 0; g < kAccCols / 16; ++g) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(col0 + 16 * g, r);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[8 * g + j] += __uint_as_float(r[j]);
+                        for (int j = 0; j < 16; ++j) acc[16 * g + j] += __uint_as_float(r[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < kAccCols / 8; ++g) {
+                        uint32_t r[8];
+                        tmem_ld_32x32b_x8(col0 + 8 * g, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[8 * g + j] += __uint_as_float(r[j]);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -665,7 +750,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             // warp); this thread's sums as 16-byte groups, lane-contiguous per
             // group, so that a warp writes and reads 512 contiguous bytes at a
             // time
-            const int aw = warp - 2;
+            const int aw = warp - R::acc0;
             auto slot = [&](int c) { return (c * 2 + int(rank)) * Cfg::acc_warps + aw; };
             if (w.publish >= 0) {
                 // a later part of a split tile: leave the sums for the owner
@@ -729,39 +814,69 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 // matrix edge.  With beta != 0 each lane first reads its own
                 // row's 16 values of C (16-byte loads where they fit).
                 constexpr int CB = Cfg::c_bufs;
-                const uint32_t cst0 = smem_u32(cstage + (warp - 2) * 2048 * CB);
-                if (row0 < p.M) {
+                const uint32_t cst0 = smem_u32(cstage + (warp - R::acc0) * 2048 * CB);
+                // The cluster's last unit: all its MMAs have completed (this
+                // warp has drained the last partial), so no stage is read or
+                // written any more and each warp stages all its chunks in
+                // stage memory at once -- no wait for a buffer to be read out.
+                constexpr int kChunks = kAccCols / 16;
+                static_assert(Cfg::acc_warps * kChunks * 2048 <= S * Cfg::stage_bytes,
+                              "stage memory holds the last unit's C");
+                const bool last = i == nunits - 1;
+                const uint32_t lst0 = smem_u32(smem) + (warp - R::acc0) * kChunks * 2048;
+                // alpha * acc (+ beta * C) of 16 columns into a 2 KB staging
+                // buffer: lane = row, 64-byte swizzle
+                auto stage_chunk = [&](int ch, uint32_t cst) {
 #pragma unroll
-                    for (int ch = 0; ch < kAccCols / 16; ++ch) {
+                    for (int c = 0; c < 4; ++c) {
+                        const int j = 16 * ch + 4 * c;
+                        float4 v = make_float4(p.alpha * acc[j], p.alpha * acc[j + 1],
+                                               p.alpha * acc[j + 2], p.alpha * acc[j + 3]);
+                        const int gc = col_base + j;
+                        if (p.beta != 0.0f && row < p.M && gc < p.N) {
+                            const float* src = p.C + (int64_t)row * p.ldc + gc;
+                            if (gc + 3 < p.N) {
+                                const float4 o = *reinterpret_cast<const float4*>(src);
+                                v.x = fmaf(p.beta, o.x, v.x);
+                                v.y = fmaf(p.beta, o.y, v.y);
+                                v.z = fmaf(p.beta, o.z, v.z);
+                                v.w = fmaf(p.beta, o.w, v.w);
+                            } else {
+                                v.x = fmaf(p.beta, src[0], v.x);
+                                if (gc + 1 < p.N) v.y = fmaf(p.beta, src[1], v.y);
+                                if (gc + 2 < p.N) v.z = fmaf(p.beta, src[2], v.z);
+                            }
+                        }
+                        const uint32_t a = cst + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4);
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                                     :: "r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                                     : "memory");
+                    }
+                };
+                if (row0 < p.M && last) {
+                    // every chunk staged, one proxy fence, then all the stores
+                    int nch = 0;
+#pragma unroll
+                    for (int ch = 0; ch < kChunks; ++ch) {
+                        if (col_base + 16 * ch >= p.N) break;          // warp-uniform
+                        stage_chunk(ch, lst0 + ch * 2048);
+                        ++nch;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        for (int ch = 0; ch < nch; ++ch)
+                            tma_store_2d(&mapC, col_base + 16 * ch, row0, lst0 + ch * 2048);
+                        bulk_commit();
+                    }
+                } else if (row0 < p.M) {
+#pragma unroll
+                    for (int ch = 0; ch < kChunks; ++ch) {
                         if (col_base + 16 * ch >= p.N) break;          // warp-uniform
                         const uint32_t cst = cst0 + (ch % CB) * 2048;
                         if (lane == 0) bulk_wait_read_n<CB - 1>();      // this buffer free again
                         __syncwarp();
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const int j = 16 * ch + 4 * c;
-                            float4 v = make_float4(p.alpha * acc[j], p.alpha * acc[j + 1],
-                                                   p.alpha * acc[j + 2], p.alpha * acc[j + 3]);
-                            const int gc = col_base + j;
-                            if (p.beta != 0.0f && row < p.M && gc < p.N) {
-                                const float* src = p.C + (int64_t)row * p.ldc + gc;
-                                if (gc + 3 < p.N) {
-                                    const float4 o = *reinterpret_cast<const float4*>(src);
-                                    v.x = fmaf(p.beta, o.x, v.x);
-                                    v.y = fmaf(p.beta, o.y, v.y);
-                                    v.z = fmaf(p.beta, o.z, v.z);
-                                    v.w = fmaf(p.beta, o.w, v.w);
-                                } else {
-                                    v.x = fmaf(p.beta, src[0], v.x);
-                                    if (gc + 1 < p.N) v.y = fmaf(p.beta, src[1], v.y);
-                                    if (gc + 2 < p.N) v.z = fmaf(p.beta, src[2], v.z);
-                                }
-                            }
-                            const uint32_t a = cst + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4);
-                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
-                                         :: "r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-                                         : "memory");
-                        }
+                        stage_chunk(ch, cst);
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
@@ -809,7 +924,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     __syncwarp();
     tc_fence_before();
     cluster_sync();
-    if (warp == 0) {
+    if (warp == R::producer) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
                      :: "r"(tmem), "r"(Cfg::tmem_cols) : "memory");

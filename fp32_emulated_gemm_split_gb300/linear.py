@@ -9,23 +9,62 @@ emulated FP32 GEMM; because the model's forces are derivatives of its energy,
 the gradient with respect to the layer input goes through the same GEMM.
 This module does that for both emulations:
 
-  forward          y  = x W^T + b      emu_sgemm(x, W, transB=1)
-  input gradient   dx = dy W           emu_sgemm(dy, W)
+  forward          y  = x W^T + b      emu_sgemm_bsplit(x, pieces of W)
+  input gradient   dx = dy W           emu_sgemm_bsplit(dy, pieces of W^T)
   weight gradient  dW = dy^T x         emu_sgemm(dy, x, transA=1)
   bias gradient    db = sum of dy over the leading dimensions
 
 Inputs of any leading shape (..., in_features) are flattened to 2-D.
+
+The weight is the same for every batch until an optimiser changes it, so
+the layer splits it once per version of the weight (two piece sets: W for
+the forward product, W^T for the input gradient) and the forward and
+input-gradient products run emu_sgemm_bsplit on those pieces: no split of
+the weight per call, and in BF16x9 with 4096 rows or more and at most 256
+output columns a single kernel launch per product.  The pieces are dropped
+and made again whenever the weight's storage or version changes (an
+in-place update bumps the version).
 """
 from __future__ import annotations
 
 import torch
 
-from . import emu_sgemm
+from . import emu_sgemm, emu_sgemm_bsplit, emu_split_b
+
+
+class _WeightPieces:
+    """The split pieces of one weight, for the forward product (op(B) = W^T)
+    and the input gradient (op(B) = W), made on first use and remade when
+    the weight changes."""
+
+    def __init__(self):
+        self._cache = {}
+
+    def get(self, weight, transB, mode):
+        key = (bool(transB), mode)
+        stamp = (weight.data_ptr(), weight._version, tuple(weight.shape), weight.device)
+        hit = self._cache.get(key)
+        if hit is None or hit[0] != stamp:
+            hit = (stamp, emu_split_b(weight.detach(), transB=transB, mode=mode))
+            self._cache[key] = hit
+        return hit[1]
+
+    def clear(self):
+        self._cache.clear()
+
+
+def _product(a, weight, out, transB, beta, mode, pieces):
+    """out = a op(W) + beta out, with W's pieces from the cache when the mode
+    runs on the tensor cores."""
+    if pieces is not None and mode != "fp32_simt":
+        emu_sgemm_bsplit(a, pieces.get(weight, transB, mode), out, beta=beta, mode=mode)
+    else:
+        emu_sgemm(a, weight, out, transB=transB, beta=beta, mode=mode)
 
 
 class _EmuLinearFn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, x, weight, bias, mode):
+    def forward(ctx, x, weight, bias, mode, pieces):
         lead = x.shape[:-1]
         x2 = x.reshape(-1, x.shape[-1])
         if x2.stride(-1) != 1:
@@ -34,11 +73,12 @@ class _EmuLinearFn(torch.autograd.Function):
         if x2.shape[0] > 0:
             if bias is not None:
                 out.copy_(bias.expand_as(out))
-                emu_sgemm(x2, weight, out, transB=True, beta=1.0, mode=mode)
+                _product(x2, weight, out, True, 1.0, mode, pieces)
             else:
-                emu_sgemm(x2, weight, out, transB=True, mode=mode)
+                _product(x2, weight, out, True, 0.0, mode, pieces)
         ctx.save_for_backward(x2, weight)
         ctx.mode = mode
+        ctx.pieces = pieces
         ctx.has_bias = bias is not None
         ctx.lead = lead
         return out.reshape(*lead, weight.shape[0])
@@ -53,7 +93,7 @@ class _EmuLinearFn(torch.autograd.Function):
         if ctx.needs_input_grad[0]:
             gx = torch.empty_like(x2)
             if g2.shape[0] > 0:
-                emu_sgemm(g2, weight, gx, mode=ctx.mode)
+                _product(g2, weight, gx, False, 0.0, ctx.mode, ctx.pieces)
             else:
                 gx.zero_()
             gx = gx.reshape(*ctx.lead, weight.shape[1])
@@ -65,7 +105,7 @@ class _EmuLinearFn(torch.autograd.Function):
                 gw.zero_()
         if ctx.has_bias and ctx.needs_input_grad[2]:
             gb = g2.sum(dim=0)
-        return gx, gw, gb, None
+        return gx, gw, gb, None, None
 
 
 class EmuLinear(torch.nn.Module):
@@ -84,6 +124,7 @@ class EmuLinear(torch.nn.Module):
         self.in_features = in_features
         self.out_features = out_features
         self.mode = mode
+        self._pieces = _WeightPieces()
 
     @classmethod
     def from_linear(cls, layer: torch.nn.Linear, mode="bf16x9") -> "EmuLinear":
@@ -94,12 +135,13 @@ class EmuLinear(torch.nn.Module):
         m.in_features = layer.in_features
         m.out_features = layer.out_features
         m.mode = mode
+        m._pieces = _WeightPieces()
         return m
 
     def forward(self, x):
         if x.dtype != torch.float32:
             raise TypeError("EmuLinear computes FP32 in and out")
-        return _EmuLinearFn.apply(x, self.weight, self.bias, self.mode)
+        return _EmuLinearFn.apply(x, self.weight, self.bias, self.mode, self._pieces)
 
     def extra_repr(self):
         return (f"in_features={self.in_features}, out_features={self.out_features}, "

@@ -181,6 +181,43 @@ emu_status_t emu_sgemm_host(int transA, int transB, int64_t M, int64_t N, int64_
                             int mode, emu_stream_t stream);
 
 /*
+ * emu_sgemm_bsplit -- emu_sgemm with op(B) given already split.
+ *
+ * For a B that stays the same over many calls -- the weight of a linear
+ * layer, applied to batch after batch of activations, as in the MLIP layers
+ * the blog post measures (Figure 3) -- split it once and pass its pieces:
+ * a call then runs no split of B, and in BF16X9 with A stored K-major
+ * (transA == 0, lda % 4 == 0, A 16-byte aligned) and N <= 256, M >= 4096
+ * it is a single kernel launch that splits A on chip (the FUSED or
+ * FUSED_TMEM path of emu_set_path; EMU_PATH_TWOPASS splits A into the
+ * workspace first).  Consecutive calls on one stream overlap each kernel's
+ * launch and prologue with the end of the one before it (programmatic
+ * dependent launch).
+ *
+ *  Bp, ldbp   the pieces of op(B)^T (N x K, K-major) as the mode's
+ *             consecutive planes of N rows x ldbp elements, plane i at
+ *             element offset i * N * ldbp:
+ *               BF16X9  3 planes of BF16 bits (uint16), as emu_split_bf16x3
+ *                       writes them for op(B)^T (trans = !transB);
+ *               BF16X3  the first 2 of those planes;
+ *               TF32X3  2 FP32 planes (HI, LO) of emu_split_tf32x2;
+ *               TF32X3_OY  HI and LO of emu_split_tf32x2_scaled;
+ *               TF32    1 plane, HI.
+ *             Device memory owned by the caller, 16-byte aligned; ldbp >= K
+ *             and a multiple of 8; columns K..ldbp-1 are not read.  The
+ *             pieces must not change while a call that reads them runs.
+ *  mode       any emu_mode_t but EMU_MODE_FP32_SIMT; the strategy
+ *             (emu_set_strategy) does not apply: the call runs `mode`.
+ * The other arguments, the layout of A and C, the results and the error
+ * codes are emu_sgemm's (with B given by its pieces, the result is the one
+ * emu_sgemm computes for that B).  Uses the library's workspace for A's
+ * pieces only where A is split into it.
+ */
+emu_status_t emu_sgemm_bsplit(int transA, int64_t M, int64_t N, int64_t K, float alpha,
+                              const float* A, int64_t lda, const void* Bp, int64_t ldbp,
+                              float beta, float* C, int64_t ldc, int mode, emu_stream_t stream);
+
+/*
  * emu_split_bf16x3 -- the split/pack step of BF16X9 on its own.
  *
  * Writes the three BF16 pieces (raw bit patterns) of op(X), rows x cols:

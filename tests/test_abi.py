@@ -129,3 +129,25 @@ def test_c_client_runs(emu, tmp_path):
     out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0, out.stdout + out.stderr
     assert out.stdout.startswith("ok ")
+
+
+def _bsplit(L, transA=0, M=4, N=4, K=4, lda=4, ldbp=8, ldc=4, mode=0, A=1, Bp=16, C=1):
+    return L.emu_sgemm_bsplit(transA, M, N, K, 1.0, A, lda, Bp, ldbp, 0.0, C, ldc, mode, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(M=-1), dict(K=-1), dict(transA=2), dict(mode=2), dict(mode=6), dict(lda=3),
+    dict(ldbp=3), dict(ldbp=12), dict(ldc=3), dict(Bp=None), dict(Bp=8), dict(A=None),
+    dict(C=None), dict(N=1 << 31),
+])
+def test_bsplit_bad_arguments_are_rejected_on_the_host(emu, kw):
+    """emu_sgemm_bsplit: FP32_SIMT has no pieces, the pieces' rows must be a
+    multiple of 8 elements and their base 16-byte aligned (TMA), ldbp >= K;
+    nothing is launched or dereferenced."""
+    assert _bsplit(emu.lib(), **kw) == -1
+
+
+def test_bsplit_empty_problem_is_a_noop(emu):
+    L = emu.lib()
+    assert L.emu_sgemm_bsplit(0, 0, 5, 3, 1.0, None, 3, None, 8, 0.0, None, 5, 0, None) == 0
+    assert L.emu_sgemm_bsplit(0, 5, 0, 3, 1.0, None, 3, None, 8, 0.0, None, 1, 0, None) == 0

@@ -92,3 +92,39 @@ def test_swapped_energy_model_energy_and_forces(emu):
     assert err(f_emu) <= 2e-6
     # the emulated forces are not worse than FP32's by more than rounding noise
     assert err(f_emu) <= 2 * err(f_32) + 1e-7
+
+
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_weight_pieces_follow_the_weight(emu, mode):
+    """The layer keeps its weight's split pieces between calls and remakes
+    them after an in-place update (an optimiser step) or a new weight: the
+    output always matches the current weight, bit for bit the same as
+    emu_sgemm on it, and the forward product runs no split kernel once the
+    pieces exist."""
+    import torch
+    from fp32_emulated_gemm_split_gb300.linear import EmuLinear
+    torch.manual_seed(3)
+    lin = EmuLinear(256, 256, bias=False, device="cuda", mode=mode)
+    x = torch.randn(12288, 256, device="cuda")
+
+    def direct():
+        return emu.emu_sgemm(x, lin.weight.detach(), transB=True, mode=mode)
+
+    with torch.no_grad():
+        y0 = lin(x)
+        assert torch.equal(y0, direct())
+        emu.emu_profile_enable(True)
+        y1 = lin(x)                                  # pieces reused
+        torch.cuda.synchronize()
+        n_split = emu.emu_profile_read("split")[0]
+        emu.emu_profile_enable(False)
+        assert torch.equal(y1, y0)
+        if mode == "bf16x9":
+            assert n_split == 0                      # one fused launch, A split on chip
+        lin.weight.mul_(0.5)                         # in place: the version changes
+        y2 = lin(x)
+        assert torch.equal(y2, direct())
+        assert not torch.equal(y2, y0)
+        lin.weight = torch.nn.Parameter(torch.randn(256, 256, device="cuda"))
+        y3 = lin(x)
+        assert torch.equal(y3, direct())
