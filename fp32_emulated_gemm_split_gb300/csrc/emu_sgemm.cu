@@ -386,8 +386,8 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
 // Whether op(A) can be read directly by the fused kernel: K-major rows that
 // start on 16-byte boundaries (a TMA requirement).
 bool fused_ok(int mode, int transA, const float* A, int64_t lda) {
-    return mode == EMU_MODE_BF16X9 && transA == 0 && (lda % 4) == 0 &&
-           (reinterpret_cast<uintptr_t>(A) & 15) == 0;
+    return (mode == EMU_MODE_BF16X9 || mode == EMU_MODE_TF32X3) && transA == 0 &&
+           (lda % 4) == 0 && (reinterpret_cast<uintptr_t>(A) & 15) == 0;
 }
 
 // Tensor-memory fused path: B's three pieces go to the workspace (one split
@@ -446,49 +446,54 @@ emu_status_t run_fused_tmem(int transB, int64_t M, int64_t N, int64_t K, float a
 // pieces straight into the A half of each shared-memory stage, where the
 // two-pass path's TMA would have put them: 256-wide tiles, A read from HBM
 // once as FP32, its pieces never written out.
-emu_status_t run_fused_smem(int transB, int64_t M, int64_t N, int64_t K, float alpha,
+emu_status_t run_fused_smem(int mode, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                             const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
                             float* C, int64_t ldc, DeviceState* d, cudaStream_t stream,
                             bool b_ready = false, BPieces bext = {}) {
+    // BF16x9: three BF16 pieces per K block of 64; TF32x3: hi and lo (FP32
+    // containers) per K block of 32
+    const bool tf32 = mode == kModeTf32x3;
+    const int pieces = mode_pieces(mode), es = mode_piece_bytes(mode);
+    const int box_k = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
     int64_t ldp = plane_ld(K);
-    uint16_t* pb = nullptr;
+    uint8_t* pb = nullptr;
     emu_status_t st;
     if (bext.p) {
-        pb = const_cast<uint16_t*>(static_cast<const uint16_t*>(bext.p));
+        pb = const_cast<uint8_t*>(static_cast<const uint8_t*>(bext.p));
         ldp = bext.ld;
     } else {
-        if (b_ready && d->ws_bytes < (size_t)3 * N * ldp * 2) return EMU_ERR_INVALID_VALUE;
-        st = ensure_buffer(&d->ws, &d->ws_bytes, (size_t)3 * N * ldp * 2);
+        const size_t need = (size_t)pieces * N * ldp * es;
+        if (b_ready && d->ws_bytes < need) return EMU_ERR_INVALID_VALUE;
+        st = ensure_buffer(&d->ws, &d->ws_bytes, need);
         if (st != EMU_OK) return st;
-        pb = static_cast<uint16_t*>(d->ws);
+        pb = static_cast<uint8_t*>(d->ws);
     }
     cudaError_t e = cudaSuccess;
     if (!b_ready && !bext.p) {
         ProfScope ps(0, stream);
-        e = launch_split_bf16x3(B, N, K, ldb, !transB, pb, pb + N * ldp, pb + 2 * N * ldp, ldp,
-                                stream);
+        e = launch_split_pieces(mode, B, N, K, ldb, !transB, pb, ldp, stream);
     }
     if (e != cudaSuccess) return from_cuda(e);
     const int bn = kblock_bn(N);
     CUtensorMap mapB;
-    st = make_plane_map(&mapB, pb, false, N, K, ldp, 3, 64, bn / 2);
+    st = make_plane_map(&mapB, pb, tf32, N, K, ldp, pieces, box_k, bn / 2);
     if (st != EMU_OK) return st;
     const CUtensorMap mapA = mapB;           // not read: the split warps fill A's stages
     TcGemmParams p = {};
     p.err = d->err;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
-    p.num_kb = (int)((K + 63) / 64);
+    p.num_kb = (int)((K + box_k - 1) / box_k);
     p.tiles_m = (int)((M + 255) / 256);
     p.tiles_n = (int)((N + bn - 1) / bn);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
     p.A32 = A; p.lda = lda;
     CUtensorMap mapC = mapB;
     p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
-    st = plan_tail(p, kModeBf16x9, 256, bn, 3, d);
+    st = plan_tail(p, mode, 256, bn, 3, d);
     if (st != EMU_OK) return st;
     {
         ProfScope ps(2, stream);
-        e = launch_gemm_kblock(0, bn, 3, mapA, mapB, mapC, p, d->sms, stream, true);
+        e = launch_gemm_kblock(mode, bn, 3, mapA, mapB, mapC, p, d->sms, stream, true);
     }
     return from_cuda(e);
 }
@@ -522,10 +527,19 @@ Plan plan_call(int transA, int64_t M, int64_t N, int64_t K, const float* A, int6
     // pieces are then reused by four column tiles).
     const bool small_n = g_path == EMU_PATH_AUTO && N <= 256 && M >= 4096;
     const bool on_chip = pl.mode != EMU_MODE_FP32_SIMT && fused_ok(pl.mode, transA, A, lda);
+    // the tensor-memory kernel splits BF16x9 pieces only; TF32x3 has the
+    // shared-memory one, which AUTO does not take: measured on GB300 against
+    // two-pass (20 calls back to back) it is no faster on the MLIP layers
+    // (1.1M x 256 x 256 1212 / 1216 us, 1.1M x 256 x 1024 4477 / 4385 us,
+    // 12288 x 256 x 256 33.9 / 25.8 us): a TF32 K block is a third of a BF16x9
+    // one's MMA time, so the per-tile epilogue and hand-offs dominate either way
+    const bool tm = pl.mode == EMU_MODE_BF16X9;
     pl.fused = !on_chip ? 0
-             : g_path == EMU_PATH_FUSED_TMEM ? 1
+             : g_path == EMU_PATH_FUSED_TMEM ? (tm ? 1 : 0)
              : g_path == EMU_PATH_FUSED ? 3
-             : small_n ? (N > 128 ? 3 : 1) : 0;
+             : !small_n ? 0
+             : pl.mode == EMU_MODE_TF32X3 ? 0
+             : (N > 128 ? 3 : 1);
     return pl;
 }
 
@@ -539,8 +553,8 @@ emu_status_t run_planned(const Plan& pl, int transA, int transB, int64_t M, int6
                                           ldc, stream));
     }
     if (pl.fused == 3)
-        return run_fused_smem(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream,
-                              b_ready, bext);
+        return run_fused_smem(pl.mode, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d,
+                              stream, b_ready, bext);
     if (pl.fused == 1)
         return run_fused_tmem(transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, d, stream,
                               b_ready, bext);
@@ -639,8 +653,7 @@ emu_status_t host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_
     if (pl.mode != EMU_MODE_FP32_SIMT) {
         const int64_t ldp = plane_ld(K);
         const size_t pb = (size_t)mode_pieces(pl.mode) * mode_piece_bytes(pl.mode) * ldp;
-        const size_t need = pl.fused ? (size_t)3 * N * ldp * 2
-                                     : (pb * N + 1023) / 1024 * 1024 + pb * mc;
+        const size_t need = pl.fused ? pb * N : (pb * N + 1023) / 1024 * 1024 + pb * mc;
         emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, need);
         if (st != EMU_OK) return st;
     }

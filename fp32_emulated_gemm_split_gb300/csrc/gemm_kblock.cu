@@ -160,7 +160,12 @@ struct KCfg {
     // bytes a piece barrier waits for (both CTAs)
     static constexpr uint32_t piece_tx = TM || SMS ? 2 * b_tile : 2 * (kATile + b_tile);
     static_assert(stages >= 2, "shared memory too small for two stages");
-    static_assert(!(FUSED && MODE != kModeBf16x9), "the fused path splits BF16x9 pieces only");
+    static_assert(!(FUSED == 1 && MODE != kModeBf16x9) &&
+                      !(FUSED == 3 && MODE != kModeBf16x9 && MODE != kModeTf32x3),
+                  "the fused paths split BF16x9 pieces (and, in shared memory, TF32x3 ones)");
+    // 128-byte lines in one row of one K block of FP32 A (64 BF16-mode
+    // elements: 2; 32 TF32-mode elements: 1)
+    static constexpr int a32_lines = elems * 4 / 128;
 };
 
 __device__ __forceinline__ void st_release_gpu(unsigned* a, unsigned v) {
@@ -313,10 +318,11 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
             tile_pos(u0.tile, p.tiles_m, p.tiles_n, tm0, tn0);
             const int row0 = tm0 * kBM + int(rank) * kHalfRows +
                              kSmemSplitRows * (warp - R::split0);
+            constexpr int L = Cfg::a32_lines;
             for (int d = 0; d < 2 && u0.kb0 + d < u0.kb1; ++d) {
-                for (int t = lane; t < 2 * kSmemSplitRows; t += 32) {
-                    const int prow = row0 + (t >> 1);
-                    const int pk = (u0.kb0 + d) * 64 + 32 * (t & 1);
+                for (int t = lane; t < L * kSmemSplitRows; t += 32) {
+                    const int prow = row0 + t / L;
+                    const int pk = (u0.kb0 + d) * Cfg::elems + 32 * (t % L);
                     if (prow < p.M && pk < p.K)
                         asm volatile("prefetch.global.L2 [%0];"
                                      :: "l"(p.A32 + (int64_t)prow * p.lda + pk));
@@ -537,25 +543,29 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
         // prefetch this warp's rows of the block two ahead into L2 (across
         // tile boundaries); load this block's rows, then, once the MMA has
         // consumed the block that last used stage s, split this CTA's 128
-        // rows x 64 K of FP32 A (warp w: rows 16 w .. +15, four rows per
-        // step, eight lanes per row, 8 floats per lane) and store the three
-        // pieces into the stage's A half in the 128-byte swizzled K-major
-        // layout the MMA reads (16-byte chunk j of row r at chunk j ^ (r % 8):
-        // the eight lanes of a row hit eight bank groups; zeros past M and
-        // K); fence for the tensor core, meet the other split warps, and one
-        // thread counts this CTA in on the leader's barrier.
+        // rows of FP32 A (warp w: rows 16 w .. +15, four rows per step, eight
+        // lanes per row, each lane one 16-byte chunk of the 128-byte rows of
+        // the pieces: 8 elements for BF16x9, whose K block is 64 wide, 4 for
+        // TF32x3, whose block is 32 wide) and store the pieces into the
+        // stage's A half in the 128-byte swizzled K-major layout the MMA
+        // reads (chunk j of row r at chunk j ^ (r % 8): the eight lanes of a
+        // row hit eight bank groups; zeros past M and K); fence for the
+        // tensor core, meet the other split warps, and one thread counts this
+        // CTA in on the leader's barrier.
+        constexpr bool TF = Cfg::tf32;
+        constexpr int EL = TF ? 4 : 8;            // FP32 elements per lane and row
+        constexpr int L = Cfg::a32_lines;
         const int sw = warp - R::split0;
-        const int rsub = lane >> 3, chunk = lane & 7, c8 = chunk * 8;
+        const int rsub = lane >> 3, chunk = lane & 7;
         const uint32_t aready_leader0 = map_to_rank(aready0, 0);
         constexpr int RW = kSmemSplitRows, IT = RW / 4;   // rows per warp, 4-row steps
-        // L2 prefetch of this warp's rows x 64 K of one block (two 128-byte
-        // lines per row); a hint only, so it may run ahead of the grid
-        // dependency below
+        // L2 prefetch of this warp's rows of one block (L 128-byte lines per
+        // row); a hint only, so it may run ahead of the grid dependency below
         auto prefetch_block = [&](int arow_, int kb_) {
 #pragma unroll
-            for (int t = lane; t < 2 * RW; t += 32) {
-                const int prow = arow_ + RW * sw + (t >> 1);
-                const int pk = kb_ * 64 + 32 * (t & 1);
+            for (int t = lane; t < L * RW; t += 32) {
+                const int prow = arow_ + RW * sw + t / L;
+                const int pk = kb_ * Cfg::elems + 32 * (t % L);
                 if (prow < p.M && pk < p.K)
                     asm volatile("prefetch.global.L2 [%0];"
                                  :: "l"(p.A32 + (int64_t)prow * p.lda + pk));
@@ -594,22 +604,28 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 else if (i + 1 < nunits && wnext.kb0 + (kb + kAhead - w.kb1) < wnext.kb1)
                     prefetch_block(arow_next, wnext.kb0 + (kb + kAhead - w.kb1));
                 // this block's FP32 rows first: their latency overlaps the wait
-                const int k = kb * 64 + c8;
-                float4 x[IT][2];
+                const int k = kb * Cfg::elems + chunk * EL;
+                float4 x[IT][EL / 4];
 #pragma unroll
                 for (int it = 0; it < IT; ++it) {
                     const int row = arow + RW * sw + 4 * it + rsub;
-                    x[it][0] = x[it][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int v = 0; v < EL / 4; ++v) x[it][v] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (row < p.M && k < p.K) {
                         const float* src = p.A32 + (int64_t)row * p.lda + k;
-                        if (k + 7 < p.K) {
-                            x[it][0] = __ldg(reinterpret_cast<const float4*>(src));
-                            x[it][1] = __ldg(reinterpret_cast<const float4*>(src + 4));
+                        if (k + EL - 1 < p.K) {
+#pragma unroll
+                            for (int v = 0; v < EL / 4; ++v)
+                                x[it][v] = __ldg(reinterpret_cast<const float4*>(src + 4 * v));
                         } else {
-                            float t[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                            for (int j = 0; j < 8 && k + j < p.K; ++j) t[j] = src[j];
-                            x[it][0] = make_float4(t[0], t[1], t[2], t[3]);
-                            x[it][1] = make_float4(t[4], t[5], t[6], t[7]);
+                            float t[EL];
+#pragma unroll
+                            for (int j = 0; j < EL; ++j) t[j] = 0.f;
+                            for (int j = 0; j < EL && k + j < p.K; ++j) t[j] = src[j];
+#pragma unroll
+                            for (int v = 0; v < EL / 4; ++v)
+                                x[it][v] = make_float4(t[4 * v], t[4 * v + 1], t[4 * v + 2],
+                                                       t[4 * v + 3]);
                         }
                     }
                 }
@@ -619,16 +635,32 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     const uint32_t st = smem_u32(smem + s * Cfg::stage_bytes);
 #pragma unroll
                     for (int it = 0; it < IT; ++it) {
-                        uint4 q0, q1, q2;
-                        split_bf16x3_pair(x[it][0].x, x[it][0].y, q0.x, q1.x, q2.x);
-                        split_bf16x3_pair(x[it][0].z, x[it][0].w, q0.y, q1.y, q2.y);
-                        split_bf16x3_pair(x[it][1].x, x[it][1].y, q0.z, q1.z, q2.z);
-                        split_bf16x3_pair(x[it][1].z, x[it][1].w, q0.w, q1.w, q2.w);
                         const int r = RW * sw + 4 * it + rsub;
                         const uint32_t off = r * 128 + ((chunk ^ (r & 7)) << 4);
-                        st_shared_v4(st + off, q0);
-                        st_shared_v4(st + kATile + off, q1);
-                        st_shared_v4(st + 2 * kATile + off, q2);
+                        if constexpr (TF) {
+                            // TF32x3: hi and lo, FP32 containers (no scaling)
+                            float4 hi, lo;
+                            split_tf32x2(x[it][0].x, hi.x, lo.x);
+                            split_tf32x2(x[it][0].y, hi.y, lo.y);
+                            split_tf32x2(x[it][0].z, hi.z, lo.z);
+                            split_tf32x2(x[it][0].w, hi.w, lo.w);
+                            st_shared_v4(st + off, make_uint4(__float_as_uint(hi.x),
+                                                              __float_as_uint(hi.y),
+                                                              __float_as_uint(hi.z),
+                                                              __float_as_uint(hi.w)));
+                            st_shared_v4(st + kATile + off,
+                                         make_uint4(__float_as_uint(lo.x), __float_as_uint(lo.y),
+                                                    __float_as_uint(lo.z), __float_as_uint(lo.w)));
+                        } else {
+                            uint4 q0, q1, q2;
+                            split_bf16x3_pair(x[it][0].x, x[it][0].y, q0.x, q1.x, q2.x);
+                            split_bf16x3_pair(x[it][0].z, x[it][0].w, q0.y, q1.y, q2.y);
+                            split_bf16x3_pair(x[it][EL / 8].x, x[it][EL / 8].y, q0.z, q1.z, q2.z);
+                            split_bf16x3_pair(x[it][EL / 8].z, x[it][EL / 8].w, q0.w, q1.w, q2.w);
+                            st_shared_v4(st + off, q0);
+                            st_shared_v4(st + kATile + off, q1);
+                            st_shared_v4(st + 2 * kATile + off, q2);
+                        }
                     }
                     fence_proxy_async_smem();        // generic writes -> the tensor core
                 }
@@ -639,7 +671,6 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 if (sw == 0 && lane == 0) mbar_arrive_remote(aready_leader0 + 8 * s);
             }
         }
-        if (!ok) *abort_flag = 1;
     } else if (Cfg::TM && warp >= R::split0 && warp < R::split0 + R::split) {
         // ------------------------------------------------------ split warps
         // Split every K block of this cluster's tiles, as soon as its FP32
@@ -1036,6 +1067,9 @@ cudaError_t launch_kblock_t(const CUtensorMap& mapA, const CUtensorMap& mapB,
 }  // namespace
 
 int gemm_kblock_clusters(int mode, int bn, int fused, int sms) {
+    if (fused == 3 && mode == kModeTf32x3)
+        return bn == 128 ? max_clusters_t<kModeTf32x3, 128, 3>(sms)
+                         : max_clusters_t<kModeTf32x3, 256, 3>(sms);
     if (fused == 3)
         return bn == 128 ? max_clusters_t<kModeBf16x9, 128, 3>(sms)
                          : max_clusters_t<kModeBf16x9, 256, 3>(sms);
@@ -1075,9 +1109,13 @@ cudaError_t launch_gemm_kblock(int mode, int bn, int fused, const CUtensorMap& m
     const int clusters = sched_grid_clusters(tiles, q.tail_tiles, q.tail_clusters, resident);
     cudaError_t e;
     if (fused == 3) {
-        if (mode != kModeBf16x9 || !q.A32) return cudaErrorInvalidValue;
-        e = bn == 128 ? launch_kblock_t<kModeBf16x9, 128, 3>(mapA, mapB, mapC, q, clusters, stream, pdl)
-                      : launch_kblock_t<kModeBf16x9, 256, 3>(mapA, mapB, mapC, q, clusters, stream, pdl);
+        if ((mode != kModeBf16x9 && mode != kModeTf32x3) || !q.A32) return cudaErrorInvalidValue;
+        if (mode == kModeTf32x3)
+            e = bn == 128 ? launch_kblock_t<kModeTf32x3, 128, 3>(mapA, mapB, mapC, q, clusters, stream, pdl)
+                          : launch_kblock_t<kModeTf32x3, 256, 3>(mapA, mapB, mapC, q, clusters, stream, pdl);
+        else
+            e = bn == 128 ? launch_kblock_t<kModeBf16x9, 128, 3>(mapA, mapB, mapC, q, clusters, stream, pdl)
+                          : launch_kblock_t<kModeBf16x9, 256, 3>(mapA, mapB, mapC, q, clusters, stream, pdl);
     } else if (fused) {
         if (mode != kModeBf16x9 || bn != 128) return cudaErrorInvalidValue;
         e = launch_kblock_t<kModeBf16x9, 128, 1>(mapA, mapB, mapC, q, clusters, stream, pdl);

@@ -88,7 +88,8 @@ typedef enum {
 typedef enum {
     EMU_PATH_AUTO = 0,     /* the library chooses per call */
     EMU_PATH_TWOPASS = 1,  /* split kernels write the pieces to the workspace, then the GEMM */
-    EMU_PATH_FUSED = 2,    /* one kernel reads FP32 A and splits it into shared memory */
+    EMU_PATH_FUSED = 2,    /* one kernel reads FP32 A and splits it into shared memory
+                              (BF16x9 and TF32x3) */
     EMU_PATH_FUSED_TMEM = 3 /* the same, split into tensor memory (128-wide tiles) */
 } emu_path_t;
 
@@ -300,11 +301,12 @@ emu_status_t emu_sgemm_noalloc(int transA, int transB, int64_t M, int64_t N, int
 /* Select the implementation of the tensor-core modes for later calls on this
  * process (EMU_PATH_AUTO by default; the environment variable
  * EMU_SGEMM_PATH=auto|twopass|fused|fused_tmem sets the initial value).
- * FUSED and FUSED_TMEM apply to BF16x9 with op(A) = A stored with 16-byte
- * aligned rows (lda % 4 == 0); other calls run two-pass.  AUTO takes FUSED
- * for M >= 4096 and 128 < N <= 256, FUSED_TMEM for M >= 4096 and N <= 128,
- * two-pass otherwise.  Not thread-safe with respect to concurrent emu_sgemm
- * calls. */
+ * FUSED applies to BF16x9 and TF32x3, FUSED_TMEM to BF16x9, each with
+ * op(A) = A stored with 16-byte aligned rows (lda % 4 == 0); other calls run
+ * two-pass.  AUTO takes FUSED for BF16x9 with M >= 4096 and 128 < N <= 256,
+ * FUSED_TMEM for BF16x9 with M >= 4096 and N <= 128, two-pass otherwise
+ * (TF32x3 split on chip was measured no faster than two-pass).  Not
+ * thread-safe with respect to concurrent emu_sgemm calls. */
 emu_status_t emu_set_path(int path);
 int emu_get_path(void);
 

@@ -160,3 +160,18 @@ def test_ladder_modes_form_their_products(emu, kind, mode, shape):
     assert np.array_equal(C.view(np.uint32), want.view(np.uint32))
     if mode in ("tf32x3", "tf32x3_oy"):
         assert np.array_equal(C, BC.exact(A, B, tA, tB).astype(np.float32))
+
+
+@pytest.mark.parametrize("shape", SMALL + [(12288, 256, 1024, 0, 1), (1536, 512, 700, 0, 1)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("kind", ["a0", "b0"])
+def test_tf32x3_on_chip_forms_its_products(emu, kind, shape):
+    """TF32x3 with A split in shared memory by the GEMM kernel: the exact
+    product, bit for bit, with the on-chip kernel asserted to have run."""
+    M, N, K, tA, tB = shape
+    A, B = BC.make(kind, M, N, K, tA, tB, seed=M + 5 * N + K)
+    C, ran = _gemm(emu, A, B, tA, tB, mode="tf32x3", path="fused")
+    assert ran == ["gemm_fused"], ran
+    E = BC.exact(A, B, tA, tB).astype(np.float32)
+    assert np.array_equal(C.view(np.uint32), E.view(np.uint32))
+    _check_oracle_sample(A, B, tA, tB, C, fn=oracle.gemm_tf32x3)

@@ -327,20 +327,25 @@ class _fused_path:
 @pytest.mark.parametrize("shape", SHAPES + [(1000, 700, 300), (257, 129, 4096)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("transB", [0, 1])
-@pytest.mark.parametrize("path", ON_CHIP)
-def test_fused_path_every_element(emu, shape, transB, path):
+@pytest.mark.parametrize("path,mode", [("fused", "bf16x9"), ("fused_tmem", "bf16x9"),
+                                       ("fused", "tf32x3")])
+def test_fused_path_every_element(emu, shape, transB, path, mode):
     M, N, K = shape
     r = W.rng(M * 11 + N * 5 + K + transB)
     A = W.normal(r, (M, K))
     B = W.normal(r, (N, K) if transB else (K, N))
     C0 = W.uniform(r, (M, N))
     with _fused_path(emu, path):
-        C = _run(emu, A, B, False, transB, 1.5, -0.75, C0, "bf16x9")
+        C = _run(emu, A, B, False, transB, 1.5, -0.75, C0, mode)
     Cref, Sabs = oracle.gemm_ref(A, B, False, transB, 1.5, -0.75, C0)
-    assert checks.error_ratio(C, Cref, Sabs, K, 1.5, -0.75, C0) <= 1.0
-    C2 = _run(emu, A, B, False, transB, 1.5, -0.75, C0, "bf16x9")      # two-pass
-    bound = checks.elementwise_bound(K, 1.5, -0.75, Sabs, C0)
+    assert checks.error_ratio(C, Cref, Sabs, K, 1.5, -0.75, C0, mode=mode) <= 1.0
+    C2 = _run(emu, A, B, False, transB, 1.5, -0.75, C0, mode)          # two-pass
+    bound = checks.elementwise_bound(K, 1.5, -0.75, Sabs, C0, mode=mode)
     assert np.all(np.abs(C.astype(np.float64) - C2) <= bound)
+    if mode == "tf32x3" and K >= 32:
+        # the same pieces and the same K blocks: the same bits as two-pass
+        # unless a split tail groups the blocks differently
+        assert np.mean(C == C2) > 0.5
 
 
 @pytest.mark.parametrize("path", ON_CHIP)
@@ -442,8 +447,8 @@ def test_tail_parts_with_alpha_beta(emu, shape, transB, path, mode):
     clusters -- with alpha, beta and C0 applied once by the tile's owner:
     within each mode's bound on every element (sampled on the largest
     shapes) and the same bits on a second call."""
-    if path in ON_CHIP and mode != "bf16x9":
-        pytest.skip("the on-chip paths are BF16x9 only")
+    if (path == "fused_tmem" and mode != "bf16x9") or (path == "fused" and mode not in ("bf16x9", "tf32x3")):
+        pytest.skip("on-chip splits: BF16x9 (both kernels) and TF32x3 (shared memory)")
     M, N, K = shape
     r = W.rng(M + 5 * N + 11 * K)
     A = W.normal(r, (M, K))
