@@ -70,13 +70,15 @@ cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int6
 cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
                                 float* HI, float* LO, int64_t ldp, cudaStream_t stream,
                                 float lo_scale = 1.0f, bool pdl = false);
-// The pieces a tensor-core mode reads, as consecutive planes of rows x ldp
-// elements (BF16 bits or TF32-valued FP32) starting at `planes`.
+// The pieces a tensor-core mode reads, as planes of rows x ldp elements
+// (BF16 bits or TF32-valued FP32) starting at `planes`, plane_rows rows of
+// ldp apart (0: rows, consecutive planes; more: the rows of a panel of a
+// larger set of planes).
 // pdl: launch as a programmatic dependent of the kernel ahead in the stream
 // (only where the two are independent); the split still completes after it.
 cudaError_t launch_split_pieces(int mode, const float* X, int64_t rows, int64_t cols, int64_t ld,
                                 int trans, void* planes, int64_t ldp, cudaStream_t stream,
-                                bool pdl = false);
+                                bool pdl = false, int64_t plane_rows = 0);
 // Bytes of one piece element of a mode.
 constexpr int mode_piece_bytes(int m) { return mode_is_tf32(m) ? 4 : 2; }
 // mode: one of the kMode* variants; bn: tile width 128 or 256 (the two

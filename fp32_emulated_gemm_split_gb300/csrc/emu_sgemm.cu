@@ -37,6 +37,7 @@ struct DeviceState {
     // and per-chunk events (created on first use, kept until exit)
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t ev_in[kHostChunksMax] = {}, ev_done[kHostChunksMax] = {};
+    cudaEvent_t ev_panel = nullptr;      // each column panel of op(B) landed
     // the GEMM's stream-K tail: one slot of partial sums per cluster (grown on
     // demand), flags (zeroed once) and the epoch that marks this call's flags
     void* part = nullptr;
@@ -186,15 +187,18 @@ EncodeTiledFn encode_fn() {
 }
 
 // Tensor map over `planes` row-major planes of rows x cols elements (row
-// stride ld elements, plane stride rows*ld), box of box_cols x box_rows,
-// 128-byte swizzle, zero fill outside the matrix.
+// stride ld elements, plane stride plane_rows*ld, plane_rows 0 meaning
+// rows), box of box_cols x box_rows, 128-byte swizzle, zero fill outside the
+// matrix.
 emu_status_t make_plane_map(CUtensorMap* map, const void* base, bool fp32, int64_t rows,
-                            int64_t cols, int64_t ld, int planes, int box_cols, int box_rows) {
+                            int64_t cols, int64_t ld, int planes, int box_cols, int box_rows,
+                            int64_t plane_rows = 0) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return EMU_ERR_CUDA;
     const int esize = fp32 ? 4 : 2;
+    const int64_t prow = plane_rows > 0 ? plane_rows : rows;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
-    cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(rows * ld * esize)};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(prow * ld * esize)};
     cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
     cuuint32_t elem_strides[3] = {1, 1, 1};
     CUresult r = enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -322,12 +326,46 @@ struct BPieces {
     int64_t ld = 0;
 };
 
+// The tensor-core GEMM on pieces already in device memory: op(A)'s as
+// planes of M rows x plane_ld(K), a_plane_rows rows apart, and op(B)^T's as
+// planes of N rows x b_ld, b_plane_rows rows apart (0: M, N).  Launched as a
+// programmatic dependent of the split ahead of it in the stream.
+emu_status_t gemm_on_pieces(int mode, const void* ap, int64_t a_plane_rows, const void* bp,
+                            int64_t b_ld, int64_t b_plane_rows, int64_t M, int64_t N, int64_t K,
+                            float alpha, float beta, float* C, int64_t ldc, DeviceState* d,
+                            cudaStream_t stream) {
+    const int64_t ldp = plane_ld(K);
+    const int tf32 = mode_is_tf32(mode);
+    const int planes = mode_pieces(mode);
+    const int box_cols = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
+    // the two cheaper modes are built for 256-wide tiles only
+    const int bn = (mode == kModeBf16x9 || mode == kModeTf32x3) ? kblock_bn(N) : 256;
+    CUtensorMap mapA, mapB;
+    emu_status_t st = make_plane_map(&mapA, ap, tf32, M, K, ldp, planes, box_cols, 128, a_plane_rows);
+    if (st != EMU_OK) return st;
+    st = make_plane_map(&mapB, bp, tf32, N, K, b_ld, planes, box_cols, bn / 2, b_plane_rows);
+    if (st != EMU_OK) return st;
+
+    TcGemmParams p = {};
+    p.err = d->err;
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.num_kb = (int)((K + box_cols - 1) / box_cols);
+    p.tiles_m = (int)((M + 255) / 256);
+    p.tiles_n = (int)((N + bn - 1) / bn);
+    p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
+    CUtensorMap mapC = mapB;                 // placeholder when C is stored directly
+    p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
+    st = plan_tail(p, mode, 256, bn, 0, d);
+    if (st != EMU_OK) return st;
+    ProfScope ps(1, stream);
+    return from_cuda(launch_gemm_kblock(mode, bn, 0, mapA, mapB, mapC, p, d->sms, stream, true));
+}
+
 emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
                           float alpha, const float* A, int64_t lda, const float* B, int64_t ldb,
                           float beta, float* C, int64_t ldc, DeviceState* d, cudaStream_t stream,
                           bool b_ready = false, BPieces bext = {}) {
     const int64_t ldp = plane_ld(K);
-    const int tf32 = mode_is_tf32(mode);
     const int planes = mode_pieces(mode);
     const int esize = mode_piece_bytes(mode);
     const size_t a_bytes = (size_t)planes * M * ldp * esize;
@@ -352,35 +390,10 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
         e = launch_split_pieces(mode, B, N, K, ldb, !transB, wb, ldp, stream, true);
     }
     if (e != cudaSuccess) return from_cuda(e);
-
-    const int box_cols = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
-    // the two cheaper modes are built for 256-wide tiles only
-    const int bn = (mode == kModeBf16x9 || mode == kModeTf32x3) ? kblock_bn(N) : 256;
-    CUtensorMap mapA, mapB;
-    st = make_plane_map(&mapA, wa, tf32, M, K, ldp, planes, box_cols, 128);
-    if (st != EMU_OK) return st;
     if (bext.p)
-        st = make_plane_map(&mapB, bext.p, tf32, N, K, bext.ld, planes, box_cols, bn / 2);
-    else
-        st = make_plane_map(&mapB, wb, tf32, N, K, ldp, planes, box_cols, bn / 2);
-    if (st != EMU_OK) return st;
-
-    TcGemmParams p = {};
-    p.err = d->err;
-    p.M = (int)M; p.N = (int)N; p.K = (int)K;
-    p.num_kb = (int)((K + box_cols - 1) / box_cols);
-    p.tiles_m = (int)((M + 255) / 256);
-    p.tiles_n = (int)((N + bn - 1) / bn);
-    p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
-    CUtensorMap mapC = mapB;                 // placeholder when C is stored directly
-    p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
-    st = plan_tail(p, mode, 256, bn, 0, d);
-    if (st != EMU_OK) return st;
-    {
-        ProfScope ps(1, stream);
-        e = launch_gemm_kblock(mode, bn, 0, mapA, mapB, mapC, p, d->sms, stream, true);
-    }
-    return from_cuda(e);
+        return gemm_on_pieces(mode, wa, 0, bext.p, bext.ld, 0, M, N, K, alpha, beta, C, ldc, d,
+                              stream);
+    return gemm_on_pieces(mode, wa, 0, wb, ldp, 0, M, N, K, alpha, beta, C, ldc, d, stream);
 }
 
 // Whether op(A) can be read directly by the fused kernel: K-major rows that
@@ -618,13 +631,24 @@ emu_status_t emu_sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K, 
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
-// emu_sgemm_host for large problems: B goes first, then op(A) (and C when
-// beta != 0) in row chunks on a copy stream; each chunk's GEMM runs on the
-// caller's stream as soon as its rows have landed (B's pieces are split once,
-// by the first chunk), and each chunk of C goes back on a second copy stream
-// while the next chunk computes.  Host->device copies, the GEMM and
-// device->host copies overlap; the result is the same as one call's, as row
-// chunks of C are independent.
+// emu_sgemm_host for large problems.  Host->device copies go on a copy
+// stream in the order the GEMMs need them; each GEMM runs on the caller's
+// stream as soon as its operands have landed, and each row chunk of C goes
+// back on a second copy stream while the next chunk computes.  When op(B) is
+// wide (the two-pass kernels, N >= 2 panels), the first row chunk of op(A)
+// crosses first and is split once, then op(B) crosses in column panels, each
+// split into its rows of B's pieces and multiplied by that first chunk as it
+// lands, so that the tensor cores start after one panel rather than after
+// all of B (on GB300 the link moves about 210 GB/s to the device: 8192^2
+// FP32 take 1.3 ms).  The remaining row chunks then run full width with B's
+// pieces split once.  Otherwise B crosses first, whole, and the first chunk
+// splits it.  Row chunks of C are independent, so the result is what one
+// call computes (up to the last wave's K split, which follows the tile
+// count of each launch).
+constexpr int64_t kHostPanelCols = 1024;    // op(B) columns per panel
+constexpr int64_t kHostPanelRows = 2048;    // rows of the first chunk with panels
+constexpr int64_t kHostChunkBytes = int64_t(64) << 20;   // op(A) and C bytes per later chunk
+
 emu_status_t host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                             const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
                             float* C, int64_t ldc, int mode, DeviceState* d, float* dA, float* dB,
@@ -633,59 +657,119 @@ emu_status_t host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_
     if (!d->s_in) {
         e = cudaStreamCreateWithFlags(&d->s_in, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d->s_out, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d->ev_panel, cudaEventDisableTiming);
         for (int i = 0; i < kHostChunksMax && e == cudaSuccess; ++i) {
             e = cudaEventCreateWithFlags(&d->ev_in[i], cudaEventDisableTiming);
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d->ev_done[i], cudaEventDisableTiming);
         }
         if (e != cudaSuccess) return from_cuda(e);
     }
-    // row chunks: a multiple of 256 rows (whole tile rows), about 64 MB of
-    // op(A) each, 2 to kHostChunksMax of them
-    const int64_t row_bytes = (transA ? 1 : lda) * 4 * (transA ? K : 1) + N * 4;
-    int64_t nch = (M * row_bytes) / (int64_t(64) << 20);
-    nch = nch < 2 ? 2 : (nch > kHostChunksMax ? kHostChunksMax : nch);
-    const int64_t mc = (((M + nch - 1) / nch) + 255) / 256 * 256;
-    nch = (M + mc - 1) / mc;
-
     const Plan pl = plan_call(transA, M, N, K, dA, lda, mode, d);
+    const bool panels = pl.mode != EMU_MODE_FP32_SIMT && pl.fused == 0 &&
+                        N >= 2 * kHostPanelCols && b_bytes >= (size_t(16) << 20);
+    // at most 64 panels: wider ones for very wide B (multiples of 256 columns)
+    int64_t pw = kHostPanelCols;
+    if (panels && (N + pw - 1) / pw > 64) pw = ((N + 63) / 64 + 255) / 256 * 256;
+
+    // row chunks: whole 256-row tiles, about 64 MB of op(A) each; with panels
+    // the first chunk is kHostPanelRows rows and the rest are cut the same way
+    const int64_t row_bytes = (transA ? 1 : lda) * 4 * (transA ? K : 1) + N * 4;
+    int64_t bounds[kHostChunksMax + 1];
+    int nch = 0;
+    bounds[0] = 0;
+    int64_t m0 = 0;
+    if (panels) {
+        m0 = M < kHostPanelRows ? M : kHostPanelRows;
+        bounds[++nch] = m0;
+    }
+    if (m0 < M) {
+        const int64_t rest = M - m0;
+        const int64_t cap = kHostChunksMax - nch;
+        int64_t n = (rest * row_bytes) / kHostChunkBytes;
+        n = n < 2 ? 2 : n;
+        n = n > cap ? cap : n;
+        const int64_t mc = (((rest + n - 1) / n) + 255) / 256 * 256;
+        for (int64_t r = m0; r < M; r += mc) bounds[++nch] = (M - r < mc) ? M : r + mc;
+    }
+    int64_t max_rows = 0;
+    for (int i = 0; i < nch; ++i)
+        max_rows = bounds[i + 1] - bounds[i] > max_rows ? bounds[i + 1] - bounds[i] : max_rows;
+
     // size the workspace for the largest chunk now: no reallocation (and no
     // loss of B's pieces) inside the loop
+    const int64_t ldp = plane_ld(K);
+    const size_t pb = pl.mode == EMU_MODE_FP32_SIMT
+                          ? 0
+                          : (size_t)mode_pieces(pl.mode) * mode_piece_bytes(pl.mode) * ldp;
+    const size_t b_region = (pb * N + 1023) / 1024 * 1024;
     if (pl.mode != EMU_MODE_FP32_SIMT) {
-        const int64_t ldp = plane_ld(K);
-        const size_t pb = (size_t)mode_pieces(pl.mode) * mode_piece_bytes(pl.mode) * ldp;
-        const size_t need = pl.fused ? pb * N : (pb * N + 1023) / 1024 * 1024 + pb * mc;
+        const size_t need = pl.fused ? pb * N : b_region + pb * max_rows;
         emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, need);
         if (st != EMU_OK) return st;
     }
+    uint8_t* wb = static_cast<uint8_t*>(d->ws);
+    uint8_t* wa = wb + b_region;
+    const size_t prow = pb / mode_pieces(pl.mode == EMU_MODE_FP32_SIMT ? kModeBf16x9 : pl.mode);
+
     // the copy streams start after the caller's earlier work on its stream
     e = cudaEventRecord(d->ev_done[0], stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(d->s_in, d->ev_done[0], 0);
-    if (e == cudaSuccess && b_bytes)
+    if (e == cudaSuccess && b_bytes && !panels)
         e = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, d->s_in);
     emu_status_t st = EMU_OK;
-    for (int64_t i = 0; i < nch && e == cudaSuccess && st == EMU_OK; ++i) {
-        const int64_t m0 = i * mc, rows = (M - m0 < mc) ? M - m0 : mc;
+    for (int i = 0; i < nch && e == cudaSuccess && st == EMU_OK; ++i) {
+        const int64_t r0 = bounds[i], rows = bounds[i + 1] - bounds[i];
         if (transA == 0) {
-            e = cudaMemcpyAsync(dA + m0 * lda, A + m0 * lda, size_t((rows - 1) * lda + K) * 4,
+            e = cudaMemcpyAsync(dA + r0 * lda, A + r0 * lda, size_t((rows - 1) * lda + K) * 4,
                                 cudaMemcpyHostToDevice, d->s_in);
-        } else {   // op(A)'s rows m0.. are columns of the stored K x M matrix
-            e = cudaMemcpy2DAsync(dA + m0, size_t(lda) * 4, A + m0, size_t(lda) * 4,
+        } else {   // op(A)'s rows r0.. are columns of the stored K x M matrix
+            e = cudaMemcpy2DAsync(dA + r0, size_t(lda) * 4, A + r0, size_t(lda) * 4,
                                   size_t(rows) * 4, size_t(K), cudaMemcpyHostToDevice, d->s_in);
         }
         const size_t c_chunk = size_t((rows - 1) * ldc + N) * 4;
         if (e == cudaSuccess && beta != 0.0f)
-            e = cudaMemcpyAsync(dC + m0 * ldc, C + m0 * ldc, c_chunk, cudaMemcpyHostToDevice,
+            e = cudaMemcpyAsync(dC + r0 * ldc, C + r0 * ldc, c_chunk, cudaMemcpyHostToDevice,
                                 d->s_in);
         if (e == cudaSuccess) e = cudaEventRecord(d->ev_in[i], d->s_in);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, d->ev_in[i], 0);
         if (e != cudaSuccess) break;
-        st = run_planned(pl, transA, transB, rows, N, K, alpha, transA ? dA + m0 : dA + m0 * lda,
-                         lda, dB, ldb, beta, dC + m0 * ldc, ldc, d, stream, i > 0);
-        if (st != EMU_OK) break;
+        const float* Ai = transA ? dA + r0 : dA + r0 * lda;
+        if (panels && i == 0) {
+            {
+                ProfScope ps(0, stream);
+                e = launch_split_pieces(pl.mode, Ai, rows, K, lda, transA, wa, ldp, stream);
+            }
+            for (int64_t j0 = 0; j0 < N && e == cudaSuccess && st == EMU_OK; j0 += pw) {
+                const int64_t w = N - j0 < pw ? N - j0 : pw;
+                // op(B)'s columns j0..j0+w: rows of B (transB) or a column block
+                if (transB)
+                    e = cudaMemcpyAsync(dB + j0 * ldb, B + j0 * ldb, size_t((w - 1) * ldb + K) * 4,
+                                        cudaMemcpyHostToDevice, d->s_in);
+                else
+                    e = cudaMemcpy2DAsync(dB + j0, size_t(ldb) * 4, B + j0, size_t(ldb) * 4,
+                                          size_t(w) * 4, size_t(K), cudaMemcpyHostToDevice,
+                                          d->s_in);
+                if (e == cudaSuccess) e = cudaEventRecord(d->ev_panel, d->s_in);
+                if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, d->ev_panel, 0);
+                if (e != cudaSuccess) break;
+                {
+                    ProfScope ps(0, stream);
+                    e = launch_split_pieces(pl.mode, transB ? dB + j0 * ldb : dB + j0, w, K, ldb,
+                                            !transB, wb + j0 * prow, ldp, stream, false, N);
+                }
+                if (e == cudaSuccess)
+                    st = gemm_on_pieces(pl.mode, wa, 0, wb + j0 * prow, ldp, N, rows, w, K, alpha,
+                                        beta, dC + j0, ldc, d, stream);
+            }
+        } else {
+            st = run_planned(pl, transA, transB, rows, N, K, alpha, Ai, lda, dB, ldb, beta,
+                             dC + r0 * ldc, ldc, d, stream, i > 0);
+        }
+        if (st != EMU_OK || e != cudaSuccess) break;
         e = cudaEventRecord(d->ev_done[i], stream);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(d->s_out, d->ev_done[i], 0);
         if (e == cudaSuccess)
-            e = cudaMemcpyAsync(C + m0 * ldc, dC + m0 * ldc, c_chunk, cudaMemcpyDeviceToHost,
+            e = cudaMemcpyAsync(C + r0 * ldc, dC + r0 * ldc, c_chunk, cudaMemcpyDeviceToHost,
                                 d->s_out);
     }
     // wait for everything issued, whatever failed
@@ -981,6 +1065,8 @@ emu_status_t emu_shutdown(void) {
                 if (d.ev_done[j]) cudaEventDestroy(d.ev_done[j]);
                 d.ev_in[j] = d.ev_done[j] = nullptr;
             }
+            if (d.ev_panel) cudaEventDestroy(d.ev_panel);
+            d.ev_panel = nullptr;
             d.s_in = d.s_out = nullptr;
         }
     }

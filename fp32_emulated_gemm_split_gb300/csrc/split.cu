@@ -316,8 +316,8 @@ cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int6
 
 cudaError_t launch_split_pieces(int mode, const float* X, int64_t rows, int64_t cols, int64_t ld,
                                 int trans, void* planes, int64_t ldp, cudaStream_t stream,
-                                bool pdl) {
-    const int64_t n = rows * ldp;
+                                bool pdl, int64_t plane_rows) {
+    const int64_t n = (plane_rows > 0 ? plane_rows : rows) * ldp;
     if (mode_is_tf32(mode)) {
         float* hi = static_cast<float*>(planes);
         return launch_split_tf32x2(X, rows, cols, ld, trans, hi,

@@ -166,14 +166,21 @@ emu_status_t emu_sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
  * stream before it returns, so C holds the result on return.  Same
  * arguments, layout and error codes as emu_sgemm; the device buffers are
  * grown on demand and released by emu_shutdown().  When more than 64 MB
- * move (and M >= 512), the copies are pipelined with the GEMM: B first, then
- * op(A) and C in row chunks of whole 256-row tiles on a library-owned copy
- * stream, each chunk's GEMM on `stream` as its rows land (B's pieces split
- * once), and C's chunks back on a second library-owned stream.  The result
- * meets the same accuracy bound as one emu_sgemm call; it is bit for bit the
- * same unless the split of the GEMM's last wave along K (which depends on the
- * tile count) differs between the call and its chunks.  Host buffers in
- * pinned memory let the copies overlap; pageable ones work too.
+ * move (and M >= 512), the copies are pipelined with the GEMM: op(A) and C
+ * cross in row chunks of whole 256-row tiles on a library-owned copy
+ * stream, each chunk's GEMM runs on `stream` as its rows land, and C's
+ * chunks go back on a second library-owned stream.  B crosses first, whole,
+ * and the first chunk splits it -- except where the two-pass kernels run
+ * with N >= 2048 and B of at least 16 MiB: there op(A)'s first 2048 rows
+ * cross first, then op(B) in column panels of 1024 columns (wider when there
+ * would be more than 64), each split into its rows of B's pieces and
+ * multiplied by those first rows as it lands, so that the tensor cores start
+ * after one panel instead of all of B; the later chunks reuse B's pieces.
+ * The result meets the same accuracy bound as one emu_sgemm call; it is bit
+ * for bit the same unless the split of the GEMM's last wave along K (which
+ * depends on the tile count of each launch) differs between the call and
+ * its chunks or panels.  Host buffers in pinned memory let the copies
+ * overlap; pageable ones work too.
  */
 emu_status_t emu_sgemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K,
                             float alpha, const float* A, int64_t lda,

@@ -140,6 +140,24 @@ def test_host_entry_point_pipelined(emu, kind):
     assert np.array_equal(C.view(np.uint32), E.view(np.uint32))
 
 
+@pytest.mark.parametrize("kind,transB", [("a2", 0), ("b1", 1), ("b2", 0)])
+def test_host_entry_point_column_panels(emu, kind, transB):
+    """emu_sgemm_host with a wide op(B) (3000 x 2304 x 1900, B 17.5 MB): B's
+    column panels are split into their rows of B's pieces as they land and
+    multiplied by op(A)'s first 2048 rows; the remaining rows then use the
+    whole of B's pieces.  Exact, so bit for bit on every output."""
+    A, B = BC.make(kind, 3000, 2304, 1900, 0, transB, seed=8 + transB)
+    E = BC.exact(A, B, 0, transB).astype(np.float32)
+    emu.emu_profile_enable(True)
+    try:
+        C = emu.emu_sgemm_host(A, B, transB=bool(transB))
+        launches = emu.emu_profile_read("gemm_tc")[0]
+    finally:
+        emu.emu_profile_enable(False)
+    assert launches == 3 + 2, launches          # three panels, two more row chunks
+    assert np.array_equal(C.view(np.uint32), E.view(np.uint32))
+
+
 LADDER = {"tf32x3": oracle.gemm_tf32x3, "tf32x3_oy": oracle.gemm_tf32x3_oy,
           "bf16x3": oracle.gemm_bf16x3, "tf32": oracle.gemm_tf32}
 

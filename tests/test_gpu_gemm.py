@@ -263,6 +263,69 @@ def test_host_entry_pipelined_rows_match_one_call(emu, transA, transB, beta, mod
         assert np.array_equal(dev, host)
 
 
+def _profiled(emu, fn):
+    """Run fn with the launch counters on; returns (result, launches by kind)."""
+    emu.emu_profile_enable(True)
+    try:
+        out = fn()
+        counts = {k: emu.emu_profile_read(k)[0] for k in ("split", "gemm_tc", "gemm_fused")}
+    finally:
+        emu.emu_profile_enable(False)
+    return out, counts
+
+
+@pytest.mark.parametrize("transA,transB,beta,mode",
+                         [(0, 0, 0.0, "bf16x9"), (1, 1, 0.5, "bf16x9"), (0, 1, -1.0, "tf32x3"),
+                          (1, 0, 1.0, "bf16x3"), (0, 0, 0.0, "tf32"), (0, 1, 0.25, "tf32x3_oy")])
+def test_host_entry_column_panels(emu, transA, transB, beta, mode):
+    """A wide op(B) crosses to the device in column panels, each multiplied by
+    op(A)'s first 2048 rows as it lands; the rest of op(A) follows in row
+    chunks.  M = 5000, N = 2600 (panels of 1024, 1024 and 552 columns), K =
+    1700 (B is 17.7 MB): three panel GEMMs and two row-chunk GEMMs, every
+    split one launch (A's first chunk, three panels, two chunks)."""
+    M, N, K = 5000, 2600, 1700
+    r = W.rng(40 + transA + 2 * transB)
+    A = W.normal(r, (K, M) if transA else (M, K))
+    B = W.normal(r, (N, K) if transB else (K, N))
+    C0 = W.normal(r, (M, N))
+    host, counts = _profiled(emu, lambda: emu.emu_sgemm_host(
+        A, B, C0.copy(), transA=transA, transB=transB, alpha=0.75, beta=beta, mode=mode))
+    assert counts == {"split": 6, "gemm_tc": 5, "gemm_fused": 0}, counts
+    dev = _run(emu, A, B, transA, transB, alpha=0.75, beta=beta, C0=C0, mode=mode)
+    bmode = mode if mode in checks.MODE_EXTRA else "bf16x9"
+    mi, ni = W.sample_pairs(M, N, 2048, seed=7)
+    # every panel and chunk boundary is sampled too
+    edges = np.array([0, 2047, 2048, 2049, 3583, 3584, 4999])
+    cols = np.array([0, 1023, 1024, 2047, 2048, 2599])
+    mi = np.concatenate([mi, np.repeat(edges, cols.size)])
+    ni = np.concatenate([ni, np.tile(cols, edges.size)])
+    Cref, Sabs = oracle.gemm_ref(A, B, transA, transB, 0.75, beta, C0, pairs=(mi, ni))
+    for C in (host, dev):
+        assert checks.error_ratio(C[mi, ni], Cref, Sabs, K, 0.75, beta, C0[mi, ni],
+                                  mode=bmode) <= 1.0
+    bound = checks.elementwise_bound(K, 0.75, beta, Sabs, C0[mi, ni], mode=bmode)
+    assert np.all(np.abs(host[mi, ni].astype(np.float64) - dev[mi, ni]) <= 2 * bound)
+    assert np.all(np.isfinite(host))
+
+
+def test_host_entry_column_panels_wide_b(emu):
+    """N = 70000 > 64 panels of 1024: the panels widen (to 1280 columns) and
+    every column of C is still written."""
+    import torch
+    M, N, K = 600, 70000, 64
+    r = W.rng(44)
+    A = W.normal(r, (M, K))
+    B = W.normal(r, (K, N))
+    host, counts = _profiled(emu, lambda: emu.emu_sgemm_host(A, B))
+    assert counts["gemm_tc"] == 55, counts
+    dev = _run(emu, A, B)
+    mi, ni = W.sample_pairs(M, N, 4096, seed=8)
+    Cref, Sabs = oracle.gemm_ref(A, B, pairs=(mi, ni))
+    assert checks.error_ratio(host[mi, ni], Cref, Sabs, K, 1.0, 0.0) <= 1.0
+    assert np.all(np.isfinite(host))
+    assert np.allclose(host, dev, rtol=0, atol=1e-5 * float(np.abs(dev).max()))
+
+
 @pytest.mark.parametrize("path", ["auto", "fused_tmem"])
 def test_host_entry_pipelined_fused_shape(emu, path):
     """N = 256 rows of an MLIP layer: an on-chip path in every chunk (AUTO
