@@ -115,6 +115,12 @@ __global__ void __launch_bounds__(256) split2_rows_scalar(const float* __restric
 // op(X) = X^T: op(X)[r][c] = X[c * ld + r].  A 64 x 64 tile goes through
 // shared memory so that both the FP32 reads (along stored rows) and the
 // piece writes (along op rows, two BF16 per 4-byte store) are coalesced.
+// Grid: x walks the tiles along op columns (stored rows), y the tiles along
+// op rows, looping where there are more than gridDim.y of them.  Consecutive
+// blocks thus write neighbouring 128-byte segments of the same op rows:
+// measured on GB300 at 8192^2 (B's split for the square benchmark), 124.2 us
+// against 130.9 us with x along op rows; grouping the tiles in squares of
+// 2-16 or streaming stores gained nothing more.
 constexpr int kT = 64;
 
 __global__ void __launch_bounds__(256) split3_transposed(const float* __restrict__ X, int64_t rows,
@@ -125,35 +131,38 @@ __global__ void __launch_bounds__(256) split3_transposed(const float* __restrict
     griddep_launch_dependents();
     __shared__ float tile[kT][kT + 1];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
-    const int64_t r0 = (int64_t)blockIdx.x * kT;              // op rows  = stored columns
-    const int64_t c0 = (int64_t)blockIdx.y * kT;              // op cols  = stored rows
-    // load: stored row (c0 + i), stored columns r0 + tx, r0 + tx + 32
-    for (int i = ty; i < kT; i += 8) {
-        const int64_t sr = c0 + i;
+    const int64_t c0 = (int64_t)blockIdx.x * kT;              // op cols  = stored rows
+    for (int64_t rt = blockIdx.y; rt * kT < rows; rt += gridDim.y) {
+        const int64_t r0 = rt * kT;                           // op rows  = stored columns
+        // load: stored row (c0 + i), stored columns r0 + tx, r0 + tx + 32
+        for (int i = ty; i < kT; i += 8) {
+            const int64_t sr = c0 + i;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t sc = r0 + tx + 32 * h;
-            tile[i][tx + 32 * h] = (sr < cols && sc < rows) ? __ldcs(X + sr * ld + sc) : 0.0f;
+            for (int h = 0; h < 2; ++h) {
+                const int64_t sc = r0 + tx + 32 * h;
+                tile[i][tx + 32 * h] = (sr < cols && sc < rows) ? __ldcs(X + sr * ld + sc) : 0.0f;
+            }
         }
-    }
-    __syncthreads();
-    // store: op row (r0 + j), op columns c0 + 2*tx, c0 + 2*tx + 1
-    for (int j = ty; j < kT; j += 8) {
-        const int64_t r = r0 + j;
-        if (r >= rows) break;
-        const int64_t c = c0 + 2 * tx;
-        uint16_t a0, a1, a2, b0, b1, b2;
-        split_bf16x3(tile[2 * tx][j], a0, a1, a2);
-        split_bf16x3(tile[2 * tx + 1][j], b0, b1, b2);
-        const int64_t o = r * ldp + c;
-        if (c + 1 < cols && (o & 1) == 0) {
-            *reinterpret_cast<uint32_t*>(P0 + o) = a0 | (uint32_t(b0) << 16);
-            *reinterpret_cast<uint32_t*>(P1 + o) = a1 | (uint32_t(b1) << 16);
-            if (P2) *reinterpret_cast<uint32_t*>(P2 + o) = a2 | (uint32_t(b2) << 16);
-        } else {
-            if (c < cols) { P0[o] = a0; P1[o] = a1; if (P2) P2[o] = a2; }
-            if (c + 1 < cols) { P0[o + 1] = b0; P1[o + 1] = b1; if (P2) P2[o + 1] = b2; }
+        __syncthreads();
+        // store: op row (r0 + j), op columns c0 + 2*tx, c0 + 2*tx + 1
+        for (int j = ty; j < kT; j += 8) {
+            const int64_t r = r0 + j;
+            if (r >= rows) break;
+            const int64_t c = c0 + 2 * tx;
+            uint16_t a0, a1, a2, b0, b1, b2;
+            split_bf16x3(tile[2 * tx][j], a0, a1, a2);
+            split_bf16x3(tile[2 * tx + 1][j], b0, b1, b2);
+            const int64_t o = r * ldp + c;
+            if (c + 1 < cols && (o & 1) == 0) {
+                *reinterpret_cast<uint32_t*>(P0 + o) = a0 | (uint32_t(b0) << 16);
+                *reinterpret_cast<uint32_t*>(P1 + o) = a1 | (uint32_t(b1) << 16);
+                if (P2) *reinterpret_cast<uint32_t*>(P2 + o) = a2 | (uint32_t(b2) << 16);
+            } else {
+                if (c < cols) { P0[o] = a0; P1[o] = a1; if (P2) P2[o] = a2; }
+                if (c + 1 < cols) { P0[o + 1] = b0; P1[o + 1] = b1; if (P2) P2[o + 1] = b2; }
+            }
         }
+        __syncthreads();         // the tile is refilled by the next op-row tile
     }
     griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
@@ -170,33 +179,36 @@ __global__ void __launch_bounds__(256) split3_transposed_vec(const float* __rest
     griddep_launch_dependents();
     __shared__ float tile[kT][kT + 1];               // [op col (stored row)][op row]
     const int tid = threadIdx.x;
-    const int64_t r0 = (int64_t)blockIdx.x * kT;     // op rows  = stored columns
-    const int64_t c0 = (int64_t)blockIdx.y * kT;     // op cols  = stored rows
+    const int64_t c0 = (int64_t)blockIdx.x * kT;     // op cols  = stored rows
+    for (int64_t rt = blockIdx.y; rt * kT < rows; rt += gridDim.y) {
+        const int64_t r0 = rt * kT;                  // op rows  = stored columns
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int idx = tid + 256 * i;               // 0 .. 1023
-        const int k = idx >> 4, r4 = (idx & 15) * 4;
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(X + (c0 + k) * ld + r0 + r4));
-        tile[k][r4 + 0] = v.x;
-        tile[k][r4 + 1] = v.y;
-        tile[k][r4 + 2] = v.z;
-        tile[k][r4 + 3] = v.w;
-    }
-    __syncthreads();
-    const int rr = tid >> 2, cp = tid & 3;           // op row in tile, 16-element part
-    uint32_t w0[8], w1[8], w2[8];
+        for (int i = 0; i < 4; ++i) {
+            const int idx = tid + 256 * i;               // 0 .. 1023
+            const int k = idx >> 4, r4 = (idx & 15) * 4;
+            const float4 v = __ldcs(reinterpret_cast<const float4*>(X + (c0 + k) * ld + r0 + r4));
+            tile[k][r4 + 0] = v.x;
+            tile[k][r4 + 1] = v.y;
+            tile[k][r4 + 2] = v.z;
+            tile[k][r4 + 3] = v.w;
+        }
+        __syncthreads();
+        const int rr = tid >> 2, cp = tid & 3;           // op row in tile, 16-element part
+        uint32_t w0[8], w1[8], w2[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        split_bf16x3_pair(tile[16 * cp + 2 * i][rr], tile[16 * cp + 2 * i + 1][rr], w0[i], w1[i], w2[i]);
-    const int64_t o = (r0 + rr) * ldp + c0 + 16 * cp;
-    uint4* d0 = reinterpret_cast<uint4*>(P0 + o);
-    uint4* d1 = reinterpret_cast<uint4*>(P1 + o);
-    uint4* d2 = reinterpret_cast<uint4*>(P2 + o);
+        for (int i = 0; i < 8; ++i)
+            split_bf16x3_pair(tile[16 * cp + 2 * i][rr], tile[16 * cp + 2 * i + 1][rr], w0[i], w1[i], w2[i]);
+        const int64_t o = (r0 + rr) * ldp + c0 + 16 * cp;
+        uint4* d0 = reinterpret_cast<uint4*>(P0 + o);
+        uint4* d1 = reinterpret_cast<uint4*>(P1 + o);
+        uint4* d2 = reinterpret_cast<uint4*>(P2 + o);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        d0[q] = make_uint4(w0[4 * q], w0[4 * q + 1], w0[4 * q + 2], w0[4 * q + 3]);
-        d1[q] = make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
-        if (P2) d2[q] = make_uint4(w2[4 * q], w2[4 * q + 1], w2[4 * q + 2], w2[4 * q + 3]);
+        for (int q = 0; q < 2; ++q) {
+            d0[q] = make_uint4(w0[4 * q], w0[4 * q + 1], w0[4 * q + 2], w0[4 * q + 3]);
+            d1[q] = make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
+            if (P2) d2[q] = make_uint4(w2[4 * q], w2[4 * q + 1], w2[4 * q + 2], w2[4 * q + 3]);
+        }
+        __syncthreads();         // the tile is refilled by the next op-row tile
     }
     griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
@@ -208,30 +220,33 @@ __global__ void __launch_bounds__(256) split2_transposed(const float* __restrict
     griddep_launch_dependents();
     __shared__ float tile[kT][kT + 1];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int64_t r0 = (int64_t)blockIdx.x * kT;
-    const int64_t c0 = (int64_t)blockIdx.y * kT;
-    for (int i = ty; i < kT; i += 8) {
-        const int64_t sr = c0 + i;
+    const int64_t c0 = (int64_t)blockIdx.x * kT;
+    for (int64_t rt = blockIdx.y; rt * kT < rows; rt += gridDim.y) {
+        const int64_t r0 = rt * kT;
+        for (int i = ty; i < kT; i += 8) {
+            const int64_t sr = c0 + i;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t sc = r0 + tx + 32 * h;
-            tile[i][tx + 32 * h] = (sr < cols && sc < rows) ? __ldcs(X + sr * ld + sc) : 0.0f;
-        }
-    }
-    __syncthreads();
-    for (int j = ty; j < kT; j += 8) {
-        const int64_t r = r0 + j;
-        if (r >= rows) break;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t c = c0 + tx + 32 * h;
-            if (c < cols) {
-                float hi, lo;
-                split_tf32x2(tile[tx + 32 * h][j], hi, lo, lo_scale);
-                HI[r * ldp + c] = hi;
-                if (LO) LO[r * ldp + c] = lo;
+            for (int h = 0; h < 2; ++h) {
+                const int64_t sc = r0 + tx + 32 * h;
+                tile[i][tx + 32 * h] = (sr < cols && sc < rows) ? __ldcs(X + sr * ld + sc) : 0.0f;
             }
         }
+        __syncthreads();
+        for (int j = ty; j < kT; j += 8) {
+            const int64_t r = r0 + j;
+            if (r >= rows) break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t c = c0 + tx + 32 * h;
+                if (c < cols) {
+                    float hi, lo;
+                    split_tf32x2(tile[tx + 32 * h][j], hi, lo, lo_scale);
+                    HI[r * ldp + c] = hi;
+                    if (LO) LO[r * ldp + c] = lo;
+                }
+            }
+        }
+        __syncthreads();         // the tile is refilled by the next op-row tile
     }
     griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
@@ -259,6 +274,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, cudaStream_t stream, b
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The transposed kernels' grid: op-column tiles along x, op-row tiles along
+// y (at most 65535; the kernels loop over the rest).
+dim3 transposed_grid(int64_t rows, int64_t cols) {
+    const int64_t rt = (rows + kT - 1) / kT;
+    return dim3((unsigned)((cols + kT - 1) / kT), (unsigned)(rt < 65535 ? rt : 65535));
+}
+
 int grid_for(int64_t work, int threads) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -276,7 +298,7 @@ cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int6
     if (rows == 0 || cols == 0) return cudaSuccess;
     cudaError_t e;
     if (trans) {
-        const dim3 grid((unsigned)((rows + kT - 1) / kT), (unsigned)((cols + kT - 1) / kT));
+        const dim3 grid = transposed_grid(rows, cols);
         if (rows % kT == 0 && cols % kT == 0 && ld % 4 == 0 && ldp % 8 == 0 && aligned16(X) &&
             aligned16(P0) && aligned16(P1) && aligned16(P2))
             e = launch_pdl(split3_transposed_vec, grid, stream, pdl, X, rows, cols, ld, P0, P1, P2,
@@ -300,7 +322,7 @@ cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int6
     if (rows == 0 || cols == 0) return cudaSuccess;
     cudaError_t e;
     if (trans) {
-        const dim3 grid((unsigned)((rows + kT - 1) / kT), (unsigned)((cols + kT - 1) / kT));
+        const dim3 grid = transposed_grid(rows, cols);
         e = launch_pdl(split2_transposed, grid, stream, pdl, X, rows, cols, ld, HI, LO, ldp,
                        lo_scale);
     } else if (cols % 4 == 0 && ld % 4 == 0 && ldp % 4 == 0 && aligned16(X) && aligned16(HI) &&
