@@ -224,7 +224,7 @@ def bench_gpu(args):
                     "kernel": dom_name,
                     "peak_source": f"{peak_src} bf16 burst" + (" / 2 (tf32 nominal ratio)" if tf32_mode else ""),
                     "kernel_ms": round(per_launch_ms, 4)}
-        traffic = load_traffic(dom_name, args.workload, g.mode)
+        traffic = load_traffic(dom_name, g.name, g.mode)
         if traffic is not None:
             roofline["traffic"] = traffic
 
