@@ -210,13 +210,17 @@ emu_status_t make_plane_map(CUtensorMap* map, const void* base, bool fp32, int64
 
 // 2-D map over C for the bulk tensor stores of the GEMM epilogue (any beta;
 // with beta != 0 the epilogue reads C itself first): box of 16 columns x 32
-// rows, 64-byte swizzle.  Returns false (and the
-// kernel stores C directly) when C's rows are not 16-byte aligned.
+// rows, 64-byte swizzle.  The map covers the first N & ~3 columns only: a
+// bulk store clips a box at the edge of the map in whole 16-byte units
+// (measured on GB300: with N = 4k + 1..3 it wrote zeros up to column 4k + 3,
+// past C), so the epilogue stores the last N % 4 columns of each row itself.
+// Returns false (and the kernel stores C directly) when C's rows are not
+// 16-byte aligned or C is narrower than 4 columns.
 bool make_c_map(CUtensorMap* map, float* C, int64_t M, int64_t N, int64_t ldc) {
-    if ((ldc % 4) != 0 || (reinterpret_cast<uintptr_t>(C) & 15) != 0) return false;
+    if ((ldc % 4) != 0 || (reinterpret_cast<uintptr_t>(C) & 15) != 0 || N < 4) return false;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t dims[2] = {(cuuint64_t)(N & ~int64_t(3)), (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)(ldc * 4)};
     cuuint32_t box[2] = {16, 32};
     cuuint32_t elem_strides[2] = {1, 1};

@@ -842,9 +842,13 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                 // Stage 32 rows x 16 columns at a time in this warp's 2 KB
                 // buffer (64-byte swizzle: conflict-free writes) and let one
                 // bulk tensor store write them, coalesced and clipped at the
-                // matrix edge.  With beta != 0 each lane first reads its own
-                // row's 16 values of C (16-byte loads where they fit).
+                // edge of the C map, which ends at column N & ~3 (a bulk store
+                // clips in whole 16-byte units); each lane stores its row's
+                // last N % 4 columns itself.  With beta != 0 each lane first
+                // reads its own row's 16 values of C (16-byte loads where
+                // they fit).
                 constexpr int CB = Cfg::c_bufs;
+                const int n4 = p.N & ~3;                    // the C map's width
                 const uint32_t cst0 = smem_u32(cstage + (warp - R::acc0) * 2048 * CB);
                 // The cluster's last unit: all its MMAs have completed (this
                 // warp has drained the last partial), so no stage is read or
@@ -882,6 +886,14 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                         asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
                                      :: "r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                                      : "memory");
+                        // gc is a multiple of 4: a group at or past N & ~3
+                        // holds the (at most 3) columns the map leaves out
+                        if (gc >= n4 && gc < p.N && row < p.M) {
+                            float* dst = p.C + (int64_t)row * p.ldc + gc;
+                            dst[0] = v.x;
+                            if (gc + 1 < p.N) dst[1] = v.y;
+                            if (gc + 2 < p.N) dst[2] = v.z;
+                        }
                     }
                 };
                 if (row0 < p.M && last) {
@@ -897,7 +909,8 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     __syncwarp();
                     if (lane == 0) {
                         for (int ch = 0; ch < nch; ++ch)
-                            tma_store_2d(&mapC, col_base + 16 * ch, row0, lst0 + ch * 2048);
+                            if (col_base + 16 * ch < n4)
+                                tma_store_2d(&mapC, col_base + 16 * ch, row0, lst0 + ch * 2048);
                         bulk_commit();
                     }
                 } else if (row0 < p.M) {
@@ -911,7 +924,7 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&mapC, col_base + 16 * ch, row0, cst);
+                            if (col_base + 16 * ch < n4) tma_store_2d(&mapC, col_base + 16 * ch, row0, cst);
                             bulk_commit();
                         }
                     }

@@ -594,3 +594,39 @@ def test_misaligned_operands_and_long_k(emu, path):
         assert checks.error_ratio(C2, Cref2, Sabs2, 65536, 1.0, 0.0) <= 1.0
     finally:
         emu.emu_set_path("auto")
+
+
+@pytest.mark.parametrize("path,mode,M,K", [("twopass", "bf16x9", 300, 200),
+                                           ("twopass", "tf32x3", 300, 200),
+                                           ("fused", "bf16x9", 4200, 130),
+                                           ("fused_tmem", "bf16x9", 4200, 130),
+                                           ("twopass", "bf16x9", 1536, 700)])
+def test_c_columns_past_n_are_untouched(emu, path, mode, M, K):
+    """C as the first N columns of a wider matrix (ldc = 64, a multiple of
+    four, so the epilogue's bulk tensor stores run): columns N..63 keep their
+    values for every N = 1..33, beta = 0 and 1, and columns < N are right.
+    A bulk store clips at the edge of its map in 16-byte units, so the
+    library maps C only up to N & ~3 and stores the rest per lane.  The last
+    shape splits its last round along K (parts summed by the tile's owner)."""
+    import torch
+    old = emu.emu_get_path()
+    emu.emu_set_path(path)
+    try:
+        for N in list(range(1, 18)) + [21, 30, 31, 33]:
+            r = W.rng(N + M)
+            A = W.normal(r, (M, K))
+            B = W.normal(r, (K, N), std=K ** -0.5)
+            C0 = W.normal(r, (M, 64))
+            for beta in (0.0, 1.0):
+                Cs = to_dev(C0)
+                emu.emu_sgemm(to_dev(A), to_dev(B), Cs[:, :N], beta=beta, mode=mode)
+                torch.cuda.synchronize()
+                got = Cs.cpu().numpy()
+                assert np.array_equal(got[:, N:], C0[:, N:]), (N, beta)
+                mi, ni = W.sample_pairs(M, N, 512, seed=N)
+                Cref, Sabs = oracle.gemm_ref(A, B, beta=beta, C0=np.ascontiguousarray(C0[:, :N]),
+                                             pairs=(mi, ni))
+                assert checks.error_ratio(got[mi, ni], Cref, Sabs, K, 1.0, beta, C0[mi, ni],
+                                          mode=_bound_mode(mode)) <= 1.0, (N, beta)
+    finally:
+        emu.emu_set_path(old)
