@@ -45,11 +45,13 @@ def _draw(i):
              entry=ENTRIES[int(r.integers(0, len(ENTRIES)))],
              alpha=float([1.0, -0.75, 2.0 ** int(r.integers(-20, 21))][int(r.integers(0, 3))]),
              beta=float([0.0, 0.0, 1.0, 0.5, -2.0][int(r.integers(0, 5))]),
-             pads=[int(v) for v in r.integers(0, 9, 3)])
+             pads=[int(v) for v in r.integers(0, 9, 3)],
+             offs=[int(v) for v in r.integers(0, 4, 3)] if r.random() < 0.5 else [0, 0, 0])
     # the host-buffer entry point takes contiguous arrays; the split-B entry
     # point needs a tensor-core mode and some depth; noalloc a fitting problem
     if c["entry"] == "host":
         c["pads"] = [0, 0, 0]
+        c["offs"] = [0, 0, 0]
     if c["entry"] == "bsplit" and (c["mode"] == "fp32_simt" or K == 0):
         c["entry"] = "sgemm"
     ldp = max((K + 7) // 8 * 8, 8)
@@ -58,12 +60,14 @@ def _draw(i):
     return c, r
 
 
-def _padded(torch, X, pad):
-    """A device copy of X whose rows are `pad` elements longer (a strided view)."""
+def _padded(torch, X, pad, off=0):
+    """A device copy of X whose rows are `pad` elements longer and which
+    starts `off` elements into its allocation (a strided view; off = 1..3
+    leaves its base off the 16-byte grid), NaN around it."""
     rows, cols = X.shape
-    S = torch.full((rows, cols + pad), float("nan"), device="cuda")
-    S[:, :cols] = torch.from_numpy(np.ascontiguousarray(X)).cuda()
-    return S[:, :cols]
+    S = torch.full((rows + 1, cols + pad + off), float("nan"), device="cuda")
+    S[:rows, off:off + cols] = torch.from_numpy(np.ascontiguousarray(X)).cuda()
+    return S[:rows, off:off + cols]
 
 
 @pytest.mark.parametrize("i", range(NCASES))
@@ -82,11 +86,12 @@ def test_random_gemm(emu, i):
                                    alpha=c["alpha"], beta=c["beta"], mode=c["mode"])
             pad_ok = True
         else:
-            dA = _padded(torch, A, c["pads"][0])
-            dB = _padded(torch, B, c["pads"][1])
-            Cs = torch.full((M, N + c["pads"][2]), SENTINEL, device="cuda")
-            Cs[:, :N] = torch.from_numpy(C0).cuda()
-            dC = Cs[:, :N]
+            dA = _padded(torch, A, c["pads"][0], c["offs"][0])
+            dB = _padded(torch, B, c["pads"][1], c["offs"][1])
+            oc = c["offs"][2]
+            Cs = torch.full((M, N + c["pads"][2] + oc), SENTINEL, device="cuda")
+            Cs[:, oc:oc + N] = torch.from_numpy(C0).cuda()
+            dC = Cs[:, oc:oc + N]
             kw = dict(alpha=c["alpha"], beta=c["beta"], mode=c["mode"])
             if c["entry"] == "bsplit":
                 P = emu.emu_split_b(dB, transB=bool(tB), mode=c["mode"])
@@ -97,11 +102,17 @@ def test_random_gemm(emu, i):
                 emu.emu_sgemm(dA, dB, dC, transA=bool(tA), transB=bool(tB), **kw)
             torch.cuda.synchronize()
             full = Cs.cpu().numpy()
-            C = np.ascontiguousarray(full[:, :N])
-            pad_ok = bool(np.all(full[:, N:] == np.float32(SENTINEL)))
+            C = np.ascontiguousarray(full[:, oc:oc + N])
+            pad_ok = bool(np.all(full[:, :oc] == np.float32(SENTINEL)) and
+                          np.all(full[:, oc + N:] == np.float32(SENTINEL)))
     finally:
         emu.emu_set_path(old)
     assert pad_ok, f"case {i}: C written outside its {N} columns ({c})"
+    _check(c, i, A, B, C0, C)
+
+
+def _check(c, i, A, B, C0, C):
+    M, N, K, tA, tB = c["M"], c["N"], c["K"], c["tA"], c["tB"]
     assert np.all(np.isfinite(C)), f"case {i}: non-finite output ({c})"
     if K == 0:              # C = beta C0, one exact FP32 product per element
         assert np.array_equal(C, np.float32(c["beta"]) * C0), f"case {i} ({c})"
@@ -117,6 +128,56 @@ def test_random_gemm(emu, i):
     ratio = checks.error_ratio(C[mi, ni], Cref, Sabs, K, c["alpha"], c["beta"], C0[mi, ni],
                                mode=bmode)
     assert ratio <= 1.0, f"case {i}: error ratio {ratio} ({c})"
+
+
+def _draw_on_chip(i):
+    """Shapes for the on-chip split paths and the K-split last round: many
+    rows, at most 256 columns (or a ragged width above), K-major A."""
+    r = np.random.Generator(np.random.PCG64(9191 + i))
+    M = int(r.integers(4096, 20001))
+    N = int(r.integers(1, 257)) if r.random() < 0.75 else int(r.integers(257, 700))
+    K = int(np.exp(r.uniform(np.log(8), np.log(1200))))
+    c = dict(M=M, N=N, K=K, tA=0, tB=int(r.integers(0, 2)),
+             mode=["bf16x9", "tf32x3"][int(r.integers(0, 2))],
+             path=PATHS[int(r.integers(0, len(PATHS)))],
+             entry=["sgemm", "bsplit"][int(r.integers(0, 2))],
+             alpha=float([1.0, -0.75, 0.5][int(r.integers(0, 3))]),
+             beta=float([0.0, 1.0, 0.5][int(r.integers(0, 3))]),
+             pads=[int(v) for v in r.integers(0, 9, 3)],
+             offs=[int(v) for v in r.integers(0, 4, 3)] if r.random() < 0.3 else [0, 0, 0])
+    return c, r
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_gemm_on_chip_shapes(emu, i):
+    import torch
+    c, r = _draw_on_chip(i)
+    M, N, K, tB = c["M"], c["N"], c["K"], c["tB"]
+    A = W.normal(r, (M, K))
+    B = W.normal(r, (N, K) if tB else (K, N), std=K ** -0.5)
+    C0 = W.normal(r, (M, N))
+    old = emu.emu_get_path()
+    emu.emu_set_path(c["path"])
+    try:
+        dA = _padded(torch, A, c["pads"][0], c["offs"][0])
+        dB = _padded(torch, B, c["pads"][1], c["offs"][1])
+        oc = c["offs"][2]
+        Cs = torch.full((M, N + c["pads"][2] + oc), SENTINEL, device="cuda")
+        Cs[:, oc:oc + N] = torch.from_numpy(C0).cuda()
+        dC = Cs[:, oc:oc + N]
+        kw = dict(alpha=c["alpha"], beta=c["beta"], mode=c["mode"])
+        if c["entry"] == "bsplit":
+            P = emu.emu_split_b(dB, transB=bool(tB), mode=c["mode"])
+            emu.emu_sgemm_bsplit(dA, P, dC, **kw)
+        else:
+            emu.emu_sgemm(dA, dB, dC, transB=bool(tB), **kw)
+        torch.cuda.synchronize()
+        full = Cs.cpu().numpy()
+    finally:
+        emu.emu_set_path(old)
+    assert np.all(full[:, :oc] == np.float32(SENTINEL)), f"case {i} ({c})"
+    assert np.all(full[:, oc + N:] == np.float32(SENTINEL)), f"case {i} ({c})"
+    _check(c, i, A, B, C0, np.ascontiguousarray(full[:, oc:oc + N]))
 
 
 def test_no_device_error_after_fuzz(emu):
