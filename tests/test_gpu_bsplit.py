@@ -153,3 +153,29 @@ def test_bad_pieces_are_rejected(emu):
                               C.data_ptr(), 48, 2, h) == -1
     torch.cuda.synchronize()
     assert torch.all(C == 3.0)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("K", [1001, 1005, 1007, 64 + 3])
+def test_padding_columns_of_the_pieces_are_not_read(emu, mode, K):
+    """Columns K..ldbp-1 of the pieces hold NaN (BF16 0x7FC0, FP32 NaN): the
+    tensor copies clip at K, so the result is finite and equal, bit for bit,
+    to the same call on zero-padded pieces."""
+    import torch
+    r = W.rng(K)
+    M, N = 700, 300
+    A = to_dev(W.normal(r, (M, K)))
+    B = to_dev(W.normal(r, (N, K), std=K ** -0.5))
+    P = emu.emu_split_b(B, transB=True, mode=mode)
+    ref = torch.empty(M, N, device="cuda")
+    emu.emu_sgemm_bsplit(A, P, ref, mode=mode)
+    Q = P.clone()
+    if Q.dtype == torch.int16:
+        Q[:, :, K:] = 0x7FC0
+    else:
+        Q[:, :, K:] = float("nan")
+    out = torch.empty(M, N, device="cuda")
+    emu.emu_sgemm_bsplit(A, Q, out, mode=mode)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    assert torch.equal(out.view(torch.int32), ref.view(torch.int32))

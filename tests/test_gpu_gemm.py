@@ -630,3 +630,38 @@ def test_c_columns_past_n_are_untouched(emu, path, mode, M, K):
                                           mode=_bound_mode(mode)) <= 1.0, (N, beta)
     finally:
         emu.emu_set_path(old)
+
+
+@pytest.mark.parametrize("path,mode", [("fused", "bf16x9"), ("fused", "tf32x3"),
+                                       ("fused_tmem", "bf16x9")])
+@pytest.mark.parametrize("K", [129, 130, 131, 257, 1023])
+def test_on_chip_split_does_not_read_past_k(emu, path, mode, K):
+    """A is read as FP32 by the GEMM kernel (TMA into shared memory, or
+    16-byte loads by the split warps): with K = 4k + 1..3 and NaN in the
+    padding of A's rows (lda a multiple of 4, so the on-chip path runs), the
+    result is finite and within the bound."""
+    import torch
+    M, N = 4200, 200 if path == "fused" else 100
+    lda = (K + 3) // 4 * 4 + 4
+    r = W.rng(K + N)
+    A = W.normal(r, (M, K))
+    B = W.normal(r, (N, K), std=K ** -0.5)
+    S = torch.full((M, lda), float("nan"), device="cuda")
+    S[:, :K] = to_dev(A)
+    C = torch.empty(M, N, device="cuda")
+    old = emu.emu_get_path()
+    emu.emu_set_path(path)
+    try:
+        emu.emu_profile_enable(True)
+        emu.emu_sgemm(S[:, :K], to_dev(B), C, transB=True, mode=mode)
+        torch.cuda.synchronize()
+        ran = emu.emu_profile_read("gemm_fused")[0]
+        emu.emu_profile_enable(False)
+    finally:
+        emu.emu_set_path(old)
+    assert ran == 1
+    got = C.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    mi, ni = W.sample_pairs(M, N, 2048, seed=K)
+    Cref, Sabs = oracle.gemm_ref(A, B, transB=True, pairs=(mi, ni))
+    assert checks.error_ratio(got[mi, ni], Cref, Sabs, K, 1.0, 0.0, mode=_bound_mode(mode)) <= 1.0
