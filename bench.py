@@ -252,6 +252,7 @@ def bench_gpu(args):
             del dA, dB, dC
             torch.cuda.empty_cache()
             out["configs"] = bench_configs(emu, stream, peaks, peak_src)
+            out["ladder"] = bench_ladder(emu, stream, peaks, peak_src)
             dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
             dC = torch.from_numpy(C0).cuda() if C0 is not None else torch.empty((g.M, g.N), device="cuda")
         if not args.no_e2e:
@@ -449,6 +450,65 @@ def bench_configs(emu, stream, peaks, peak_src, reps=10):
     return res
 
 
+# The accuracy ladder on one shape: every tensor-core mode of the library,
+# its tensor products per emulated FP32 product and whether it runs on the
+# TF32 datapath (half the BF16 rate).
+LADDER = {"bf16x9": (9, False), "tf32x3": (3, True), "tf32x3_oy": (3, True),
+          "bf16x3": (3, False), "tf32": (1, True)}
+
+
+def bench_ladder(emu, stream, peaks, peak_src, reps=10):
+    """Every tensor-core mode on the 8192^3 workload's operands (drawn on the
+    GPU), 10 calls back to back: effective FP32 TFLOP/s, the dominant
+    kernel's tensor throughput over its own datapath's peak (the mode's
+    products per FP32 product; TF32 against half the BF16 peak), and the
+    relative error on 4096 sampled outputs against an FP64 product of the
+    same operands."""
+    import torch
+    from fp32_emulated_gemm_split_gb300 import workloads as W
+    p_bf16 = float(peaks["bf16_tflops"])
+    g = W.WORKLOADS["square8192_normal"]
+    A, B, _ = device_operands(g)
+    C = torch.empty((g.M, g.N), device="cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(77)
+    mi = torch.randint(0, g.M, (4096,), generator=gen, device="cuda")
+    ni = torch.randint(0, g.N, (4096,), generator=gen, device="cuda")
+    ref = (A[mi].double() * B[:, ni].t().double()).sum(1)
+    res = {}
+    for mode, (products, tf32) in LADDER.items():
+        run = lambda: emu.emu_sgemm(A, B, C, mode=mode, stream=stream)
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        emu.emu_profile_enable(True)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(reps):
+            run()
+        e.record(stream)
+        torch.cuda.synchronize()
+        n, ms = emu.emu_profile_read("gemm_tc")
+        emu.emu_profile_enable(False)
+        step = s.elapsed_time(e) / reps
+        k_ms = ms / max(n, 1)
+        peak = p_bf16 / 2.0 if tf32 else p_bf16
+        got = C[mi, ni].double()
+        res[mode] = {
+            "value": round(g.flops / (step * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms": round(step, 4), "kernel_ms": round(k_ms, 4),
+            "kernel_frac": round(products * g.flops / (k_ms * 1e-3) / 1e12 / peak, 4),
+            "rel_error": float(f"{float((got - ref).norm() / ref.norm()):.3e}"),
+        }
+    res["_how"] = ("square8192_normal operands drawn on the GPU; 10 calls back to back; "
+                   "kernel_frac: products x 2MNK / kernel time / peak "
+                   f"({peak_src} BF16 burst; TF32 modes: half of it); rel_error: relative "
+                   "Frobenius error on 4096 sampled outputs against FP64")
+    del A, B, C
+    torch.cuda.empty_cache()
+    return res
+
+
 def pick_workload(W, args):
     """The named workload, optionally with another mode or another M,N,K
     (same value distribution) for small profiling runs."""
@@ -627,7 +687,7 @@ def main(argv=None):
     ap.add_argument("--no-simt", action="store_true", help="skip the SIMT FP32 context number")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-configs", action="store_true",
-                    help="skip the timing of the other configurations")
+                    help="skip the timing of the other configurations and of the accuracy ladder")
     ap.add_argument("--shape", default=None, help="M,N,K override (same distribution)")
     ap.add_argument("--path", default=None, choices=[None, "auto", "twopass", "fused", "fused_tmem"],
                     help="implementation of the tensor-core modes (default: the library's)")
