@@ -649,9 +649,9 @@ emu_status_t emu_sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K, 
 // the first lands soon after B, the middle ones make fewer and fuller
 // launches, and the last one's copy back is the tail that nothing overlaps
 // (measured at 8192^3: 1.8-2.3 % faster than equal chunks).  Otherwise B
-// crosses first, whole, and the first chunk splits it.  Row chunks of C are independent, so the result is what one
-// call computes (up to the last wave's K split, which follows the tile
-// count of each launch).
+// crosses first, whole, and the first chunk splits it.  Row chunks of C are
+// independent, so the result is what one call computes (up to the last
+// wave's K split, which follows the tile count of each launch).
 constexpr int64_t kHostPanelCols = 1024;    // op(B) columns per panel
 constexpr int64_t kHostPanelRows = 2048;    // rows of the first chunk with panels
 constexpr int64_t kHostChunkBytes = int64_t(48) << 20;   // op(A) and C bytes per later chunk
@@ -678,8 +678,9 @@ emu_status_t host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_
     int64_t pw = kHostPanelCols;
     if (panels && (N + pw - 1) / pw > 64) pw = ((N + 63) / 64 + 255) / 256 * 256;
 
-    // row chunks: whole 256-row tiles, about 64 MB of op(A) each; with panels
-    // the first chunk is kHostPanelRows rows and the rest are cut the same way
+    // row chunks of whole 256-row tiles (at most kHostChunksMax): with panels
+    // the first is kHostPanelRows rows; the rest about kHostChunkBytes of
+    // op(A) and C each, or growing then shrinking after panels
     const int64_t row_bytes = (transA ? 1 : lda) * 4 * (transA ? K : 1) + N * 4;
     int64_t bounds[kHostChunksMax + 1];
     int nch = 0;
