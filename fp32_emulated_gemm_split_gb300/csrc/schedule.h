@@ -106,18 +106,25 @@ EMU_HD Unit sched_unit(const TileSchedule& s, int c, int i) {
 // The tail of a GEMM of `tiles` tiles of num_kb K blocks on `resident`
 // clusters.  None when the tiles fill whole rounds.  Otherwise the r =
 // tiles % resident tiles of the last round are shared by Ct clusters, the
-// cheaper of two ways by a cost in half K blocks, where handing one part's
-// sums to the owner (one FP32 slot written, then read) costs fix2 half
-// blocks (it depends on how long a K block of the mode takes):
-//   * aligned: Ct = s r, s = min(resident / r, 8, num_kb / 2) >= 2: every
+// cheapest plan by a cost in half K blocks.  Handing one part's sums to the
+// owner (one FP32 slot written, then read) costs fix2 half blocks (it
+// depends on how long a K block of the mode takes; measured with up to 8
+// parts per tile).  An owner reads its parts one after another, so each
+// part past the 8th adds rd = (fix2 + 2) / 3 half blocks (reading a slot is
+// about a third of the hand-over: 1.5 of 5.5 us for a 256-wide tile).
+//   * aligned: Ct = s r, 2 <= s <= min(resident / r, num_kb / 2): every
 //     range lies inside one tile, each cluster makes one hand-over:
-//     cost 2 ceil(num_kb / s) + fix2;
-//   * stream-K: Ct = min(resident, r num_kb / 2, 8 r): ranges of two K
+//     cost 2 ceil(num_kb / s) + fix2 + max(s - 8, 0) rd;
+//   * stream-K: 2 <= Ct <= min(resident, r num_kb / 2): ranges of two K
 //     blocks or more that may cross tiles, so a cluster can both publish
-//     (its first part) and own (its last): cost 2 ceil(W / Ct) + 2 fix2,
+//     (its first part) and own (its last), and a tile has up to ceil(Ct / r)
+//     parts: cost 2 ceil(W / Ct) + 2 fix2 + max(ceil(Ct / r) - 8, 0) rd,
 //     W = r num_kb.
-// The tail is split only when the cheaper cost beats the unsplit round
-// (2 num_kb) by at least a whole K block.
+// Every s and Ct is tried, the larger first (a tie keeps the wider split;
+// up to 8 parts a tile the costs fall as s and Ct grow).  The tail is split
+// only when the cheapest cost beats the unsplit round (2 num_kb) by at least
+// a whole K block.  A few deep tiles (a weight gradient: 256 x 256 with K in
+// the millions) are then spread over every resident cluster.
 EMU_HD void sched_plan_tail(int tiles, int num_kb, int resident, int fix2, int* tail_tiles,
                             int* tail_clusters) {
     *tail_tiles = 0;
@@ -126,23 +133,25 @@ EMU_HD void sched_plan_tail(int tiles, int num_kb, int resident, int fix2, int* 
     const int r = tiles % resident;
     if (r == 0) return;
     const int64_t W = static_cast<int64_t>(r) * num_kb;
+    const int64_t rd = (fix2 + 2) / 3;
     int64_t best = 2 * static_cast<int64_t>(num_kb) - 1;    // a cost must be below this
     int64_t best_ct = 0;
-    int s = resident / r;
-    if (s > 8) s = 8;
-    if (s > num_kb / 2) s = num_kb / 2;
-    if (s >= 2) {
-        const int64_t cost = 2 * ((num_kb + s - 1) / s) + fix2;
+    int smax = resident / r;
+    if (smax > num_kb / 2) smax = num_kb / 2;
+    for (int s = smax; s >= 2; --s) {
+        const int64_t cost = 2 * ((num_kb + s - 1) / s) + fix2 + (s > 8 ? s - 8 : 0) * rd;
         if (cost < best) {
             best = cost;
             best_ct = static_cast<int64_t>(s) * r;
         }
     }
-    int64_t ct = resident;
-    if (ct > W / 2) ct = W / 2;
-    if (ct > 8 * static_cast<int64_t>(r)) ct = 8 * static_cast<int64_t>(r);
-    if (ct >= 2 && ct != best_ct) {
-        const int64_t cost = 2 * ((W + ct - 1) / ct) + 2 * static_cast<int64_t>(fix2);
+    int64_t cmax = resident;
+    if (cmax > W / 2) cmax = W / 2;
+    for (int64_t ct = cmax; ct >= 2; --ct) {
+        if (ct % r == 0 && ct / r <= smax) continue;        // the aligned plan above
+        const int64_t parts = (ct + r - 1) / r;
+        const int64_t cost = 2 * ((W + ct - 1) / ct) + 2 * static_cast<int64_t>(fix2) +
+                             (parts > 8 ? parts - 8 : 0) * rd;
         if (cost < best) {
             best = cost;
             best_ct = ct;

@@ -472,9 +472,9 @@ def test_subnormal_operands_through_the_tensor_core(emu, mode):
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("mode", ["bf16x9", "tf32x3", "bf16x3"])
 def test_tail_split_shapes(emu, shape, mode):
-    """Shapes whose last round of tiles runs stream-K (its K blocks shared by
-    many clusters in consecutive ranges: 1 tile over 16 clusters, 16 tiles
-    over 76, 6 tiles over 48, the last 28 of 256 tiles over 76): within the
+    """Shapes whose last round of tiles runs split along K (its K blocks
+    shared by several clusters: 1 tile in 13 parts, 16 tiles over 76, 6
+    tiles over 48, the last 28 of 256 tiles over 76): within the
     bound, every element where the oracle is fast enough, and the same bits
     on a second call (the reduction order is fixed)."""
     M, N, K = shape
@@ -496,7 +496,7 @@ def test_tail_split_shapes(emu, shape, mode):
 @pytest.mark.parametrize("shape,transB,path", [
     ((1536, 512, 700), True, "twopass"),      # BF16x9: 12 tiles of 11 blocks, 5 parts each
     ((4864, 512, 700), False, "twopass"),     # 38 tiles of 11 blocks, 2 parts each
-    ((300, 384, 4100), True, "auto"),         # 4 tiles of 65 blocks (last one ragged), 8 parts
+    ((300, 384, 4100), True, "auto"),         # 4 tiles of 65 blocks (last one ragged), 13 parts
     ((12288, 256, 1024), False, "twopass"),   # 48 tiles of 16 blocks, stream-K over 76
     ((12288, 256, 4096), True, "twopass"),    # 48 tiles of 64 blocks, stream-K in every mode
     ((12288, 256, 1024), False, "fused_tmem"),  # 96 tiles: 20 left over, 3 parts each
@@ -665,3 +665,35 @@ def test_on_chip_split_does_not_read_past_k(emu, path, mode, K):
     mi, ni = W.sample_pairs(M, N, 2048, seed=K)
     Cref, Sabs = oracle.gemm_ref(A, B, transB=True, pairs=(mi, ni))
     assert checks.error_ratio(got[mi, ni], Cref, Sabs, K, 1.0, 0.0, mode=_bound_mode(mode)) <= 1.0
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 1105920, 1), (256, 256, 100000, 0),
+                                   (512, 256, 65536, 1), (300, 200, 50000, 0)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_deep_k_tiles_spread_over_every_cluster(emu, shape, mode):
+    """Weight-gradient shapes (dW = dY^T X over 1.1M rows is one 256 x 256
+    tile of 17,280 K blocks): the few tiles are cut into many more than 8
+    parts, every resident cluster takes some, and each tile's owner adds all
+    of its parts in K order -- within the bound against the oracle on
+    sampled outputs, with alpha and beta, and the same bits on a second
+    call."""
+    import torch
+    M, N, K, tA = shape
+    r = W.rng(M + N + K)
+    A = W.normal(r, (K, M) if tA else (M, K))
+    B = W.normal(r, (K, N), std=K ** -0.5)
+    C0 = W.uniform(r, (M, N))
+    dA, dB = to_dev(A), to_dev(B)
+    outs = []
+    for _ in range(2):
+        C = to_dev(C0)
+        emu.emu_sgemm(dA, dB, C, transA=bool(tA), alpha=0.75, beta=0.5, mode=mode)
+        torch.cuda.synchronize()
+        outs.append(C.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+    assert emu.emu_get_last_device_error() == 0
+    mi, ni = W.sample_pairs(M, N, 768, seed=K)
+    Cref, Sabs = oracle.gemm_ref(A, B, tA, False, 0.75, 0.5, C0, pairs=(mi, ni))
+    assert checks.error_ratio(outs[0][mi, ni], Cref, Sabs, K, 0.75, 0.5, C0[mi, ni],
+                              mode=_bound_mode(mode)) <= 1.0

@@ -9,6 +9,8 @@ cluster counts:
 * the tail takes only the last, partial round of tiles, on at most the
   resident clusters: either each tile in equal parts inside it (a multiple
   of the tile count) or stream-K ranges of two K blocks or more on average;
+  a few deep tiles (weight-gradient shapes, K blocks in the thousands) are
+  spread over more than 8 clusters each;
 * a cluster leaves sums in at most one slot (its own), that unit is the first
   of its tail range, and it waits on nothing before it;
 * the owner of a split tile is the last unit of its range, and the parts it
@@ -32,6 +34,9 @@ TILES = [1, 2, 3, 5, 16, 28, 36, 47, 48, 75, 76, 77, 96, 100, 151, 152, 153, 192
 KBS = [1, 2, 3, 4, 5, 8, 16, 17, 63, 64, 128, 256]
 RESIDENT = [1, 2, 37, 64, 74, 76]
 FIX2 = [0, 3, 8, 15]          # hand-over cost in half K blocks
+# few tiles with many K blocks: 256 x 256 weight gradients over 65K-1.1M rows
+DEEP_TILES = [1, 2, 3, 5, 9, 77]
+DEEP_KBS = [1024, 4096, 17280]
 
 
 @pytest.fixture(scope="module")
@@ -41,6 +46,8 @@ def dump(tmp_path_factory):
                     os.path.join(HERE, "sched_dump.cpp"), "-o", exe],
                    check=True, capture_output=True, text=True)
     cases = [(t, k, r, f) for t in TILES for k in KBS for r in RESIDENT for f in FIX2]
+    cases += [(t, k, r, f) for t in DEEP_TILES for k in DEEP_KBS for r in (2, 74, 76)
+              for f in FIX2]
     out = subprocess.run([exe], input="".join(f"{t} {k} {r} {f}\n" for t, k, r, f in cases),
                          check=True, capture_output=True, text=True, timeout=300).stdout
     plans = {}
@@ -66,7 +73,7 @@ def test_plan_takes_only_the_last_round(dump):
             assert tc == 0 and g == min(tiles, res)
             continue
         assert tt == tiles % res
-        assert 2 <= tc <= res and tc <= 8 * tt
+        assert 2 <= tc <= res
         assert tc % tt == 0 or tc <= tt * kb // 2
         assert g == (res if tiles > tt else tc)
 
@@ -159,3 +166,17 @@ def test_known_plans(dump):
     assert plan(4320, 4) == (0, 0)
     assert dump[(96, 16, 76, 3)]["tail_clusters"] == 60
     assert dump[(96, 16, 76, 3)]["grid"] == 76
+
+
+def test_deep_tiles_spread_over_every_cluster(dump):
+    """A 256 x 256 weight gradient over 1.1M rows is one tile of 17280 K
+    blocks: it takes every resident cluster (cost 2*228 + 3 + 68 = 527 half
+    blocks against 2*2160 + 3 = 4323 for 8 parts), 227-228 blocks each; a
+    tile of 128 blocks takes 16 (2*8 + 3 + 8 = 27 against 35 for 8)."""
+    p = dump[(1, 17280, 76, 3)]
+    assert (p["tail_tiles"], p["tail_clusters"], p["grid"]) == (1, 76, 76)
+    work = [sum(u[3] - u[2] for u in us) for us in p["units"].values()]
+    assert max(work) - min(work) <= 1 and max(work) == 228
+    assert dump[(1, 128, 76, 3)]["tail_clusters"] == 16
+    for t in DEEP_TILES[:-1]:
+        assert dump[(t, 17280, 76, 3)]["tail_clusters"] >= 75
