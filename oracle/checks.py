@@ -30,12 +30,17 @@ FROBENIUS_TOL = 2e-6
 
 
 # Representation error of the cheaper modes, per product, relative to |a||b|.
-# Two BF16 pieces leave |x - x0 - 2^-8 x1| <= 2^-18 |x|, so the kept products
-# miss at most about 2 * 2^-18 and the dropped 2^-16 a1 b1 adds at most about
-# 2^-18 more: below 2^-16 in all.  One TF32 piece leaves |x - hi| <= 2^-11 |x|,
-# so the product misses at most 2 * 2^-11 + 2^-22 < 2^-10 + 2^-21.
+# Two BF16 pieces (8 significant bits each, unit roundoff 2^-8): |x - x0| <=
+# 2^-8 |x| and |x1| <= (1 + 2^-8) |x|; the second rounding, of 2^8 (x - x0)
+# (at most |x| in magnitude, so a half ulp is at most 2^-9 |x| there), leaves
+# |x - x0 - 2^-8 x1| <= 2^-17 |x|.  With a^ = a0 + 2^-8 a1 and r_a = a - a^,
+# ab minus the kept products a0 b0 + 2^-8 (a0 b1 + a1 b0) is 2^-16 a1 b1 +
+# a^ r_b + r_a b^ + r_a r_b, at most (2^-16 (1 + 2^-8)^2 + 2 * 2^-17 (1 +
+# 2^-17) + 2^-34) |a||b| < 2^-15 + 2^-22 (random pairs reach 2^-15.1).  One
+# TF32 piece leaves |x - hi| <= 2^-11 |x|, so the product misses at most
+# 2 * 2^-11 + 2^-22 < 2^-10 + 2^-21.
 MODE_EXTRA = {"bf16x9": 0.0, "tf32x3": 2.0 ** -20, "tf32x3_oy": 2.0 ** -20,
-              "bf16x3": 2.0 ** -16, "tf32": 2.0 ** -10 + 2.0 ** -21}
+              "bf16x3": 2.0 ** -15 + 2.0 ** -22, "tf32": 2.0 ** -10 + 2.0 ** -21}
 
 
 def elementwise_bound(K, alpha, beta, Sabs, C0=None, mode="bf16x9"):

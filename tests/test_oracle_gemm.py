@@ -378,6 +378,27 @@ def test_cheaper_rungs_within_their_bounds_and_ordered(mode, fn):
     assert e > checks.FROBENIUS_TOL       # misses the criterion BF16x9 and TF32x3 meet
 
 
+def test_bf16x3_piece_error_matches_its_bound():
+    """The two-piece representation error, measured on the oracle's own
+    split over 2^20 normal values: |x - x0 - 2^-8 x1| reaches 2^-17 |x| (not
+    less: 2^-18 would be too small) and never exceeds it; the kept products
+    of random pairs miss by more than 2^-16 |a||b| and never by more than
+    the rung's allowance, 2^-15 + 2^-22."""
+    r = R(85)
+    x = W.normal(r, (1, 1 << 20))
+    p0, p1, _ = oracle.split_bf16x3(x)
+    f = lambda p: (p.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    x0, x1 = f(p0)[0], f(p1)[0]
+    xd = x[0].astype(np.float64)
+    rel = np.abs(xd - x0 - 2.0 ** -8 * x1) / np.abs(xd)
+    assert 2.0 ** -18 < rel.max() <= 2.0 ** -17
+    h = xd.size // 2
+    a, b = xd[:h], xd[h:]
+    kept = x0[:h] * x0[h:] + 2.0 ** -8 * (x0[:h] * x1[h:] + x1[:h] * x0[h:])
+    err = np.abs(a * b - kept) / np.abs(a * b)
+    assert 2.0 ** -16 < err.max() <= checks.MODE_EXTRA["bf16x3"]
+
+
 def test_bf16x3_exact_on_16_bit_integers():
     r = R(84)
     A = r.integers(-(1 << 15), 1 << 15, (8, 8)).astype(np.float32)   # 16 significant bits
