@@ -7,7 +7,8 @@ on B split once, emu_sgemm_host on host buffers, emu_sgemm_noalloc where its
 64 MiB array holds the pieces).  The result must meet the mode's element-wise
 bound against the oracle's FP64 product on sampled outputs (every corner and
 tile edge included), every output must be finite, and the padding columns of
-C must keep the values they had: the kernels write nothing outside C.
+C and 33 rows below it must keep the values they had: the kernels write
+nothing outside C.
 
 Bound: "Limitations and decision criteria" of the NVIDIA blog post (BF16x9
 matches FP32 accuracy); the cheaper rungs by their piece error (oracle.checks).
@@ -28,6 +29,7 @@ ENTRIES = ["sgemm", "bsplit", "host", "noalloc"]
 PIECE_BYTES = {"bf16x9": 6, "tf32x3": 8, "tf32x3_oy": 8, "bf16x3": 4, "tf32": 4, "fp32_simt": 0}
 NCASES = 48
 SENTINEL = 7.25
+ROWS_BELOW = 33         # sentinel rows under C: more than one 32-row store box
 
 
 @pytest.fixture(scope="module")
@@ -89,9 +91,9 @@ def test_random_gemm(emu, i):
             dA = _padded(torch, A, c["pads"][0], c["offs"][0])
             dB = _padded(torch, B, c["pads"][1], c["offs"][1])
             oc = c["offs"][2]
-            Cs = torch.full((M, N + c["pads"][2] + oc), SENTINEL, device="cuda")
-            Cs[:, oc:oc + N] = torch.from_numpy(C0).cuda()
-            dC = Cs[:, oc:oc + N]
+            Cs = torch.full((M + ROWS_BELOW, N + c["pads"][2] + oc), SENTINEL, device="cuda")
+            Cs[:M, oc:oc + N] = torch.from_numpy(C0).cuda()
+            dC = Cs[:M, oc:oc + N]
             kw = dict(alpha=c["alpha"], beta=c["beta"], mode=c["mode"])
             if c["entry"] == "bsplit":
                 P = emu.emu_split_b(dB, transB=bool(tB), mode=c["mode"])
@@ -102,9 +104,10 @@ def test_random_gemm(emu, i):
                 emu.emu_sgemm(dA, dB, dC, transA=bool(tA), transB=bool(tB), **kw)
             torch.cuda.synchronize()
             full = Cs.cpu().numpy()
-            C = np.ascontiguousarray(full[:, oc:oc + N])
-            pad_ok = bool(np.all(full[:, :oc] == np.float32(SENTINEL)) and
-                          np.all(full[:, oc + N:] == np.float32(SENTINEL)))
+            C = np.ascontiguousarray(full[:M, oc:oc + N])
+            pad_ok = bool(np.all(full[:M, :oc] == np.float32(SENTINEL)) and
+                          np.all(full[:M, oc + N:] == np.float32(SENTINEL)) and
+                          np.all(full[M:] == np.float32(SENTINEL)))
     finally:
         emu.emu_set_path(old)
     assert pad_ok, f"case {i}: C written outside its {N} columns ({c})"
@@ -162,9 +165,9 @@ def test_random_gemm_on_chip_shapes(emu, i):
         dA = _padded(torch, A, c["pads"][0], c["offs"][0])
         dB = _padded(torch, B, c["pads"][1], c["offs"][1])
         oc = c["offs"][2]
-        Cs = torch.full((M, N + c["pads"][2] + oc), SENTINEL, device="cuda")
-        Cs[:, oc:oc + N] = torch.from_numpy(C0).cuda()
-        dC = Cs[:, oc:oc + N]
+        Cs = torch.full((M + ROWS_BELOW, N + c["pads"][2] + oc), SENTINEL, device="cuda")
+        Cs[:M, oc:oc + N] = torch.from_numpy(C0).cuda()
+        dC = Cs[:M, oc:oc + N]
         kw = dict(alpha=c["alpha"], beta=c["beta"], mode=c["mode"])
         if c["entry"] == "bsplit":
             P = emu.emu_split_b(dB, transB=bool(tB), mode=c["mode"])
@@ -175,9 +178,10 @@ def test_random_gemm_on_chip_shapes(emu, i):
         full = Cs.cpu().numpy()
     finally:
         emu.emu_set_path(old)
-    assert np.all(full[:, :oc] == np.float32(SENTINEL)), f"case {i} ({c})"
-    assert np.all(full[:, oc + N:] == np.float32(SENTINEL)), f"case {i} ({c})"
-    _check(c, i, A, B, C0, np.ascontiguousarray(full[:, oc:oc + N]))
+    assert np.all(full[:M, :oc] == np.float32(SENTINEL)), f"case {i} ({c})"
+    assert np.all(full[:M, oc + N:] == np.float32(SENTINEL)), f"case {i} ({c})"
+    assert np.all(full[M:] == np.float32(SENTINEL)), f"case {i}: rows past M written ({c})"
+    _check(c, i, A, B, C0, np.ascontiguousarray(full[:M, oc:oc + N]))
 
 
 def test_no_device_error_after_fuzz(emu):
