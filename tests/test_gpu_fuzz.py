@@ -74,12 +74,29 @@ def _padded(torch, X, pad, off=0):
 
 @pytest.mark.parametrize("i", range(NCASES))
 def test_random_gemm(emu, i):
+    _random_gemm(emu, i, _draw, "normal")
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_gemm_wide_exponents(emu, i):
+    """The same draws with the stress distribution in A, B and C0: exponents
+    over 2^-30..2^30, 1 % zeros and 0.1 % FP32 subnormals, so that products
+    span 2^120 and some fall among the subnormals."""
+    _random_gemm(emu, 500 + i, _draw, "stress")
+
+
+def _random_gemm(emu, i, draw, dist):
     import torch
-    c, r = _draw(i)
+    c, r = draw(i)
     M, N, K, tA, tB = c["M"], c["N"], c["K"], c["tA"], c["tB"]
-    A = W.normal(r, (K, M) if tA else (M, K))
-    B = W.normal(r, (N, K) if tB else (K, N), std=max(K, 1) ** -0.5)
-    C0 = W.normal(r, (M, N))
+    if dist == "stress":
+        A = W.stress(r, (K, M) if tA else (M, K))
+        B = W.stress(r, (N, K) if tB else (K, N))
+        C0 = W.stress(r, (M, N))
+    else:
+        A = W.normal(r, (K, M) if tA else (M, K))
+        B = W.normal(r, (N, K) if tB else (K, N), std=max(K, 1) ** -0.5)
+        C0 = W.normal(r, (M, N))
     old = emu.emu_get_path()
     emu.emu_set_path(c["path"])
     try:
