@@ -104,6 +104,21 @@ cudaError_t launch_timeout_probe(int* err, uint64_t limit_ns, cudaStream_t strea
 // PERFORMANT strategy (chooser.cu): the mode that runs for a requested mode
 // (the FP32 SIMT kernel where it is predicted faster), and the two time
 // estimates in microseconds; sms is the device's SM count.
+// What handing one part's sums to the tile's owner costs, in half K blocks
+// of the mode (the split tail's planner, schedule.h, and the time model of
+// the PERFORMANT strategy use it): writing and reading a slot takes about 4
+// us for 256-wide tiles (2 us for 128-wide ones, whose K blocks also take half
+// as long), against measured K blocks of 2.7 us (BF16x9), 1.1 us (TF32x3, its
+// Ootomo-Yokota variant and BF16x3) and 0.53 us (single-pass TF32).
+inline int handover_half_blocks(int mode) {
+    switch (mode) {
+        case kModeBf16x9: return 3;
+        case kModeTf32x3:
+        case kModeTf32x3Oy: return 8;
+        case kModeBf16x3: return 7;
+        default: return 15;
+    }
+}
 int choose_mode(int64_t M, int64_t N, int64_t K, int mode, int performant, int sms);
 double predict_tc_us(int64_t M, int64_t N, int64_t K, int mode, int sms);
 double predict_simt_us(int64_t M, int64_t N, int64_t K, int sms);

@@ -235,21 +235,6 @@ bool make_c_map(CUtensorMap* map, float* C, int64_t M, int64_t N, int64_t ldc) {
 // sharing the tail.  Sets p.tail_*, p.part_ws, p.flags and p.epoch.
 constexpr int kFlagsBytes = 64 << 10;
 
-// What handing one part's sums to the tile's owner costs, in half K blocks
-// of the mode: writing and reading a slot takes about 4 us for 256-wide
-// tiles (2 us for 128-wide ones, whose K blocks also take half as long),
-// against measured K blocks of 2.7 us (BF16x9), 1.1 us (TF32x3, its
-// Ootomo-Yokota variant and BF16x3) and 0.53 us (single-pass TF32).
-int handover_half_blocks(int mode) {
-    switch (mode) {
-        case kModeBf16x9: return 3;
-        case kModeTf32x3:
-        case kModeTf32x3Oy: return 8;
-        case kModeBf16x3: return 7;
-        default: return 15;
-    }
-}
-
 emu_status_t plan_tail(TcGemmParams& p, int mode, int bm, int bn, int fused, DeviceState* d) {
     const int tiles = p.tiles_m * p.tiles_n;
     const int clusters = gemm_kblock_clusters(mode, bn, fused, d->sms);
