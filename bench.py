@@ -253,6 +253,7 @@ def bench_gpu(args):
             torch.cuda.empty_cache()
             out["configs"] = bench_configs(emu, stream, peaks, peak_src)
             out["ladder"] = bench_ladder(emu, stream, peaks, peak_src)
+            out["weight_gradients"] = bench_weight_gradients(emu, stream, peaks, peak_src)
             dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
             dC = torch.from_numpy(C0).cuda() if C0 is not None else torch.empty((g.M, g.N), device="cuda")
         if not args.no_e2e:
@@ -509,6 +510,53 @@ def bench_ladder(emu, stream, peaks, peak_src, reps=10):
     return res
 
 
+def bench_weight_gradients(emu, stream, peaks, peak_src, reps=5):
+    """The weight gradients of the 17,280-atom MLIP layers, dW = dY^T X over
+    their 1,105,920 rows (what EmuLinear's backward computes): M x N x K =
+    256 x 256 x 1105920 and 1024 x 256 x 1105920, op(A) = dY^T (transA),
+    BF16x9, operands drawn on the GPU, `reps` calls back to back.  A few
+    output tiles with K blocks in the thousands: the GEMM's tail spreads
+    them over every SM pair."""
+    import torch
+    p_bf16 = float(peaks["bf16_tflops"])
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2024)
+    res = {}
+    for (M, N, K) in [(256, 256, 1105920), (1024, 256, 1105920)]:
+        dY = torch.randn((K, M), generator=gen, device="cuda")
+        X = torch.randn((K, N), generator=gen, device="cuda").mul_(K ** -0.5)
+        C = torch.empty((M, N), device="cuda")
+        run = lambda: emu.emu_sgemm(dY, X, C, transA=True, stream=stream)
+        for _ in range(2):
+            run()
+        torch.cuda.synchronize()
+        emu.emu_profile_enable(True)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(reps):
+            run()
+        e.record(stream)
+        torch.cuda.synchronize()
+        n, ms = emu.emu_profile_read("gemm_tc")
+        ns, mss = emu.emu_profile_read("split")
+        emu.emu_profile_enable(False)
+        step = s.elapsed_time(e) / reps
+        flops = 2.0 * M * N * K
+        k_ms = ms / max(n, 1)
+        res[f"{M}x{N}x{K}"] = {
+            "value": round(flops / (step * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms": round(step, 4), "kernel_ms": round(k_ms, 4),
+            "kernel_frac": round(9 * flops / (k_ms * 1e-3) / 1e12 / p_bf16, 4),
+            "split_ms": round(mss / reps, 4),
+        }
+        del dY, X, C
+        torch.cuda.empty_cache()
+    res["_how"] = ("dW = dY^T X of the 1.1M-row MLIP layers (transA), BF16x9, operands drawn "
+                   "on the GPU, 5 calls back to back; kernel_frac: 18MNK / GEMM time / "
+                   f"{peak_src} BF16 burst peak; split_ms: both operands' (transposed) splits")
+    return res
+
+
 def pick_workload(W, args):
     """The named workload, optionally with another mode or another M,N,K
     (same value distribution) for small profiling runs."""
@@ -687,7 +735,8 @@ def main(argv=None):
     ap.add_argument("--no-simt", action="store_true", help="skip the SIMT FP32 context number")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-configs", action="store_true",
-                    help="skip the timing of the other configurations and of the accuracy ladder")
+                    help="skip the timing of the other configurations, the accuracy ladder "
+                         "and the weight gradients")
     ap.add_argument("--shape", default=None, help="M,N,K override (same distribution)")
     ap.add_argument("--path", default=None, choices=[None, "auto", "twopass", "fused", "fused_tmem"],
                     help="implementation of the tensor-core modes (default: the library's)")
