@@ -17,6 +17,9 @@ criteria below make that concrete:
   product, so its bound adds 2^-20 |alpha| S_abs.  The cheaper rungs (two
   BF16 pieces, single-pass TF32) add their own representation error
   (MODE_EXTRA).
+* below FP32's normal range the pieces of the split rungs are rounded to
+  their format's subnormal quantum, an absolute error per operand
+  (MODE_SUB_ABS); callers that pass S1 = sum_k |a_mk| + |b_kn| get it added.
 * relative Frobenius error ||C - C_ref||_F / ||C_ref||_F <= 2e-6 on
   normally distributed inputs.
 """
@@ -43,18 +46,47 @@ MODE_EXTRA = {"bf16x9": 0.0, "tf32x3": 2.0 ** -20, "tf32x3_oy": 2.0 ** -20,
               "bf16x3": 2.0 ** -15 + 2.0 ** -22, "tf32": 2.0 ** -10 + 2.0 ** -21}
 
 
-def elementwise_bound(K, alpha, beta, Sabs, C0=None, mode="bf16x9"):
+# Below FP32's normal range (2^-126) a piece is rounded with its format's
+# subnormal quantum: TF32 keeps the top 10 of FP32's 23 mantissa bits
+# (quantum 2^-136), BF16 the top 7 (2^-133).  So the pieces leave an absolute
+# error per operand on top of the relative one: TF32x3 and single-pass TF32 up
+# to 2^-137 (the last piece's half quantum), the Ootomo-Yokota split 2^-148
+# (its residual is scaled by 2^11 before rounding), two BF16 pieces 2^-142
+# (the second piece is scaled by 2^-8), BF16x9 nothing (its third piece
+# reaches 2^-149, FP32's own quantum).  A product a b then misses by up to
+# E (|a| + |b|) more, and a sum by E S1 with S1 = sum_k |a_mk| + |b_kn|.
+MODE_SUB_ABS = {"bf16x9": 0.0, "tf32x3": 2.0 ** -137, "tf32x3_oy": 2.0 ** -148,
+                "bf16x3": 2.0 ** -142, "tf32": 2.0 ** -137}
+
+
+def operand_l1(A, B, transA=False, transB=False, pairs=None):
+    """S1 = sum_k |op(A)[m, k]| + |op(B)[k, n]| (FP64), at `pairs` or for all
+    outputs: the weight of MODE_SUB_ABS in the bound."""
+    a = np.abs(np.asarray(A, np.float64))
+    b = np.abs(np.asarray(B, np.float64))
+    ra = a.sum(axis=0) if transA else a.sum(axis=1)          # per row of op(A)
+    cb = b.sum(axis=1) if transB else b.sum(axis=0)          # per column of op(B)
+    if pairs is None:
+        return ra[:, None] + cb[None, :]
+    return ra[pairs[0]] + cb[pairs[1]]
+
+
+def elementwise_bound(K, alpha, beta, Sabs, C0=None, mode="bf16x9", S1=None):
     base = (2 * K + 2) * U + MODE_EXTRA[mode]
     b = base * abs(float(alpha)) * np.asarray(Sabs, np.float64)
     if beta != 0.0:
         b = b + 2 * U * abs(float(beta)) * np.abs(np.asarray(C0, np.float64))
+    if S1 is not None and MODE_SUB_ABS[mode] > 0.0:
+        b = b + MODE_SUB_ABS[mode] * (1 + 2.0 ** -10) * abs(float(alpha)) * np.asarray(S1, np.float64)
     return b + (9 * K + 4) * SUB
 
 
-def error_ratio(C, Cref, Sabs, K, alpha, beta, C0=None, mode="bf16x9"):
-    """max |C - C_ref| / bound; the result passes when this is <= 1."""
+def error_ratio(C, Cref, Sabs, K, alpha, beta, C0=None, mode="bf16x9", S1=None):
+    """max |C - C_ref| / bound; the result passes when this is <= 1.  With
+    operands that reach FP32's subnormals, pass S1 (operand_l1) so that the
+    split rungs' absolute error there is allowed for."""
     err = np.abs(np.asarray(C, np.float64) - np.asarray(Cref, np.float64))
-    bound = elementwise_bound(K, alpha, beta, Sabs, C0, mode)
+    bound = elementwise_bound(K, alpha, beta, Sabs, C0, mode, S1)
     if err.size == 0:
         return 0.0
     return float(np.max(err / bound))

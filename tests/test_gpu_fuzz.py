@@ -145,8 +145,9 @@ def _check(c, i, A, B, C0, C):
     ni = np.concatenate([ni, np.tile(cols, rows.size)])
     Cref, Sabs = oracle.gemm_ref(A, B, tA, tB, c["alpha"], c["beta"], C0, pairs=(mi, ni))
     bmode = c["mode"] if c["mode"] in checks.MODE_EXTRA else "bf16x9"
+    S1 = checks.operand_l1(A, B, tA, tB, pairs=(mi, ni))     # for subnormal operands
     ratio = checks.error_ratio(C[mi, ni], Cref, Sabs, K, c["alpha"], c["beta"], C0[mi, ni],
-                               mode=bmode)
+                               mode=bmode, S1=S1)
     assert ratio <= 1.0, f"case {i}: error ratio {ratio} ({c})"
 
 

@@ -399,6 +399,59 @@ def test_bf16x3_piece_error_matches_its_bound():
     assert 2.0 ** -16 < err.max() <= checks.MODE_EXTRA["bf16x3"]
 
 
+def _subnormals_and_edge(r, n):
+    """FP32 subnormals (random mantissa, both signs) and normals just above
+    2^-126, whose residuals after the first piece are subnormal."""
+    sub = (r.integers(1, 1 << 23, n, dtype=np.uint32) |
+           (r.integers(0, 2, n, dtype=np.uint32) << 31)).view(np.float32)
+    edge = (np.ldexp(r.uniform(1.0, 2.0, n), r.integers(-126, -118, n)) *
+            np.where(r.random(n) < 0.5, -1.0, 1.0)).astype(np.float32)
+    return np.concatenate([sub, edge]).reshape(1, -1)
+
+
+def test_split_errors_below_the_normal_range_match_their_bounds():
+    """MODE_SUB_ABS, pinned on the oracle's own splits: over 2^17 FP32
+    subnormals and small normals the absolute representation error reaches
+    within a factor two of each rung's constant and never exceeds it; BF16x9
+    represents every one exactly (its third piece reaches 2^-149)."""
+    x = _subnormals_and_edge(R(86), 1 << 16)
+    xd = x[0].astype(np.float64)
+    f = lambda p: (p.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    p0, p1, p2 = oracle.split_bf16x3(x)
+    b0, b1, b2 = f(p0)[0], f(p1)[0], f(p2)[0]
+    hi, lo = oracle.split_tf32x2(x)
+    hs, ls = oracle.split_tf32x2s(x)
+    err = {
+        "bf16x9": np.abs(xd - b0 - 2.0 ** -8 * b1 - 2.0 ** -16 * b2),
+        "bf16x3": np.abs(xd - b0 - 2.0 ** -8 * b1),
+        "tf32x3": np.abs(xd - hi[0] - lo[0].astype(np.float64)),
+        "tf32": np.abs(xd - hi[0]),
+        "tf32x3_oy": np.abs(xd - hs[0] - 2.0 ** -11 * ls[0].astype(np.float64)),
+    }
+    assert err["bf16x9"].max() == 0.0
+    for mode in ("bf16x3", "tf32x3", "tf32", "tf32x3_oy"):
+        e = checks.MODE_SUB_ABS[mode]
+        # the relative part is allowed too: |x - x^| <= rho |x| + E
+        rho = {"bf16x3": 2.0 ** -17, "tf32x3": 2.0 ** -22, "tf32": 2.0 ** -11,
+               "tf32x3_oy": 2.0 ** -22}[mode]
+        assert np.all(err[mode] <= rho * np.abs(xd) + e), mode
+        assert err[mode][: 1 << 16].max() > e / 2, mode          # attained on subnormals
+
+
+def test_subnormal_operands_need_the_absolute_term():
+    """K = 1, a a subnormal that TF32 cannot hold to the last bit, b = 1.5 *
+    2^30: the oracle's TF32x3 product misses by about 2^-137 * 2^30, far
+    above the relative terms, and within them once the absolute term
+    (operand_l1) is added."""
+    a = np.array([[np.float32(np.uint32(0x00000FFF).view(np.float32))]])   # 4095 * 2^-149
+    b = np.array([[np.float32(1.5 * 2.0 ** 30)]], np.float32)
+    Cref, Sabs = oracle.gemm_ref(a, b)
+    C = oracle.gemm_tf32x3(a, b)
+    assert checks.error_ratio(C, Cref, Sabs, 1, 1.0, 0.0, mode="tf32x3") > 100
+    S1 = checks.operand_l1(a, b)
+    assert checks.error_ratio(C, Cref, Sabs, 1, 1.0, 0.0, mode="tf32x3", S1=S1) <= 1.0
+
+
 def test_bf16x3_exact_on_16_bit_integers():
     r = R(84)
     A = r.integers(-(1 << 15), 1 << 15, (8, 8)).astype(np.float32)   # 16 significant bits
