@@ -553,7 +553,8 @@ def bench_weight_gradients(emu, stream, peaks, peak_src, reps=5):
         torch.cuda.empty_cache()
     res["_how"] = ("dW = dY^T X of the 1.1M-row MLIP layers (transA), BF16x9, operands drawn "
                    "on the GPU, 5 calls back to back; kernel_frac: 18MNK / GEMM time / "
-                   f"{peak_src} BF16 burst peak; split_ms: both operands' (transposed) splits")
+                   f"{peak_src} BF16 burst peak; split_ms: both operands' splits (row-wise, "
+                   "into M- and N-major pieces: K is more than 4 times M and N)")
     return res
 
 

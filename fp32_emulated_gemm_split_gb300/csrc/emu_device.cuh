@@ -144,13 +144,33 @@ __device__ __forceinline__ uint64_t make_sw128_kmajor_desc(uint32_t smem_addr) {
     return d;
 }
 
+// The same for an M- or N-major operand (PTX ISA, tcgen05 shared memory
+// descriptor; canonical MN-major layout with 128-byte swizzle): a tensor
+// copy of a box of 64 elements (128 bytes, the contiguous M or N direction)
+// by 64 K rows puts K row r at byte 128 r, its 16-byte chunks swizzled by
+// r % 8, so the 8-row swizzle atoms of 1024 bytes follow each other along K
+// (stride byte offset 1024) and the next 64 elements of M or N are `lbo`
+// bytes further (leading byte offset: the next box).  One K = 16 step of a
+// BF16 MMA is 16 K rows: two atoms, 2048 bytes.
+__device__ __forceinline__ uint64_t make_sw128_mn_desc(uint32_t smem_addr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(lbo >> 4) << 16;           // LBO: next 64 elements of M or N
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;         // SBO: next 8 K rows
+    d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version
+    d |= static_cast<uint64_t>(2u) << 61;                 // 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor for a dense tcgen05.mma with FP32 accumulation and
 // both operands K-major: D format F32 (bits 4-5 = 1), A and B formats in bits
 // 7-9 and 10-12 (kind::f16: 1 = BF16; kind::tf32: 2 = TF32), N >> 3 in bits
-// 17-22, M >> 4 in bits 24-28.
+// 17-22, M >> 4 in bits 24-28.  Bit 15 (A) and bit 16 (B) ask for an M- or
+// N-major operand instead (kIdescAMn, kIdescBMn).
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t M, uint32_t N) {
     return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
+constexpr uint32_t kIdescAMn = 1u << 15, kIdescBMn = 1u << 16;
 
 // 32 lanes x 8 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
@@ -199,6 +219,17 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
                  :: "r"(cluster_addr) : "memory");
+}
+
+// The same over a 4-D map (M- or N-major pieces: element, K row, 64-element
+// chunk, piece).
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar_cluster) : "memory");
 }
 
 // Tensor copy into this CTA's shared memory whose completion is counted on

@@ -60,6 +60,14 @@ struct TcGemmParams {
     float* part_ws;
     unsigned* flags;
     unsigned epoch;
+    // Two-pass BF16 modes: the layout of each operand's pieces.  0: K-major
+    // (planes of op(A)'s rows, or op(B)^T's, along K: what the split writes
+    // from a matrix stored with K contiguous).  1: M-major (A) or N-major
+    // (B): planes of K rows of M or N elements, what a plain row-wise split
+    // writes from A stored K x M (transA) or B stored K x N; the tensor core
+    // reads them through the transpose bits of its instruction descriptor,
+    // so no transposed split is needed.
+    int a_mn, b_mn;
 };
 
 // Launchers (return the launch status; nothing is synchronised).

@@ -208,6 +208,33 @@ emu_status_t make_plane_map(CUtensorMap* map, const void* base, bool fp32, int64
     return r == CUDA_SUCCESS ? EMU_OK : EMU_ERR_CUDA;
 }
 
+// 4-D map over M- or N-major pieces: `planes` planes of K rows x ld
+// elements (ld a multiple of 64; planes plane_rows rows apart, 0: K), each
+// row seen as ceil(cols / 64) chunks of 64 elements: dimensions (element,
+// K row, chunk, piece).  A box of 64 elements x box_k rows x `chunks`
+// chunks lands in shared memory as the chunks one after another, each K
+// row 128 bytes (128-byte swizzle): the M- or N-major layout the tensor
+// core reads.  K rows past K and chunks past the last are zero-filled; the
+// elements of the last chunk past `cols` are read from the row's padding
+// and reach only outputs that are never stored.
+emu_status_t make_plane_map_mn(CUtensorMap* map, const void* base, int64_t cols, int64_t K,
+                               int64_t ld, int planes, int box_k, int chunks,
+                               int64_t plane_rows = 0) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return EMU_ERR_CUDA;
+    if (ld % 64 != 0) return EMU_ERR_INVALID_VALUE;
+    const int64_t prow = plane_rows > 0 ? plane_rows : K;
+    cuuint64_t dims[4] = {64, (cuuint64_t)K, (cuuint64_t)((cols + 63) / 64), (cuuint64_t)planes};
+    cuuint64_t strides[3] = {(cuuint64_t)(ld * 2), 128, (cuuint64_t)(prow * ld * 2)};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_k, (cuuint32_t)chunks, 1};
+    cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                     strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? EMU_OK : EMU_ERR_CUDA;
+}
+
 // 2-D map over C for the bulk tensor stores of the GEMM epilogue (any beta;
 // with beta != 0 the epilogue reads C itself first): box of 16 columns x 32
 // rows, 64-byte swizzle.  The map covers the first N & ~3 columns only: a
@@ -284,7 +311,9 @@ bool fits_mul_add(uint64_t a, uint64_t b, uint64_t c, size_t* out) {
 // is formed (M, N, K up to INT32_MAX would otherwise wrap a 64-bit size).
 bool workspace_fits(int64_t M, int64_t N, int64_t K) {
     size_t bytes = 0;
-    return fits_mul_add((uint64_t)M + (uint64_t)N, 12 * (uint64_t)plane_ld(K), 2048, &bytes);
+    // K-major pieces, and M- or N-major ones (K rows of M and N rounded up to 64)
+    return fits_mul_add((uint64_t)M + (uint64_t)N, 12 * (uint64_t)plane_ld(K), 2048, &bytes) &&
+           fits_mul_add((uint64_t)M + (uint64_t)N + 128, 12 * (uint64_t)K, 2048, &bytes);
 }
 
 emu_status_t check_gemm_args(int transA, int transB, int64_t M, int64_t N, int64_t K,
@@ -315,24 +344,70 @@ struct BPieces {
     int64_t ld = 0;
 };
 
-// The tensor-core GEMM on pieces already in device memory: op(A)'s as
-// planes of M rows x plane_ld(K), a_plane_rows rows apart, and op(B)^T's as
-// planes of N rows x b_ld, b_plane_rows rows apart (0: M, N).  Launched as a
-// programmatic dependent of the split ahead of it in the stream.
-emu_status_t gemm_on_pieces(int mode, const void* ap, int64_t a_plane_rows, const void* bp,
-                            int64_t b_ld, int64_t b_plane_rows, int64_t M, int64_t N, int64_t K,
-                            float alpha, float beta, float* C, int64_t ldc, DeviceState* d,
-                            cudaStream_t stream) {
-    const int64_t ldp = plane_ld(K);
+// Where one operand's pieces are: planes starting at p, ld elements per
+// row, plane_rows rows apart (0: the planes' own row count).  mn = 0:
+// K-major, a row per row of op(A) (or of op(B)^T), K elements long.  mn = 1
+// (two-pass BF16 modes): M- or N-major, a row per K index, M (or N) elements
+// long, ld a multiple of 64 (mn_ld) -- what a row-wise split writes from A
+// stored K x M or B stored K x N.
+struct PieceSet {
+    const void* p;
+    int64_t ld;
+    int64_t plane_rows;
+    int mn;
+};
+
+// Whether a two-pass call keeps an operand's pieces M- or N-major: BF16
+// modes (TF32 pieces stay K-major), an operand stored with K as its row
+// index (A with transA, B without transB), so that its split is a row-wise
+// one, and K at least 4 times the operand's M (or N) extent.  Measured on
+// GB300 (BF16x9, same box, the same product with each operand stored both
+// ways): at 8192^3 the GEMM on N-major pieces took 0.8 % longer than on
+// K-major ones, more than the row-wise split saves over the transposed one;
+// at K = 4-8 times M and N the two were even; deeper, M- and N-major pieces
+// won (1024^2 x 32768 7 %, the weight-gradient products 256 x 256, 256 x
+// 1024 and 1024^2 x 1,105,920 6-10 %): a tile's K rows of 512 bytes follow
+// each other in memory, where K-major rows millions of elements long do not.
+// The rule depends on K and the operand's own extent only, so a row chunk of
+// op(A) never changes B's layout.
+inline bool mn_pieces(int mode, bool k_is_row, int64_t K, int64_t extent) {
+    return !mode_is_tf32(mode) && k_is_row && K >= 4 * extent;
+}
+
+// Row length of M- or N-major pieces: whole 64-element chunks (the tensor
+// copies read them a chunk at a time).
+inline int64_t mn_ld(int64_t cols) { return (cols + 63) / 64 * 64; }
+
+// Bytes of one operand's pieces: `rows` rows of op(A) (or of op(B)^T) over K.
+inline size_t piece_bytes(int mode, bool mn, int64_t rows, int64_t K) {
+    const size_t per = (size_t)mode_pieces(mode) * mode_piece_bytes(mode);
+    return mn ? per * (size_t)K * mn_ld(rows) : per * (size_t)rows * plane_ld(K);
+}
+
+// The tensor-core GEMM on pieces already in device memory (op(A)'s and
+// op(B)^T's, as PieceSet says).  Launched as a programmatic dependent of the
+// split ahead of it in the stream.
+emu_status_t gemm_on_pieces(int mode, const PieceSet& a, const PieceSet& b, int64_t M, int64_t N,
+                            int64_t K, float alpha, float beta, float* C, int64_t ldc,
+                            DeviceState* d, cudaStream_t stream) {
     const int tf32 = mode_is_tf32(mode);
     const int planes = mode_pieces(mode);
     const int box_cols = tf32 ? kTcBKBytes / 4 : kTcBKBytes / 2;
     // the two cheaper modes are built for 256-wide tiles only
     const int bn = (mode == kModeBf16x9 || mode == kModeTf32x3) ? kblock_bn(N) : 256;
+    if ((a.mn || b.mn) && tf32) return EMU_ERR_INVALID_VALUE;     // caller's bug
+    // K-major planes: a (K, rows, piece) map read in boxes of one K block x
+    // the CTA's rows; M- or N-major: boxes of one K block x the CTA's
+    // 64-element chunks
     CUtensorMap mapA, mapB;
-    emu_status_t st = make_plane_map(&mapA, ap, tf32, M, K, ldp, planes, box_cols, 128, a_plane_rows);
+    emu_status_t st = a.mn ? make_plane_map_mn(&mapA, a.p, M, K, a.ld, planes, box_cols, 128 / 64,
+                                               a.plane_rows)
+                           : make_plane_map(&mapA, a.p, tf32, M, K, a.ld, planes, box_cols, 128,
+                                            a.plane_rows);
     if (st != EMU_OK) return st;
-    st = make_plane_map(&mapB, bp, tf32, N, K, b_ld, planes, box_cols, bn / 2, b_plane_rows);
+    st = b.mn ? make_plane_map_mn(&mapB, b.p, N, K, b.ld, planes, box_cols, bn / 2 / 64,
+                                  b.plane_rows)
+              : make_plane_map(&mapB, b.p, tf32, N, K, b.ld, planes, box_cols, bn / 2, b.plane_rows);
     if (st != EMU_OK) return st;
 
     TcGemmParams p = {};
@@ -342,6 +417,7 @@ emu_status_t gemm_on_pieces(int mode, const void* ap, int64_t a_plane_rows, cons
     p.tiles_m = (int)((M + 255) / 256);
     p.tiles_n = (int)((N + bn - 1) / bn);
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
+    p.a_mn = a.mn; p.b_mn = b.mn;
     CUtensorMap mapC = mapB;                 // placeholder when C is stored directly
     p.tma_store = make_c_map(&mapC, C, M, N, ldc) ? 1 : 0;
     st = plan_tail(p, mode, 256, bn, 0, d);
@@ -355,10 +431,10 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
                           float beta, float* C, int64_t ldc, DeviceState* d, cudaStream_t stream,
                           bool b_ready = false, BPieces bext = {}) {
     const int64_t ldp = plane_ld(K);
-    const int planes = mode_pieces(mode);
-    const int esize = mode_piece_bytes(mode);
-    const size_t a_bytes = (size_t)planes * M * ldp * esize;
-    const size_t b_bytes = bext.p ? 0 : (size_t)planes * N * ldp * esize;
+    const bool a_mn = mn_pieces(mode, transA, K, M);
+    const bool b_mn = mn_pieces(mode, !transB, K, N) && !bext.p;
+    const size_t a_bytes = piece_bytes(mode, a_mn, M, K);
+    const size_t b_bytes = bext.p ? 0 : piece_bytes(mode, b_mn, N, K);
     const size_t b_region = (b_bytes + 1023) / 1024 * 1024;
     if (b_ready && d->ws_bytes < b_region + a_bytes) return EMU_ERR_INVALID_VALUE;  // caller's bug
     emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, b_region + a_bytes);
@@ -366,23 +442,28 @@ emu_status_t run_two_pass(int mode, int transA, int transB, int64_t M, int64_t N
     uint8_t* wb = static_cast<uint8_t*>(d->ws);
     uint8_t* wa = wb + b_region;
 
+    const PieceSet as{wa, a_mn ? mn_ld(M) : ldp, 0, a_mn ? 1 : 0};
+    const PieceSet bs = bext.p ? PieceSet{bext.p, bext.ld, 0, 0}
+                               : PieceSet{wb, b_mn ? mn_ld(N) : ldp, 0, b_mn ? 1 : 0};
     cudaError_t e;
     {
+        // op(A) is M x K: A itself when transA == 0; A stored K x M split
+        // row-wise into M-major pieces (BF16) or transposed (TF32)
         ProfScope ps(0, stream);
-        e = launch_split_pieces(mode, A, M, K, lda, transA, wa, ldp, stream);
+        e = a_mn ? launch_split_pieces(mode, A, K, M, lda, 0, wa, as.ld, stream)
+                 : launch_split_pieces(mode, A, M, K, lda, transA, wa, ldp, stream);
     }
     if (e != cudaSuccess) return from_cuda(e);
     if (!b_ready && !bext.p) {
-        // op(B)^T is N x K: B itself when transB == 1, B^T otherwise
+        // op(B)^T is N x K: B itself when transB == 1; B stored K x N split
+        // row-wise into N-major pieces (BF16) or transposed (TF32)
         ProfScope ps(0, stream);
         // independent of A's split: may run beside it (programmatic launch)
-        e = launch_split_pieces(mode, B, N, K, ldb, !transB, wb, ldp, stream, true);
+        e = b_mn ? launch_split_pieces(mode, B, K, N, ldb, 0, wb, bs.ld, stream, true)
+                 : launch_split_pieces(mode, B, N, K, ldb, !transB, wb, ldp, stream, true);
     }
     if (e != cudaSuccess) return from_cuda(e);
-    if (bext.p)
-        return gemm_on_pieces(mode, wa, 0, bext.p, bext.ld, 0, M, N, K, alpha, beta, C, ldc, d,
-                              stream);
-    return gemm_on_pieces(mode, wa, 0, wb, ldp, 0, M, N, K, alpha, beta, C, ldc, d, stream);
+    return gemm_on_pieces(mode, as, bs, M, N, K, alpha, beta, C, ldc, d, stream);
 }
 
 // Whether op(A) can be read directly by the fused kernel: K-major rows that
@@ -700,25 +781,33 @@ emu_status_t host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_
             for (int64_t r = m0; r < M; r += mc) bounds[++nch] = (M - r < mc) ? M : r + mc;
         }
     }
-    int64_t max_rows = 0;
-    for (int i = 0; i < nch; ++i)
-        max_rows = bounds[i + 1] - bounds[i] > max_rows ? bounds[i + 1] - bounds[i] : max_rows;
 
     // size the workspace for the largest chunk now: no reallocation (and no
-    // loss of B's pieces) inside the loop
+    // loss of B's pieces) inside the loop; the layouts are run_two_pass's
     const int64_t ldp = plane_ld(K);
-    const size_t pb = pl.mode == EMU_MODE_FP32_SIMT
-                          ? 0
-                          : (size_t)mode_pieces(pl.mode) * mode_piece_bytes(pl.mode) * ldp;
-    const size_t b_region = (pb * N + 1023) / 1024 * 1024;
-    if (pl.mode != EMU_MODE_FP32_SIMT) {
-        const size_t need = pl.fused ? pb * N : b_region + pb * max_rows;
+    const bool simt = pl.mode == EMU_MODE_FP32_SIMT;
+    auto a_mn_rows = [&](int64_t rows) {
+        return !simt && !pl.fused && mn_pieces(pl.mode, transA, K, rows);
+    };
+    const bool b_mn = !simt && !pl.fused && mn_pieces(pl.mode, !transB, K, N);
+    const size_t b_region = simt ? 0 : (piece_bytes(pl.mode, b_mn, N, K) + 1023) / 1024 * 1024;
+    if (!simt) {
+        size_t a_max = 0;                    // the largest chunk's A pieces, in its layout
+        for (int i = 0; i < nch; ++i) {
+            const int64_t rows = bounds[i + 1] - bounds[i];
+            const size_t a = piece_bytes(pl.mode, a_mn_rows(rows), rows, K);
+            a_max = a > a_max ? a : a_max;
+        }
+        const size_t need = pl.fused ? piece_bytes(pl.mode, false, N, K) : b_region + a_max;
         emu_status_t st = ensure_buffer(&d->ws, &d->ws_bytes, need);
         if (st != EMU_OK) return st;
     }
     uint8_t* wb = static_cast<uint8_t*>(d->ws);
     uint8_t* wa = wb + b_region;
-    const size_t prow = pb / mode_pieces(pl.mode == EMU_MODE_FP32_SIMT ? kModeBf16x9 : pl.mode);
+    // bytes from one row (K-major) or column (N-major) of B's pieces to the next
+    const size_t es = simt ? 0 : mode_piece_bytes(pl.mode);
+    const size_t prow = es * ldp;
+    const int64_t ldbn = mn_ld(N);
 
     // the copy streams start after the caller's earlier work on its stream
     e = cudaEventRecord(d->ev_done[0], stream);
@@ -744,9 +833,12 @@ emu_status_t host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_
         if (e != cudaSuccess) break;
         const float* Ai = transA ? dA + r0 : dA + r0 * lda;
         if (panels && i == 0) {
+            const bool a_mn = a_mn_rows(rows);
+            const PieceSet as{wa, a_mn ? mn_ld(rows) : ldp, 0, a_mn ? 1 : 0};
             {
                 ProfScope ps(0, stream);
-                e = launch_split_pieces(pl.mode, Ai, rows, K, lda, transA, wa, ldp, stream);
+                e = a_mn ? launch_split_pieces(pl.mode, Ai, K, rows, lda, 0, wa, as.ld, stream)
+                         : launch_split_pieces(pl.mode, Ai, rows, K, lda, transA, wa, ldp, stream);
             }
             for (int64_t j0 = 0; j0 < N && e == cudaSuccess && st == EMU_OK; j0 += pw) {
                 const int64_t w = N - j0 < pw ? N - j0 : pw;
@@ -762,13 +854,21 @@ emu_status_t host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_
                 if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, d->ev_panel, 0);
                 if (e != cudaSuccess) break;
                 {
+                    // into rows j0.. of B's K-major pieces (planes N rows
+                    // apart), or row-wise into columns j0.. of its N-major
+                    // ones (planes K rows apart)
                     ProfScope ps(0, stream);
-                    e = launch_split_pieces(pl.mode, transB ? dB + j0 * ldb : dB + j0, w, K, ldb,
-                                            !transB, wb + j0 * prow, ldp, stream, false, N);
+                    e = b_mn ? launch_split_pieces(pl.mode, dB + j0, K, w, ldb, 0, wb + j0 * es,
+                                                   ldbn, stream, false, K)
+                             : launch_split_pieces(pl.mode, transB ? dB + j0 * ldb : dB + j0, w, K,
+                                                   ldb, !transB, wb + j0 * prow, ldp, stream,
+                                                   false, N);
                 }
+                const PieceSet bs = b_mn ? PieceSet{wb + j0 * es, ldbn, K, 1}
+                                         : PieceSet{wb + j0 * prow, ldp, N, 0};
                 if (e == cudaSuccess)
-                    st = gemm_on_pieces(pl.mode, wa, 0, wb + j0 * prow, ldp, N, rows, w, K, alpha,
-                                        beta, dC + j0, ldc, d, stream);
+                    st = gemm_on_pieces(pl.mode, as, bs, rows, w, K, alpha, beta, dC + j0, ldc, d,
+                                        stream);
             }
         } else {
             st = run_planned(pl, transA, transB, rows, N, K, alpha, Ai, lda, dB, ldb, beta,
@@ -968,8 +1068,14 @@ size_t emu_workspace_size(int64_t M, int64_t N, int64_t K, int mode) {
     if (M <= 0 || N <= 0 || K <= 0 || mode == EMU_MODE_FP32_SIMT) return 0;
     if (!valid_mode(mode) || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return 0;
     if (!workspace_fits(M, N, K)) return SIZE_MAX;
-    const size_t per = (size_t)mode_pieces(mode) * plane_ld(K) * mode_piece_bytes(mode);
-    return (per * M + 1023) / 1024 * 1024 + per * N;
+    // B's pieces, then A's at a 1 KB boundary (run_two_pass), each in the
+    // larger of its layouts: the transposes decide which one a call takes
+    auto most = [&](int64_t rows) {
+        const size_t k_major = piece_bytes(mode, false, rows, K);
+        const size_t mn = mn_pieces(mode, true, K, rows) ? piece_bytes(mode, true, rows, K) : 0;
+        return k_major > mn ? k_major : mn;
+    };
+    return (most(N) + 1023) / 1024 * 1024 + most(M);
 }
 
 emu_status_t emu_get_last_device_error(void) {

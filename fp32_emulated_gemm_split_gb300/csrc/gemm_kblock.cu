@@ -191,22 +191,30 @@ __device__ __forceinline__ void tile_pos(int tile, int tiles_m, int tiles_n, int
     tn = r / gm;
 }
 
+// An M- or N-major piece tile in shared memory: chunks of 64 elements of M
+// or N by one K block (64 rows of 128 bytes), this far apart.
+constexpr uint32_t kMnBox = 64 * kTcBKBytes;          // 8 KB
+
 // The MMAs of one piece pair (i, j) for one K block: four K=16 (BF16) or
-// K=8 (TF32) steps inside the 128-byte swizzled rows.  `first` marks the
-// first MMA of a fresh accumulator; `shift` asks the first step to scale the
-// accumulator by 2^-SHIFT (start of a new, larger band).
+// K=8 (TF32) steps.  A K-major tile advances 32 bytes along its swizzled
+// rows per step; an M- or N-major one (bit 0 of `mn` for A, bit 1 for B;
+// BF16 only) 16 K rows, 2048 bytes.  `first` marks the first MMA of a fresh
+// accumulator; `shift` asks the first step to scale the accumulator by
+// 2^-SHIFT (start of a new, larger band).
 template <int TF32, int SHIFT = 8>
 __device__ __forceinline__ void mma_pair(uint32_t d, uint32_t a_tile, uint32_t b_tile,
-                                         uint32_t idesc, bool first, bool shift) {
-    const uint64_t adesc = make_sw128_kmajor_desc(a_tile);
-    const uint64_t bdesc = make_sw128_kmajor_desc(b_tile);
+                                         uint32_t idesc, bool first, bool shift, int mn = 0) {
+    const uint64_t adesc = (mn & 1) ? make_sw128_mn_desc(a_tile, kMnBox) : make_sw128_kmajor_desc(a_tile);
+    const uint64_t bdesc = (mn & 2) ? make_sw128_mn_desc(b_tile, kMnBox) : make_sw128_kmajor_desc(b_tile);
+    const uint64_t astep = (mn & 1) ? (2048 >> 4) : (32 >> 4);
+    const uint64_t bstep = (mn & 2) ? (2048 >> 4) : (32 >> 4);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
+        const uint64_t ak = adesc + k * astep, bk = bdesc + k * bstep;
         if (k == 0 && shift)
-            mma_cta2_scaled<TF32, SHIFT>(d, adesc + koff, bdesc + koff, idesc);
+            mma_cta2_scaled<TF32, SHIFT>(d, ak, bk, idesc);
         else
-            mma_cta2<TF32>(d, adesc + koff, bdesc + koff, idesc, (k == 0 && first) ? 0u : 1u);
+            mma_cta2<TF32>(d, ak, bk, idesc, (k == 0 && first) ? 0u : 1u);
     }
 }
 
@@ -367,6 +375,9 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // operand layouts of the pieces (bit 0: A M-major, bit 1: B N-major):
+    // two-pass BF16 modes only
+    const int mn = (Cfg::TM || Cfg::SMS || Cfg::tf32) ? 0 : ((p.a_mn ? 1 : 0) | (p.b_mn ? 2 : 0));
     // A kernel launched behind this one as a programmatic dependent (the next
     // GEMM of a run of calls on already-split weights) may start now on SMs
     // this grid leaves free: every one of its reads and writes of global
@@ -410,10 +421,22 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                     for (int pc = P - 1; pc >= 0; --pc) {
                         if (leader) mbar_arrive_expect_tx(full0 + 8 * (s * P + pc), Cfg::piece_tx);
                         const uint32_t fbl = full_leader0 + 8 * (s * P + pc);
-                        if (!Cfg::TM && !Cfg::SMS)
-                            tma_load_3d_pair(st + pc * kATile, &mapA, fbl, kb * Cfg::elems, arow, pc);
-                        tma_load_3d_pair(st + P * (Cfg::TM ? 0 : kATile) + pc * Cfg::b_tile, &mapB, fbl,
-                                         kb * Cfg::elems, brow, pc);
+                        // K-major maps are (K, rows, piece); M- or N-major
+                        // ones (K rows of M or N elements: two-pass BF16
+                        // only) are (element, K, 64-element chunk, piece),
+                        // the CTA's chunks one box, kMnBox apart
+                        if (!Cfg::TM && !Cfg::SMS) {
+                            const uint32_t adst = st + pc * kATile;
+                            if (mn & 1)
+                                tma_load_4d_pair(adst, &mapA, fbl, 0, kb * Cfg::elems, arow / 64, pc);
+                            else
+                                tma_load_3d_pair(adst, &mapA, fbl, kb * Cfg::elems, arow, pc);
+                        }
+                        const uint32_t bdst = st + P * (Cfg::TM ? 0 : kATile) + pc * Cfg::b_tile;
+                        if (mn & 2)
+                            tma_load_4d_pair(bdst, &mapB, fbl, 0, kb * Cfg::elems, brow / 64, pc);
+                        else
+                            tma_load_3d_pair(bdst, &mapB, fbl, kb * Cfg::elems, brow, pc);
                     }
                 }
             }
@@ -422,7 +445,8 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
     } else if (warp == R::mma) {
         if (lane == 0 && leader) {
             // ------------------------------------------------------ MMA issuer
-            const uint32_t idesc = make_idesc(Cfg::tf32 ? 2u : 1u, kBM, BN);
+            const uint32_t idesc = make_idesc(Cfg::tf32 ? 2u : 1u, kBM, BN) |
+                                   ((mn & 1) ? kIdescAMn : 0u) | ((mn & 2) ? kIdescBMn : 0u);
             constexpr int KBP = Cfg::kb_per_partial;
             uint32_t kbg = 0, part = 0;              // K blocks and TMEM partials so far
             uint32_t prev_s = 0;                     // band-major: stage of the pair's first block
@@ -487,17 +511,17 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                         pr(0, 0, false, true);                                    // band 0
                     } else if constexpr (MODE == kModeBf16x9) {
                         if (!ready(2)) { ok = false; break; }
-                        mma_pair<0>(d, A(2), B(2), idesc, true, false);           // band 4
+                        mma_pair<0>(d, A(2), B(2), idesc, true, false, mn);       // band 4
                         if (!ready(1)) { ok = false; break; }
-                        mma_pair<0>(d, A(1), B(2), idesc, false, true);           // band 3
-                        mma_pair<0>(d, A(2), B(1), idesc, false, false);
+                        mma_pair<0>(d, A(1), B(2), idesc, false, true, mn);       // band 3
+                        mma_pair<0>(d, A(2), B(1), idesc, false, false, mn);
                         if (!ready(0)) { ok = false; break; }
-                        mma_pair<0>(d, A(0), B(2), idesc, false, true);           // band 2
-                        mma_pair<0>(d, A(1), B(1), idesc, false, false);
-                        mma_pair<0>(d, A(2), B(0), idesc, false, false);
-                        mma_pair<0>(d, A(0), B(1), idesc, false, true);           // band 1
-                        mma_pair<0>(d, A(1), B(0), idesc, false, false);
-                        mma_pair<0>(d, A(0), B(0), idesc, false, true);           // band 0
+                        mma_pair<0>(d, A(0), B(2), idesc, false, true, mn);       // band 2
+                        mma_pair<0>(d, A(1), B(1), idesc, false, false, mn);
+                        mma_pair<0>(d, A(2), B(0), idesc, false, false, mn);
+                        mma_pair<0>(d, A(0), B(1), idesc, false, true, mn);       // band 1
+                        mma_pair<0>(d, A(1), B(0), idesc, false, false, mn);
+                        mma_pair<0>(d, A(0), B(0), idesc, false, true, mn);       // band 0
                     } else if constexpr (MODE == kModeTf32x3) {
                         if (!ready(1) || !ready(0)) { ok = false; break; }
                         mma_pair<1>(d, A(0), B(1), idesc, fresh, false);          // hi*lo
@@ -508,8 +532,8 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                         // Ootomo-Yokota: hi lo' + lo' hi, then hi hi, shift 2^-11.
                         constexpr int T = Cfg::tf32 ? 1 : 0, SH = Cfg::band_shift;
                         if (!ready(1) || !ready(0)) { ok = false; break; }
-                        mma_pair<T>(d, A(0), B(1), idesc, fresh, false);          // band 1
-                        mma_pair<T>(d, A(1), B(0), idesc, false, false);
+                        mma_pair<T>(d, A(0), B(1), idesc, fresh, false, mn);      // band 1
+                        mma_pair<T>(d, A(1), B(0), idesc, false, false, mn);
                         if (!close) {
                             prev_s = s;                  // band 0 after the next block's band 1
                             continue;                    // stage held: no empty commit yet
@@ -517,11 +541,11 @@ gemm_kblock_kernel(const __grid_constant__ CUtensorMap mapA,
                         if (!fresh) {
                             // band 0 of the pair's first block (shift), free its stage
                             const uint32_t pst = smem_u32(smem + prev_s * Cfg::stage_bytes);
-                            mma_pair<T, SH>(d, pst, pst + P * kATile, idesc, false, true);
+                            mma_pair<T, SH>(d, pst, pst + P * kATile, idesc, false, true, mn);
                             tc_commit_pair(empty0 + 8 * prev_s);
-                            mma_pair<T>(d, A(0), B(0), idesc, false, false);
+                            mma_pair<T>(d, A(0), B(0), idesc, false, false, mn);
                         } else {
-                            mma_pair<T, SH>(d, A(0), B(0), idesc, false, true);
+                            mma_pair<T, SH>(d, A(0), B(0), idesc, false, true, mn);
                         }
                     } else {
                         if (!ready(0)) { ok = false; break; }

@@ -84,13 +84,21 @@ def test_path_selection_and_workspace_size(emu):
     emu.emu_set_path("twopass")
     assert emu.emu_get_path() == "twopass"
     emu.emu_set_path("auto")
-    # three BF16 pieces of op(A) and op(B)^T, rows padded to 8 elements
-    assert emu.emu_workspace_size(100, 60, 13, "bf16x9") == (3 * 16 * 2 * 100 + 1023) // 1024 * 1024 + 3 * 16 * 2 * 60
-    assert emu.emu_workspace_size(100, 60, 13, "tf32x3") == (2 * 16 * 4 * 100 + 1023) // 1024 * 1024 + 2 * 16 * 4 * 60
+    # B's pieces first (region rounded up to 1 KB), then A's.  K-major: rows
+    # of op(A) and op(B)^T, K = 13 padded to 16 elements (K is less than 4
+    # times M and N, so no call of this shape keeps M- or N-major pieces)
+    kib = lambda x: (x + 1023) // 1024 * 1024
+    assert emu.emu_workspace_size(100, 60, 13, "bf16x9") == kib(3 * 2 * 16 * 60) + 3 * 2 * 16 * 100
+    assert emu.emu_workspace_size(100, 60, 13, "tf32x3") == kib(2 * 4 * 16 * 60) + 2 * 4 * 16 * 100
     # the cheaper rungs: two BF16 pieces, one TF32 piece
-    assert emu.emu_workspace_size(100, 60, 13, "bf16x3") == (2 * 16 * 2 * 100 + 1023) // 1024 * 1024 + 2 * 16 * 2 * 60
-    assert emu.emu_workspace_size(100, 60, 13, "tf32") == (1 * 16 * 4 * 100 + 1023) // 1024 * 1024 + 1 * 16 * 4 * 60
+    assert emu.emu_workspace_size(100, 60, 13, "bf16x3") == kib(2 * 2 * 16 * 60) + 2 * 2 * 16 * 100
+    assert emu.emu_workspace_size(100, 60, 13, "tf32") == kib(1 * 4 * 16 * 60) + 1 * 4 * 16 * 100
     assert emu.emu_workspace_size(100, 60, 13, "tf32x3_oy") == emu.emu_workspace_size(100, 60, 13, "tf32x3")
+    # one row and one column, K = 1000: the BF16 modes may keep M- and N-major
+    # pieces (1000 rows of one 64-element chunk), the larger; TF32 K-major
+    # ones (1000 elements)
+    assert emu.emu_workspace_size(1, 1, 1000, "bf16x9") == kib(3 * 2 * 1000 * 64) + 3 * 2 * 1000 * 64
+    assert emu.emu_workspace_size(1, 1, 1000, "tf32x3") == kib(2 * 4 * 1000) + 2 * 4 * 1000
     assert emu.lib().emu_workspace_size(100, 60, 13, 6) == 0
     assert emu.emu_workspace_size(100, 60, 13, "fp32_simt") == 0
     assert emu.emu_workspace_size(0, 60, 13, "bf16x9") == 0

@@ -158,6 +158,25 @@ def test_host_entry_point_column_panels(emu, kind, transB):
     assert np.array_equal(C.view(np.uint32), E.view(np.uint32))
 
 
+@pytest.mark.parametrize("kind", ["a2", "b1"])
+def test_host_entry_point_n_major_column_panels(emu, kind):
+    """emu_sgemm_host with B stored K x N and K >= 4 N (600 x 2304 x 9300,
+    B 86 MB): each column panel of B is split row-wise into its columns of
+    B's N-major pieces as it lands and multiplied by all 600 rows of op(A)
+    (three panels, no later row chunk).  Exact, so bit for bit on every
+    output."""
+    A, B = BC.make(kind, 600, 2304, 9300, 0, 0, seed=12)
+    E = BC.exact(A, B, 0, 0).astype(np.float32)
+    emu.emu_profile_enable(True)
+    try:
+        C = emu.emu_sgemm_host(A, B)
+        launches = emu.emu_profile_read("gemm_tc")[0]
+    finally:
+        emu.emu_profile_enable(False)
+    assert launches == 3, launches
+    assert np.array_equal(C.view(np.uint32), E.view(np.uint32))
+
+
 LADDER = {"tf32x3": oracle.gemm_tf32x3, "tf32x3_oy": oracle.gemm_tf32x3_oy,
           "bf16x3": oracle.gemm_bf16x3, "tf32": oracle.gemm_tf32}
 

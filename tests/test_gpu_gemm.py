@@ -88,6 +88,52 @@ def test_ragged_shapes_every_element(emu, mode, shape, transA, transB):
     assert ratio <= 1.0, ratio
 
 
+# (M, N, K): the BF16 modes keep an operand stored with K as its row index
+# M- or N-major when K >= 4 times its M (or N): both operands here ...
+LAYOUT_SHAPES = [(256, 300, 1300), (129, 257, 1100), (1, 9, 40), (64, 1000, 4100),
+                 (1536, 512, 7000), (256, 256, 100000),
+                 # ... only B ...
+                 (200, 1, 64), (1000, 60, 2000),
+                 # ... neither (K-major pieces, B^T split transposed)
+                 (300, 513, 1000), (4096, 4096, 512)]
+
+
+@pytest.mark.parametrize("shape", LAYOUT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mode", ["bf16x9", "bf16x3", "tf32x3"])
+def test_operand_layout_does_not_change_a_bit(emu, mode, shape):
+    """op(A) and op(B) fixed, stored four ways (A as M x K or K x M, B as
+    K x N or N x K).  Where K is at least 4 times M (or N), the BF16 modes
+    split an operand stored with K as its row index row-wise into M- or
+    N-major pieces, which the tensor core reads through the transpose bits
+    of its instruction descriptor; otherwise, and always for TF32x3 (the
+    control), into K-major pieces.  The products and their order are the
+    same either way, so the four results are the same bits, on the two-pass
+    path (1536 x 512 x 7000, 256 x 256 x 100000 and 4096^2 x 512 with
+    stream-K tails)."""
+    M, N, K = shape
+    r = W.rng(M + 3 * N + 7 * K)
+    opA = W.normal(r, (M, K))
+    opB = W.normal(r, (K, N), std=K ** -0.5)
+    C0 = W.uniform(r, (M, N))
+    old = emu.emu_get_path()
+    emu.emu_set_path("twopass")
+    try:
+        outs = {}
+        for tA in (0, 1):
+            for tB in (0, 1):
+                A = np.ascontiguousarray(opA.T) if tA else opA
+                B = np.ascontiguousarray(opB.T) if tB else opB
+                outs[(tA, tB)] = _run(emu, A, B, tA, tB, alpha=1.5, beta=-0.5, C0=C0, mode=mode)
+    finally:
+        emu.emu_set_path(old)
+    ref = outs[(0, 1)]                  # K-major pieces of both operands
+    for k, C in outs.items():
+        assert np.array_equal(C.view(np.uint32), ref.view(np.uint32)), k
+    mi, ni = W.sample_pairs(M, N, 1024, seed=M)
+    Cref, Sabs = oracle.gemm_ref(opA, opB, 0, 0, 1.5, -0.5, C0, pairs=(mi, ni))
+    assert checks.error_ratio(ref[mi, ni], Cref, Sabs, K, 1.5, -0.5, C0[mi, ni], mode=mode) <= 1.0
+
+
 def test_strided_operands_and_output(emu):
     import torch
     r = W.rng(5)
