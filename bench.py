@@ -554,7 +554,7 @@ def bench_weight_gradients(emu, stream, peaks, peak_src, reps=5):
     res["_how"] = ("dW = dY^T X of the 1.1M-row MLIP layers (transA), BF16x9, operands drawn "
                    "on the GPU, 5 calls back to back; kernel_frac: 18MNK / GEMM time / "
                    f"{peak_src} BF16 burst peak; split_ms: both operands' splits (row-wise, "
-                   "into M- and N-major pieces: K is more than 4 times M and N)")
+                   "into M- and N-major pieces)")
     return res
 
 
@@ -573,7 +573,8 @@ def pick_workload(W, args):
 def load_traffic(kernel, workload, mode):
     """DRAM bytes per launch of `kernel` from a committed ncu capture
     (profiles/traffic.json), if one matches this kernel, workload and mode and
-    the kernel's source has not changed since the counters were taken."""
+    none of the sources it records (the kernel, and the host code that picks
+    its operands' layouts) has changed since the counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -583,12 +584,13 @@ def load_traffic(kernel, workload, mode):
     rec = d.get(f"{kernel}:{workload}:{mode}")
     if not rec:
         return None
-    src = os.path.join(ROOT, rec["source"])
-    if not os.path.exists(src):
-        return None
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+    for rel, sha in rec["sources"].items():
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
             return None
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != sha:
+                return None
     return rec["bytes"]
 
 

@@ -357,21 +357,25 @@ struct PieceSet {
     int mn;
 };
 
-// Whether a two-pass call keeps an operand's pieces M- or N-major: BF16
-// modes (TF32 pieces stay K-major), an operand stored with K as its row
-// index (A with transA, B without transB), so that its split is a row-wise
-// one, and K at least 4 times the operand's M (or N) extent.  Measured on
-// GB300 (BF16x9, same box, the same product with each operand stored both
-// ways): at 8192^3 the GEMM on N-major pieces took 0.8 % longer than on
-// K-major ones, more than the row-wise split saves over the transposed one;
-// at K = 4-8 times M and N the two were even; deeper, M- and N-major pieces
-// won (1024^2 x 32768 7 %, the weight-gradient products 256 x 256, 256 x
-// 1024 and 1024^2 x 1,105,920 6-10 %): a tile's K rows of 512 bytes follow
-// each other in memory, where K-major rows millions of elements long do not.
-// The rule depends on K and the operand's own extent only, so a row chunk of
-// op(A) never changes B's layout.
+// Whether a two-pass call keeps an operand's pieces M- or N-major: an
+// operand stored with K as its row index (A with transA, B without transB),
+// whose split is then a row-wise one instead of a transposed one (about
+// 20 us less per 8192^2 operand on GB300).  BF16x9 always: measured on GB300
+// with launches of the two layouts alternating on one box (40-60 pairs,
+// median of the pair differences), the GEMM takes the same time on N-major
+// as on K-major pieces at 8192^3, 4096^3, 12288 x 1024 x 256 and 1.1M x 1024
+// x 256 (within 0.1 %), and less for deep K (1024^2 x 32768 7 %, the weight
+// gradients 256 x 256, 256 x 1024 and 1024^2 x 1,105,920 6-10 %: a tile's K
+// rows of 512 bytes follow each other in memory, where K-major rows millions
+// of elements long do not).  BF16x3, whose tile loads bound it, only when K
+// is at least 4 times the operand's M (or N): at 8192^3 N-major pieces cost
+// it 4.75 % (a K-major box row's L2 fetch, promoted to 256 bytes, brings the
+// next K block's bytes along).  TF32 pieces stay K-major.  The rule depends
+// on K and the operand's own extent only, so a row chunk of op(A) never
+// changes B's layout.
 inline bool mn_pieces(int mode, bool k_is_row, int64_t K, int64_t extent) {
-    return !mode_is_tf32(mode) && k_is_row && K >= 4 * extent;
+    if (!k_is_row) return false;
+    return mode == kModeBf16x9 || (mode == kModeBf16x3 && K >= 4 * extent);
 }
 
 // Row length of M- or N-major pieces: whole 64-element chunks (the tensor

@@ -348,11 +348,11 @@ int emu_choose_mode(int64_t M, int64_t N, int64_t K, int mode, int strategy, int
 double emu_predict_us(int64_t M, int64_t N, int64_t K, int mode, int sms);
 
 /* Bytes of workspace the two-pass path needs for one call of this shape,
- * whatever its transposes: the BF16 modes keep the pieces of an operand
- * stored with K as its row index (A with transA, B without transB) M- or
- * N-major (K rows of M or N elements, rounded up to 64) when K is at least
- * 4 times that operand's M (or N), otherwise pieces are K-major (rows of K
- * elements, rounded up to 8); this is the larger of the two for each
+ * whatever its transposes.  The pieces of an operand stored with K as its
+ * row index (A with transA, B without transB) are M- or N-major (K rows of
+ * M or N elements, rounded up to 64) in BF16x9, and in BF16x3 when K is at
+ * least 4 times that operand's M (or N); all other pieces are K-major (rows
+ * of K elements, rounded up to 8).  This is the larger of the two for each
  * operand, B's region rounded up to 1 KB. */
 size_t emu_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
 

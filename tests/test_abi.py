@@ -85,10 +85,13 @@ def test_path_selection_and_workspace_size(emu):
     assert emu.emu_get_path() == "twopass"
     emu.emu_set_path("auto")
     # B's pieces first (region rounded up to 1 KB), then A's.  K-major: rows
-    # of op(A) and op(B)^T, K = 13 padded to 16 elements (K is less than 4
-    # times M and N, so no call of this shape keeps M- or N-major pieces)
+    # of op(A) and op(B)^T, K = 13 padded to 16 elements.  BF16x9 keeps an
+    # operand stored with K as its row index M- or N-major (13 rows of M or
+    # N padded to 64): the larger for A (13 x 128 > 100 x 16), not for B
+    # (13 x 64 < 60 x 16).  The other modes stay K-major here (BF16x3 goes
+    # M- or N-major only when K is at least 4 times M or N)
     kib = lambda x: (x + 1023) // 1024 * 1024
-    assert emu.emu_workspace_size(100, 60, 13, "bf16x9") == kib(3 * 2 * 16 * 60) + 3 * 2 * 16 * 100
+    assert emu.emu_workspace_size(100, 60, 13, "bf16x9") == kib(3 * 2 * 16 * 60) + 3 * 2 * 13 * 128
     assert emu.emu_workspace_size(100, 60, 13, "tf32x3") == kib(2 * 4 * 16 * 60) + 2 * 4 * 16 * 100
     # the cheaper rungs: two BF16 pieces, one TF32 piece
     assert emu.emu_workspace_size(100, 60, 13, "bf16x3") == kib(2 * 2 * 16 * 60) + 2 * 2 * 16 * 100
@@ -97,6 +100,7 @@ def test_path_selection_and_workspace_size(emu):
     # one row and one column, K = 1000: the BF16 modes may keep M- and N-major
     # pieces (1000 rows of one 64-element chunk), the larger; TF32 K-major
     # ones (1000 elements)
+    assert emu.emu_workspace_size(1, 1, 1000, "bf16x3") == kib(2 * 2 * 1000 * 64) + 2 * 2 * 1000 * 64
     assert emu.emu_workspace_size(1, 1, 1000, "bf16x9") == kib(3 * 2 * 1000 * 64) + 3 * 2 * 1000 * 64
     assert emu.emu_workspace_size(1, 1, 1000, "tf32x3") == kib(2 * 4 * 1000) + 2 * 4 * 1000
     assert emu.lib().emu_workspace_size(100, 60, 13, 6) == 0

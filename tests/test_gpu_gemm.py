@@ -88,13 +88,14 @@ def test_ragged_shapes_every_element(emu, mode, shape, transA, transB):
     assert ratio <= 1.0, ratio
 
 
-# (M, N, K): the BF16 modes keep an operand stored with K as its row index
-# M- or N-major when K >= 4 times its M (or N): both operands here ...
+# (M, N, K): BF16x9 keeps an operand stored with K as its row index M- or
+# N-major; BF16x3 only when K >= 4 times its M (or N), which holds for both
+# operands here ...
 LAYOUT_SHAPES = [(256, 300, 1300), (129, 257, 1100), (1, 9, 40), (64, 1000, 4100),
                  (1536, 512, 7000), (256, 256, 100000),
                  # ... only B ...
                  (200, 1, 64), (1000, 60, 2000),
-                 # ... neither (K-major pieces, B^T split transposed)
+                 # ... neither (K-major pieces, split transposed)
                  (300, 513, 1000), (4096, 4096, 512)]
 
 
@@ -102,8 +103,8 @@ LAYOUT_SHAPES = [(256, 300, 1300), (129, 257, 1100), (1, 9, 40), (64, 1000, 4100
 @pytest.mark.parametrize("mode", ["bf16x9", "bf16x3", "tf32x3"])
 def test_operand_layout_does_not_change_a_bit(emu, mode, shape):
     """op(A) and op(B) fixed, stored four ways (A as M x K or K x M, B as
-    K x N or N x K).  Where K is at least 4 times M (or N), the BF16 modes
-    split an operand stored with K as its row index row-wise into M- or
+    K x N or N x K).  BF16x9 (and BF16x3 where K is at least 4 times M or
+    N) splits an operand stored with K as its row index row-wise into M- or
     N-major pieces, which the tensor core reads through the transpose bits
     of its instruction descriptor; otherwise, and always for TF32x3 (the
     control), into K-major pieces.  The products and their order are the
