@@ -33,6 +33,11 @@
 // (BN = 256 or 128); per K block each CTA stages 128 rows of each A piece and
 // BN/2 rows of each B^T piece (128-byte swizzled rows); one
 // tcgen05.mma.cta_group::2 (M = 256, N = BN) reads both CTAs' shared memory.
+// Two-pass BF16 pieces may instead be M- or N-major (K rows of M or N
+// elements, from a row-wise split of A stored K x M or B stored K x N): the
+// CTA's 128 rows or BN/2 columns then arrive as 64-element chunks of 64 K
+// rows, 8 KB apart, and the MMA reads them through an MN-major descriptor and
+// the transpose bit of its instruction descriptor (TcGemmParams::a_mn, b_mn).
 // Each stage has one "full" barrier per piece index so the band-4 MMAs start
 // when pieces 2 land.  Persistent: one cluster per SM pair walks the tiles;
 // tensor memory holds 512/BN partial buffers, so the tensor core fills the
