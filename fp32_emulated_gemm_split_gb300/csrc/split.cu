@@ -11,6 +11,8 @@
 // its writes: the two-piece BF16 and single-pass TF32 modes do not read it.
 // The Ootomo-Yokota variant scales the TF32 residual by 2^11 (lo_scale)
 // before rounding it.
+#include <atomic>
+
 #include "emu_device.cuh"
 
 namespace emu {
@@ -20,6 +22,14 @@ namespace {
 
 // Each thread splits 8 consecutive elements of one row: two 16-byte loads,
 // one 16-byte store per piece.  Requires 16-byte aligned rows in and out.
+// U groups per thread per step, all loaded before any is split: with U = 1
+// each thread keeps one 32-byte read in flight, too few to cover HBM's
+// latency.  Measured on GB300 (an L2 flush before each launch): 8192^2 115.3
+// / 111.3 / 109.2 us for U = 1 / 2 / 4 (U = 4: 6.15 TB/s, the speed of a
+// plain stream with the same 4-byte-read, 6-byte-write mix); 1.1M x 256
+// 480 / 451 / 442 us; 12288 x 256 10.9 us with U = 1, 12.9 with U = 4 (too
+// few groups to go round), so the launcher keeps U = 1 for small splits.
+template <int U>
 __global__ void __launch_bounds__(256) split3_rows_vec8(const float* __restrict__ X, int64_t rows,
                                                         int64_t cols, int64_t ld,
                                                         uint16_t* __restrict__ P0,
@@ -28,22 +38,35 @@ __global__ void __launch_bounds__(256) split3_rows_vec8(const float* __restrict_
     griddep_launch_dependents();
     const int64_t groups = cols / 8;
     const int64_t total = rows * groups;
-    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
-         t += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = t / groups;
-        const int64_t c = (t - r * groups) * 8;
-        const float4* src = reinterpret_cast<const float4*>(X + r * ld + c);
-        const float4 a = __ldcs(src);
-        const float4 b = __ldcs(src + 1);
-        uint4 o0, o1, o2;
-        split_bf16x3_pair(a.x, a.y, o0.x, o1.x, o2.x);
-        split_bf16x3_pair(a.z, a.w, o0.y, o1.y, o2.y);
-        split_bf16x3_pair(b.x, b.y, o0.z, o1.z, o2.z);
-        split_bf16x3_pair(b.z, b.w, o0.w, o1.w, o2.w);
-        const int64_t o = r * ldp + c;
-        *reinterpret_cast<uint4*>(P0 + o) = o0;
-        *reinterpret_cast<uint4*>(P1 + o) = o1;
-        if (P2) *reinterpret_cast<uint4*>(P2 + o) = o2;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t t0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t0 < total; t0 += U * stride) {
+        float4 a[U], b[U];
+        int64_t o[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t t = t0 + u * stride;
+            if (t < total) {
+                const int64_t r = t / groups;
+                const int64_t c = (t - r * groups) * 8;
+                const float4* src = reinterpret_cast<const float4*>(X + r * ld + c);
+                a[u] = __ldcs(src);
+                b[u] = __ldcs(src + 1);
+                o[u] = r * ldp + c;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (t0 + u * stride < total) {
+                uint4 o0, o1, o2;
+                split_bf16x3_pair(a[u].x, a[u].y, o0.x, o1.x, o2.x);
+                split_bf16x3_pair(a[u].z, a[u].w, o0.y, o1.y, o2.y);
+                split_bf16x3_pair(b[u].x, b[u].y, o0.z, o1.z, o2.z);
+                split_bf16x3_pair(b[u].z, b[u].w, o0.w, o1.w, o2.w);
+                *reinterpret_cast<uint4*>(P0 + o[u]) = o0;
+                *reinterpret_cast<uint4*>(P1 + o[u]) = o1;
+                if (P2) *reinterpret_cast<uint4*>(P2 + o[u]) = o2;
+            }
+        }
     }
     griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
@@ -69,6 +92,10 @@ __global__ void __launch_bounds__(256) split3_rows_scalar(const float* __restric
     griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
 
+// TF32 pieces, 4 consecutive elements per group, U groups per thread per
+// step as above (8192^2: 158 / 150 / 140 us for U = 1 / 2 / 4; 1.1M x 256:
+// 644 / 609 / 578 us).
+template <int U>
 __global__ void __launch_bounds__(256) split2_rows_vec4(const float* __restrict__ X, int64_t rows,
                                                         int64_t cols, int64_t ld,
                                                         float* __restrict__ HI,
@@ -76,18 +103,32 @@ __global__ void __launch_bounds__(256) split2_rows_vec4(const float* __restrict_
     griddep_launch_dependents();
     const int64_t groups = cols / 4;
     const int64_t total = rows * groups;
-    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
-         t += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = t / groups;
-        const int64_t c = (t - r * groups) * 4;
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(X + r * ld + c));
-        float4 h, l;
-        split_tf32x2(a.x, h.x, l.x, lo_scale);
-        split_tf32x2(a.y, h.y, l.y, lo_scale);
-        split_tf32x2(a.z, h.z, l.z, lo_scale);
-        split_tf32x2(a.w, h.w, l.w, lo_scale);
-        *reinterpret_cast<float4*>(HI + r * ldp + c) = h;
-        if (LO) *reinterpret_cast<float4*>(LO + r * ldp + c) = l;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t t0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t0 < total; t0 += U * stride) {
+        float4 a[U];
+        int64_t o[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t t = t0 + u * stride;
+            if (t < total) {
+                const int64_t r = t / groups;
+                const int64_t c = (t - r * groups) * 4;
+                a[u] = __ldcs(reinterpret_cast<const float4*>(X + r * ld + c));
+                o[u] = r * ldp + c;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (t0 + u * stride < total) {
+                float4 h, l;
+                split_tf32x2(a[u].x, h.x, l.x, lo_scale);
+                split_tf32x2(a[u].y, h.y, l.y, lo_scale);
+                split_tf32x2(a[u].z, h.z, l.z, lo_scale);
+                split_tf32x2(a[u].w, h.w, l.w, lo_scale);
+                *reinterpret_cast<float4*>(HI + o[u]) = h;
+                if (LO) *reinterpret_cast<float4*>(LO + o[u]) = l;
+            }
+        }
     }
     griddep_wait();          // see launch_pdl: complete only after the kernel ahead
 }
@@ -168,9 +209,13 @@ __global__ void __launch_bounds__(256) split3_transposed(const float* __restrict
 }
 
 // Vectorised form for full 64 x 64 tiles with 16-byte aligned rows on both
-// sides: each thread loads four float4 along stored rows; then lanes 4i..4i+3
-// of a warp write the 64 pieces of one op row as 16-byte stores, 128
-// contiguous bytes per piece.  Tiles at the ragged edges use the kernel above.
+// sides: each thread loads four float4 along stored rows; then for each half
+// of an op row, lanes 4i..4i+3 of a warp write its pieces as 16-byte stores
+// of consecutive 8-element groups: 64 contiguous bytes per piece and store,
+// and the four lanes' shared-memory reads fall on distinct banks.  Tiles at
+// the ragged edges use the kernel above.  Measured on GB300 at 8192^2 (an L2
+// flush before each launch): 127.6 us when each lane wrote a 16-element run
+// as two stores 32 bytes apart.
 __global__ void __launch_bounds__(256) split3_transposed_vec(const float* __restrict__ X, int64_t rows,
                                                              int64_t cols, int64_t ld,
                                                              uint16_t* __restrict__ P0,
@@ -193,20 +238,19 @@ __global__ void __launch_bounds__(256) split3_transposed_vec(const float* __rest
             tile[k][r4 + 3] = v.w;
         }
         __syncthreads();
-        const int rr = tid >> 2, cp = tid & 3;           // op row in tile, 16-element part
-        uint32_t w0[8], w1[8], w2[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            split_bf16x3_pair(tile[16 * cp + 2 * i][rr], tile[16 * cp + 2 * i + 1][rr], w0[i], w1[i], w2[i]);
-        const int64_t o = (r0 + rr) * ldp + c0 + 16 * cp;
-        uint4* d0 = reinterpret_cast<uint4*>(P0 + o);
-        uint4* d1 = reinterpret_cast<uint4*>(P1 + o);
-        uint4* d2 = reinterpret_cast<uint4*>(P2 + o);
+        const int rr = tid >> 2, cp = tid & 3;           // op row in tile, 8-element group
+        const int64_t o = (r0 + rr) * ldp + c0 + 8 * cp;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            d0[q] = make_uint4(w0[4 * q], w0[4 * q + 1], w0[4 * q + 2], w0[4 * q + 3]);
-            d1[q] = make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
-            if (P2) d2[q] = make_uint4(w2[4 * q], w2[4 * q + 1], w2[4 * q + 2], w2[4 * q + 3]);
+            const int j = 32 * q + 8 * cp;               // op columns c0 + j .. + 7
+            uint32_t w0[4], w1[4], w2[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                split_bf16x3_pair(tile[j + 2 * i][rr], tile[j + 2 * i + 1][rr], w0[i], w1[i], w2[i]);
+            *reinterpret_cast<uint4*>(P0 + o + 32 * q) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+            *reinterpret_cast<uint4*>(P1 + o + 32 * q) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+            if (P2)
+                *reinterpret_cast<uint4*>(P2 + o + 32 * q) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
         }
         __syncthreads();         // the tile is refilled by the next op-row tile
     }
@@ -245,6 +289,53 @@ __global__ void __launch_bounds__(256) split2_transposed(const float* __restrict
                     if (LO) LO[r * ldp + c] = lo;
                 }
             }
+        }
+        __syncthreads();         // the tile is refilled by the next op-row tile
+    }
+    griddep_wait();          // see launch_pdl: complete only after the kernel ahead
+}
+
+// Vectorised TF32 form for full 64 x 64 tiles with 16-byte aligned rows on
+// both sides: each thread loads four float4 along stored rows; then for
+// each of four 16-element parts of an op row, lanes 4i..4i+3 of a warp write
+// its hi (and lo) values as 16-byte stores, 64 contiguous bytes per plane and
+// store.  Tiles at the ragged edges use the kernel above.  Measured on GB300
+// at 8192^2 (an L2 flush before each launch): the kernel above 158 us (5.1
+// TB/s of the 12 bytes an element moves), the row-wise split 142 us.
+__global__ void __launch_bounds__(256) split2_transposed_vec(const float* __restrict__ X, int64_t rows,
+                                                             int64_t cols, int64_t ld,
+                                                             float* __restrict__ HI,
+                                                             float* __restrict__ LO, int64_t ldp,
+                                                             float lo_scale) {
+    griddep_launch_dependents();
+    __shared__ float tile[kT][kT + 1];               // [op col (stored row)][op row]
+    const int tid = threadIdx.x;
+    const int64_t c0 = (int64_t)blockIdx.x * kT;     // op cols  = stored rows
+    for (int64_t rt = blockIdx.y; rt * kT < rows; rt += gridDim.y) {
+        const int64_t r0 = rt * kT;                  // op rows  = stored columns
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int idx = tid + 256 * i;               // 0 .. 1023
+            const int k = idx >> 4, r4 = (idx & 15) * 4;
+            const float4 v = __ldcs(reinterpret_cast<const float4*>(X + (c0 + k) * ld + r0 + r4));
+            tile[k][r4 + 0] = v.x;
+            tile[k][r4 + 1] = v.y;
+            tile[k][r4 + 2] = v.z;
+            tile[k][r4 + 3] = v.w;
+        }
+        __syncthreads();
+        const int rr = tid >> 2, cp = tid & 3;           // op row in tile, 4-element group
+        const int64_t o = (r0 + rr) * ldp + c0 + 4 * cp;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = 16 * q + 4 * cp;               // op columns c0 + j .. + 3
+            float4 h, l;
+            split_tf32x2(tile[j + 0][rr], h.x, l.x, lo_scale);
+            split_tf32x2(tile[j + 1][rr], h.y, l.y, lo_scale);
+            split_tf32x2(tile[j + 2][rr], h.z, l.z, lo_scale);
+            split_tf32x2(tile[j + 3][rr], h.w, l.w, lo_scale);
+            *reinterpret_cast<float4*>(HI + o + 16 * q) = h;
+            if (LO) *reinterpret_cast<float4*>(LO + o + 16 * q) = l;
         }
         __syncthreads();         // the tile is refilled by the next op-row tile
     }
@@ -290,6 +381,37 @@ int grid_for(int64_t work, int threads) {
     return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
+// Blocks of 256 threads of `kern` resident at once on the device (at most
+// 8 per SM), cached per kernel.
+template <typename K>
+int resident_blocks(K kern, std::atomic<int>& cache) {
+    int v = cache.load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    int dev = 0, sms = 148, per = 1;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, 256, 0) != cudaSuccess || per < 1) {
+        cudaGetLastError();
+        per = 1;
+    }
+    v = sms * (per < 8 ? per : 8);
+    cache.store(v, std::memory_order_relaxed);
+    return v;
+}
+
+// Launch a row-wise split kernel over `groups` groups: four groups per
+// thread per step (resident grid) when there are at least four per resident
+// thread, else one (grid_for).
+template <typename K4, typename K1, typename... Args>
+cudaError_t launch_rows(K4 k4, K1 k1, std::atomic<int>& cache4, int64_t groups, cudaStream_t stream,
+                        bool pdl, Args... args) {
+    const int res = resident_blocks(k4, cache4);
+    if (groups >= 4 * (int64_t)res * 256)
+        return launch_pdl(k4, dim3(res), stream, pdl, args...);
+    return launch_pdl(k1, dim3(grid_for(groups, 256)), stream, pdl, args...);
+}
+std::atomic<int> g_res_split3{0}, g_res_split2{0};
+
 }  // namespace
 
 cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int64_t ld, int trans,
@@ -307,8 +429,8 @@ cudaError_t launch_split_bf16x3(const float* X, int64_t rows, int64_t cols, int6
             e = launch_pdl(split3_transposed, grid, stream, pdl, X, rows, cols, ld, P0, P1, P2, ldp);
     } else if (cols % 8 == 0 && ld % 4 == 0 && ldp % 8 == 0 && aligned16(X) && aligned16(P0) &&
                aligned16(P1) && aligned16(P2)) {
-        e = launch_pdl(split3_rows_vec8, dim3(grid_for(rows * (cols / 8), 256)), stream, pdl, X,
-                       rows, cols, ld, P0, P1, P2, ldp);
+        e = launch_rows(split3_rows_vec8<4>, split3_rows_vec8<1>, g_res_split3, rows * (cols / 8),
+                        stream, pdl, X, rows, cols, ld, P0, P1, P2, ldp);
     } else {
         e = launch_pdl(split3_rows_scalar, dim3(grid_for(rows * cols, 256)), stream, pdl, X, rows,
                        cols, ld, P0, P1, P2, ldp);
@@ -323,12 +445,17 @@ cudaError_t launch_split_tf32x2(const float* X, int64_t rows, int64_t cols, int6
     cudaError_t e;
     if (trans) {
         const dim3 grid = transposed_grid(rows, cols);
-        e = launch_pdl(split2_transposed, grid, stream, pdl, X, rows, cols, ld, HI, LO, ldp,
-                       lo_scale);
+        if (rows % kT == 0 && cols % kT == 0 && ld % 4 == 0 && ldp % 4 == 0 && aligned16(X) &&
+            aligned16(HI) && aligned16(LO))
+            e = launch_pdl(split2_transposed_vec, grid, stream, pdl, X, rows, cols, ld, HI, LO, ldp,
+                           lo_scale);
+        else
+            e = launch_pdl(split2_transposed, grid, stream, pdl, X, rows, cols, ld, HI, LO, ldp,
+                           lo_scale);
     } else if (cols % 4 == 0 && ld % 4 == 0 && ldp % 4 == 0 && aligned16(X) && aligned16(HI) &&
                aligned16(LO)) {
-        e = launch_pdl(split2_rows_vec4, dim3(grid_for(rows * (cols / 4), 256)), stream, pdl, X,
-                       rows, cols, ld, HI, LO, ldp, lo_scale);
+        e = launch_rows(split2_rows_vec4<4>, split2_rows_vec4<1>, g_res_split2, rows * (cols / 4),
+                        stream, pdl, X, rows, cols, ld, HI, LO, ldp, lo_scale);
     } else {
         e = launch_pdl(split2_rows_scalar, dim3(grid_for(rows * cols, 256)), stream, pdl, X, rows,
                        cols, ld, HI, LO, ldp, lo_scale);

@@ -104,16 +104,17 @@ def test_square8192_operands(emu):
     A, B, _ = W.generate(g)
     _check_bf16(emu, A)
     _check_bf16(emu, B, trans=True)
+    _check_tf32(emu, B, trans=True)                  # vectorised TF32 transpose
+    _check_tf32_scaled(emu, B, trans=True)
 
 
 @pytest.mark.parametrize("cols", [8, 64])
 def test_transposed_more_op_row_tiles_than_the_grid(emu, cols):
     """op(X) = X^T with more 64-row tiles of op rows than a grid's y extent
     (65535): the transposed kernels loop over the rest.  cols = 64 runs the
-    vectorised kernel (whole tiles), cols = 8 the ragged one and the TF32
-    split; the last tiles are the ones past the first pass."""
+    vectorised kernels (whole tiles), cols = 8 the ragged ones; the last
+    tiles are the ones past the first pass."""
     rows = 65536 * 64 + (64 if cols == 64 else 36)
     X = W.normal(W.rng(12), (cols, rows))              # stored cols x rows: op(X) is rows x cols
     _check_bf16(emu, X, trans=True)
-    if cols == 8:
-        _check_tf32(emu, X, trans=True)
+    _check_tf32(emu, X, trans=True)
