@@ -140,17 +140,20 @@ def test_host_entry_point_pipelined(emu, kind):
     assert np.array_equal(C.view(np.uint32), E.view(np.uint32))
 
 
-@pytest.mark.parametrize("kind,transB", [("a2", 0), ("b1", 1), ("b2", 0)])
-def test_host_entry_point_column_panels(emu, kind, transB):
+@pytest.mark.parametrize("kind,transA,transB", [("a2", 0, 0), ("b1", 0, 1), ("b2", 0, 0),
+                                                ("a2", 1, 0), ("b1", 1, 1)])
+def test_host_entry_point_column_panels(emu, kind, transA, transB):
     """emu_sgemm_host with a wide op(B) (3000 x 2304 x 1900, B 17.5 MB): B's
-    column panels are split into their rows of B's pieces as they land and
-    multiplied by op(A)'s first 2048 rows; the remaining rows then use the
-    whole of B's pieces.  Exact, so bit for bit on every output."""
-    A, B = BC.make(kind, 3000, 2304, 1900, 0, transB, seed=8 + transB)
-    E = BC.exact(A, B, 0, transB).astype(np.float32)
+    column panels are split into their rows (or, B stored K x N, into their
+    columns of B's N-major pieces) as they land and multiplied by op(A)'s
+    first 2048 rows (M-major pieces when A is stored K x M); the remaining
+    rows then use the whole of B's pieces.  Exact, so bit for bit on every
+    output."""
+    A, B = BC.make(kind, 3000, 2304, 1900, transA, transB, seed=8 + transB + 2 * transA)
+    E = BC.exact(A, B, transA, transB).astype(np.float32)
     emu.emu_profile_enable(True)
     try:
-        C = emu.emu_sgemm_host(A, B, transB=bool(transB))
+        C = emu.emu_sgemm_host(A, B, transA=bool(transA), transB=bool(transB))
         launches = emu.emu_profile_read("gemm_tc")[0]
     finally:
         emu.emu_profile_enable(False)
@@ -175,6 +178,21 @@ def test_host_entry_point_n_major_column_panels(emu, kind):
         emu.emu_profile_enable(False)
     assert launches == 3, launches
     assert np.array_equal(C.view(np.uint32), E.view(np.uint32))
+
+
+def test_host_entry_point_n_major_column_panels_bf16x3(emu):
+    """The same panels in BF16x3, which keeps N-major pieces only for deep K
+    (here K = 9300 >= 4 N): with a first-piece A every result is the exact
+    sum of the rung's products, so bit for bit the oracle's BF16x3."""
+    A, B = BC.make("a0", 600, 2304, 9300, 0, 0, seed=13)
+    emu.emu_profile_enable(True)
+    try:
+        C = emu.emu_sgemm_host(A, B, mode="bf16x3")
+        launches = emu.emu_profile_read("gemm_tc")[0]
+    finally:
+        emu.emu_profile_enable(False)
+    assert launches == 3, launches
+    _check_oracle_sample(A, B, 0, 0, C, n=2048, fn=oracle.gemm_bf16x3)
 
 
 LADDER = {"tf32x3": oracle.gemm_tf32x3, "tf32x3_oy": oracle.gemm_tf32x3_oy,
