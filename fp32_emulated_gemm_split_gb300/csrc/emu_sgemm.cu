@@ -367,10 +367,11 @@ struct PieceSet {
 // x 256 (within 0.1 %), and less for deep K (1024^2 x 32768 7 %, the weight
 // gradients 256 x 256, 256 x 1024 and 1024^2 x 1,105,920 6-10 %: a tile's K
 // rows of 512 bytes follow each other in memory, where K-major rows millions
-// of elements long do not).  BF16x3, whose tile loads bound it, only when K
-// is at least 4 times the operand's M (or N): at 8192^3 N-major pieces cost
-// it 4.75 % (a K-major box row's L2 fetch, promoted to 256 bytes, brings the
-// next K block's bytes along).  TF32 pieces stay K-major.  The rule depends
+// of elements long do not).  BF16x3 only when K is at least 4 times the
+// operand's M (or N): at 8192^3 N-major pieces cost it 4-5 % with the same
+// L2 and DRAM traffic and less tensor-pipe activity (75.9 against 72.5 % at
+// 4096^3), which an L2 prefetch of the next K block did not change.  TF32
+// pieces stay K-major.  The rule depends
 // on K and the operand's own extent only, so a row chunk of op(A) never
 // changes B's layout.
 inline bool mn_pieces(int mode, bool k_is_row, int64_t K, int64_t extent) {
