@@ -231,6 +231,24 @@ def test_square8192_sampled(emu, mode):
     assert ratio <= 1.0 and relf <= checks.FROBENIUS_TOL, (ratio, relf)
 
 
+def test_square8192_n_major_b_same_bits_as_k_major(emu):
+    """The benchmark's configuration (8192^3, B stored K x N, which BF16x9
+    reads as N-major pieces) gives the same bits as the same product with B
+    stored N x K (K-major pieces), on every output; the sampled check above
+    holds it to the oracle."""
+    import torch
+    g = W.WORKLOADS["square8192_normal"]
+    A, B, _ = W.generate(g)
+    dA = to_dev(A)
+    C1 = torch.empty((g.M, g.N), device="cuda")
+    C2 = torch.empty((g.M, g.N), device="cuda")
+    emu.emu_sgemm(dA, to_dev(B), C1)
+    emu.emu_sgemm(dA, to_dev(np.ascontiguousarray(B.T)), C2, transB=True)
+    torch.cuda.synchronize()
+    assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
+    assert torch.isfinite(C1).all()
+
+
 def test_bf16x9_at_least_as_accurate_as_fp32_at_long_k(emu):
     """The pages: BF16x9 matches or beats native FP32 against an FP64
     reference -- here at K = 8192, where accumulation error dominates."""
