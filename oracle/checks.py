@@ -6,12 +6,15 @@ Interatomic Potentials", section "Limitations and decision criteria"); the
 criteria below make that concrete:
 
 * element-wise, with u = 2^-24 (unit roundoff of FP32):
-      |C - C_ref| <= (2K + 2) u |alpha| S_abs + 2 u |beta C0| + (9K + 4) 2^-149
+      |C - C_ref| <= (2K + 2) u |alpha| S_abs + 2 u |beta C0|
+                     + ((9K + 4) |alpha| + 2) 2^-149
   where S_abs = sum_k |a_mk||b_kn|.  2K u |alpha| S_abs is the worst case of a
   K-term FP32 accumulation (one rounding per step, each at most u times the
   running magnitude); the 2u terms cover the two roundings of the epilogue
   alpha*acc + beta*C0; the last term covers products and partial sums that
-  land among FP32 subnormals (absolute spacing 2^-149).
+  land among FP32 subnormals (absolute spacing 2^-149): those roundings
+  happen in the accumulator, which the epilogue then multiplies by alpha,
+  and the epilogue's own roundings of a subnormal result add up to 2^-149.
 * TF32x3 drops the residual*residual product and its residual is itself
   rounded to TF32, which costs at most 3 * 2^-22 |a||b| < 2^-20 |a||b| per
   product, so its bound adds 2^-20 |alpha| S_abs.  The cheaper rungs (two
@@ -78,7 +81,7 @@ def elementwise_bound(K, alpha, beta, Sabs, C0=None, mode="bf16x9", S1=None):
         b = b + 2 * U * abs(float(beta)) * np.abs(np.asarray(C0, np.float64))
     if S1 is not None and MODE_SUB_ABS[mode] > 0.0:
         b = b + MODE_SUB_ABS[mode] * (1 + 2.0 ** -10) * abs(float(alpha)) * np.asarray(S1, np.float64)
-    return b + (9 * K + 4) * SUB
+    return b + ((9 * K + 4) * abs(float(alpha)) + 2) * SUB
 
 
 def error_ratio(C, Cref, Sabs, K, alpha, beta, C0=None, mode="bf16x9", S1=None):

@@ -438,6 +438,25 @@ def test_split_errors_below_the_normal_range_match_their_bounds():
         assert err[mode][: 1 << 16].max() > e / 2, mode          # attained on subnormals
 
 
+def test_subnormal_partial_sums_are_scaled_by_alpha():
+    """A product among FP32 subnormals keeps only a few bits in the FP32
+    accumulator (spacing 2^-149), and the epilogue multiplies that error by
+    alpha.  K = 1, a = 1.2345 * 2^-72, b = 1.4567 * 2^-72 (normal; a b about
+    57.5 * 2^-149), alpha = 2^17: the oracle's BF16x9 misses the FP64 result
+    by about 0.46 * 2^-132, over ten times the subnormal term taken in the
+    result's units, and within it taken in the accumulator's (times
+    |alpha|)."""
+    a = np.array([[1.2345 * 2.0 ** -72]], np.float32)
+    b = np.array([[1.4567 * 2.0 ** -72]], np.float32)
+    alpha = 2.0 ** 17
+    Cref, Sabs = oracle.gemm_ref(a, b, alpha=alpha)
+    C = oracle.gemm_bf16x9(a, b, alpha=alpha)
+    err = abs(float(C[0, 0]) - float(Cref[0, 0]))
+    unscaled = 4 * 2.0 ** -24 * alpha * float(Sabs[0, 0]) + 13 * 2.0 ** -149
+    assert err > 10 * unscaled
+    assert checks.error_ratio(C, Cref, Sabs, 1, alpha, 0.0) <= 1.0
+
+
 def test_subnormal_operands_need_the_absolute_term():
     """K = 1, a a subnormal that TF32 cannot hold to the last bit, b = 1.5 *
     2^30: the oracle's TF32x3 product misses by about 2^-137 * 2^30, far
