@@ -532,6 +532,37 @@ def test_subnormal_operands_through_the_tensor_core(emu, mode):
             assert np.array_equal(C.view(np.uint32), u)
 
 
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3", "tf32x3_oy", "bf16x3", "tf32"])
+def test_subnormal_operand_products_within_the_tensor_core_term(emu, mode):
+    """K = 1, so every output is one product a b: 4096 values of a with
+    exponents spread over 2^-149 .. 2^-100 (FP32 subnormals below 2^-126)
+    times 64 normal b.  BF16x9 keeps a's bits in its pieces, but products
+    with a subnormal a come out up to tens of ulps off (the tensor core's
+    truncating, scaled accumulation), while from 2^-126 up they stay within
+    two ulps (one truncation and the final rounding).  Every mode meets the element-wise bound with the operands'
+    absolute term (MODE_SUB_ABS + TC_SUB_ABS), and for BF16x9 some product
+    exceeds the bound without TC_SUB_ABS: the term is needed."""
+    r = np.random.default_rng(5)
+    M, N = 4096, 64
+    e = r.uniform(-149, -100, M)
+    a = (np.exp2(e) * r.choice([-1, 1], M)).astype(np.float32).reshape(M, 1)
+    b = (r.uniform(1, 2, N) * np.exp2(r.integers(-20, 21, N)) *
+         r.choice([-1, 1], N)).astype(np.float32).reshape(1, N)
+    C = _run(emu, a, b, mode=mode)
+    Cref, Sabs = oracle.gemm_ref(a, b)
+    S1 = checks.operand_l1(a, b)
+    bmode = mode if mode in checks.MODE_EXTRA else "bf16x9"
+    assert checks.error_ratio(C, Cref, Sabs, 1, 1.0, 0.0, mode=bmode, S1=S1) <= 1.0
+    if mode == "bf16x9":
+        err = np.abs(C.astype(np.float64) - Cref)
+        normal = np.abs(a[:, 0]) >= 2.0 ** -126
+        ulp = np.maximum(np.exp2(np.floor(np.log2(np.abs(Cref))) - 23), 2.0 ** -149)
+        assert np.all(err[normal] <= 2 * ulp[normal])
+        without = (checks.elementwise_bound(1, 1.0, 0.0, Sabs, mode="bf16x9") +
+                   checks.MODE_SUB_ABS["bf16x9"] * S1)
+        assert np.any(err > without)
+
+
 @pytest.mark.parametrize("shape", [(256, 256, 4096), (1024, 1024, 1024), (300, 513, 1000),
                                    (4096, 4096, 512)],
                          ids=lambda s: "x".join(map(str, s)))
